@@ -1,0 +1,260 @@
+"""The oracle: a plain fp64 CPU restatement of multi-round LSH attention.
+
+TEST INFRASTRUCTURE ONLY.  Only the test suite, ``__graft_entry__.smoke()`` and
+the benchmark's CPU-baseline leg import this package.  The CUDA library never
+imports, links or calls it, and it shares no code with the library.
+
+The arithmetic lives in ``lsh_oracle.c`` (plain C, fp64, compiled here with
+gcc on first use).  This module only marshals numpy arrays into it.
+
+Each function follows the Reformer pages:
+  * hash     -- angular LSH, bucket = first argmax of [xR, -xR]
+                ("Reformer" glossary, ultralytics.com, section "Atencion LSH";
+                 modulabs-hub Reformer notes, "Locality sensitive hashing")
+  * sort     -- order tokens by (bucket, position)
+                (ai-scholar.tech Reformer article, "LSH attention")
+  * attend   -- own chunk + previous chunk, same bucket, causal, self only
+                when nothing else is left (modulabs-hub notes, "LSH attention")
+  * combine  -- un-sort and logsumexp-weighted sum of rounds
+  * forward  -- all of the above for B*H heads
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "lsh_oracle.c")
+_LIB = os.path.join(_HERE, "liblsh_oracle.so")
+_lock = threading.Lock()
+_default = None
+
+SELF_LOGIT = -1.0e5
+
+
+def compile_source(src_path: str, lib_path: str) -> str:
+    """Compile one C source into a shared library (IEEE fp64, no fast-math)."""
+    tmp = lib_path + ".tmp%d" % os.getpid()
+    subprocess.check_call(
+        ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+         "-o", tmp, src_path, "-lm", "-lpthread"])
+    os.replace(tmp, lib_path)
+    return lib_path
+
+
+def build(force: bool = False) -> str:
+    """Compile lsh_oracle.c into liblsh_oracle.so when missing or stale."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        compile_source(_SRC, _LIB)
+    return _LIB
+
+
+def _f64(a):
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _i32(a):
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+class Oracle:
+    """numpy front end of one compiled copy of the oracle's C code."""
+
+    def __init__(self, lib_path: str):
+        lib = ctypes.CDLL(lib_path)
+        P = ctypes.c_void_p
+        i32, i64, f64 = ctypes.c_int, ctypes.c_long, ctypes.c_double
+        lib.oracle_hash.argtypes = [P, i64, i32, P, i32, P, P]
+        lib.oracle_hash.restype = None
+        lib.oracle_sort.argtypes = [P, i32, i32, P, P, P]
+        lib.oracle_sort.restype = None
+        lib.oracle_inv_norm.argtypes = [P, i32, i32, P]
+        lib.oracle_inv_norm.restype = None
+        lib.oracle_attend.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, P, i32, P, P]
+        lib.oracle_attend.restype = None
+        lib.oracle_combine.argtypes = [P, P, P, i32, i32, i32, P, i32, P, P]
+        lib.oracle_combine.restype = None
+        lib.oracle_forward.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, i32,
+                                       f64, i32] + [P] * 9
+        lib.oracle_forward.restype = ctypes.c_int
+        lib.oracle_self_logit.argtypes = []
+        lib.oracle_self_logit.restype = f64
+        self.lib = lib
+        self.SELF_LOGIT = lib.oracle_self_logit()
+
+    def hash(self, x, R_r, n_buckets):
+        """Buckets and top-1/top-2 margins of rows x [n, d] under one round R_r [d, nb/2]."""
+        lib = self.lib
+        x = _f64(x)
+        R_r = _f64(R_r)
+        n, d = x.shape
+        assert R_r.shape == (d, n_buckets // 2)
+        bucket = np.empty(n, np.int32)
+        margin = np.empty(n, np.float64)
+        lib.oracle_hash(_p(x), n, d, _p(R_r), n_buckets, _p(bucket), _p(margin))
+        return bucket, margin
+
+    def hash_rounds(self, x, R, n_buckets):
+        """Buckets [n_rounds, n] and margins for every round of R [n_rounds, d, nb/2]."""
+        R = _f64(R)
+        out_b = np.empty((R.shape[0], len(x)), np.int32)
+        out_m = np.empty((R.shape[0], len(x)), np.float64)
+        for r in range(R.shape[0]):
+            out_b[r], out_m[r] = self.hash(x, R[r], n_buckets)
+        return out_b, out_m
+
+    def sort(self, bucket, n_buckets):
+        """perm (sorted -> original), inv (original -> sorted), bstart [nb+1] of one segment."""
+        lib = self.lib
+        bucket = _i32(bucket)
+        L = bucket.shape[0]
+        perm = np.empty(L, np.int32)
+        inv = np.empty(L, np.int32)
+        bstart = np.empty(n_buckets + 1, np.int32)
+        lib.oracle_sort(_p(bucket), L, n_buckets, _p(perm), _p(inv), _p(bstart))
+        return perm, inv, bstart
+
+    def inv_norm(self, qk):
+        lib = self.lib
+        qk = _f64(qk)
+        L, d = qk.shape
+        out = np.empty(L, np.float64)
+        lib.oracle_inv_norm(_p(qk), L, d, _p(out))
+        return out
+
+    def attend(self, qk, v, bucket, perm, chunk, causal, scale, rows=None):
+        """One round of chunked attention for one head.
+
+        Returns (o, lse) in SORTED order: o [L, d], lse [L].  When ``rows`` (sorted
+        indices) is given, only those rows are computed and returned, in that order.
+        """
+        lib = self.lib
+        qk = _f64(qk)
+        v = _f64(v)
+        bucket = _i32(bucket)
+        perm = _i32(perm)
+        L, d = qk.shape
+        inorm = self.inv_norm(qk)
+        o = np.zeros((L, d), np.float64)
+        lse = np.zeros(L, np.float64)
+        if rows is None:
+            lib.oracle_attend(_p(qk), _p(v), _p(inorm), _p(bucket), _p(perm), L, d, chunk,
+                              int(causal), float(scale), None, 0, _p(o), _p(lse))
+            return o, lse
+        rows = _i32(rows)
+        lib.oracle_attend(_p(qk), _p(v), _p(inorm), _p(bucket), _p(perm), L, d, chunk,
+                          int(causal), float(scale), _p(rows), len(rows), _p(o), _p(lse))
+        return o[rows], lse[rows]
+
+    def combine(self, o_r, lse_r, inv, tokens=None):
+        """Un-sort and combine rounds of one head.
+
+        o_r [R, L, d] and lse_r [R, L] are in sorted order, inv [R, L].  Returns
+        (out [n, d], lse [n]) for ``tokens`` (original positions; all when None).
+        """
+        lib = self.lib
+        o_r = _f64(o_r)
+        lse_r = _f64(lse_r)
+        inv = _i32(inv)
+        R, L, d = o_r.shape
+        if tokens is None:
+            out = np.empty((L, d), np.float64)
+            lse = np.empty(L, np.float64)
+            lib.oracle_combine(_p(o_r), _p(lse_r), _p(inv), R, L, d, None, 0, _p(out), _p(lse))
+            return out, lse
+        tokens = _i32(tokens)
+        out = np.empty((len(tokens), d), np.float64)
+        lse = np.empty(len(tokens), np.float64)
+        lib.oracle_combine(_p(o_r), _p(lse_r), _p(inv), R, L, d, _p(tokens), len(tokens),
+                           _p(out), _p(lse))
+        return out, lse
+
+    def forward(self, qk, v, R, n_buckets, chunk, causal, scale, threads=None, intermediates=False):
+        """Full forward pass.  qk, v: [B, H, L, d] (or [n_heads, L, d]); R [n_rounds, d, nb/2].
+
+        Returns (out [..., L, d], lse [..., L]) and, with ``intermediates``, a dict
+        with bucket, perm, inv, bstart, margin, o_r, lse_r (per head and round).
+        """
+        lib = self.lib
+        shape = qk.shape
+        L, d = shape[-2], shape[-1]
+        n_heads = int(np.prod(shape[:-2]))
+        qk = _f64(qk).reshape(n_heads, L, d)
+        v = _f64(v).reshape(n_heads, L, d)
+        R = _f64(R)
+        n_rounds = R.shape[0]
+        assert R.shape == (n_rounds, d, n_buckets // 2)
+        if threads is None:
+            threads = os.cpu_count() or 1
+        out = np.empty((n_heads, L, d), np.float64)
+        lse = np.empty((n_heads, L), np.float64)
+        inter = None
+        if intermediates:
+            inter = dict(
+                bucket=np.empty((n_heads, n_rounds, L), np.int32),
+                perm=np.empty((n_heads, n_rounds, L), np.int32),
+                inv=np.empty((n_heads, n_rounds, L), np.int32),
+                bstart=np.empty((n_heads, n_rounds, n_buckets + 1), np.int32),
+                margin=np.empty((n_heads, n_rounds, L), np.float64),
+                o_r=np.empty((n_heads, n_rounds, L, d), np.float64),
+                lse_r=np.empty((n_heads, n_rounds, L), np.float64),
+            )
+        g = (lambda k: _p(inter[k])) if inter else (lambda k: None)
+        rc = lib.oracle_forward(_p(qk), _p(v), _p(R), n_heads, L, d, n_buckets, n_rounds, chunk,
+                                int(causal), float(scale), int(threads), _p(out), _p(lse),
+                                g("bucket"), g("perm"), g("inv"), g("bstart"), g("margin"),
+                                g("o_r"), g("lse_r"))
+        if rc != 0:
+            raise MemoryError("oracle_forward ran out of host memory")
+        out = out.reshape(shape)
+        lse = lse.reshape(shape[:-1])
+        if intermediates:
+            lead = shape[:-2]
+            inter = {k: a.reshape(lead + a.shape[1:]) for k, a in inter.items()}
+            return out, lse, inter
+        return out, lse
+
+
+def default() -> Oracle:
+    """The oracle compiled from lsh_oracle.c (built on first use)."""
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle(build())
+    return _default
+
+
+def hash(x, R_r, n_buckets):
+    return default().hash(x, R_r, n_buckets)
+
+
+def hash_rounds(x, R, n_buckets):
+    return default().hash_rounds(x, R, n_buckets)
+
+
+def sort(bucket, n_buckets):
+    return default().sort(bucket, n_buckets)
+
+
+def inv_norm(qk):
+    return default().inv_norm(qk)
+
+
+def attend(qk, v, bucket, perm, chunk, causal, scale, rows=None):
+    return default().attend(qk, v, bucket, perm, chunk, causal, scale, rows)
+
+
+def combine(o_r, lse_r, inv, tokens=None):
+    return default().combine(o_r, lse_r, inv, tokens)
+
+
+def forward(qk, v, R, n_buckets, chunk, causal, scale, threads=None, intermediates=False):
+    return default().forward(qk, v, R, n_buckets, chunk, causal, scale, threads, intermediates)

@@ -1,0 +1,379 @@
+"""Pins: facts fixed by the Reformer pages or by mathematics that the oracle must meet.
+
+Each ``pin_*`` takes an oracle front end (``oracle.Oracle``) and raises
+AssertionError when the oracle disagrees.  The checks never re-type the
+oracle's own formulas: they use printed values (``golden/``), closed forms,
+invariants, special cases that reduce to a library routine (numpy argmax and
+stable argsort, torch's scaled_dot_product_attention), and brute force on tiny
+inputs.  ``test_oracle_pins.py`` runs them on the real oracle and
+``test_oracle_mutants.py`` runs them on copies with planted mistakes.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+# --------------------------------------------------------------------------
+# Hashing
+# --------------------------------------------------------------------------
+
+def pin_hash_is_first_argmax_of_concat(orc):
+    """Bucket = first argmax of [xR, -xR] (glossary "Atencion LSH"); numpy's argmax returns
+    the first maximal index, and the margin is top-1 minus top-2 of that vector."""
+    rng = _rng(1)
+    for d, nb in ((8, 2), (16, 8), (64, 32), (128, 96)):
+        x = rng.standard_normal((200, d))
+        R = rng.standard_normal((d, nb // 2))
+        b, m = orc.hash(x, R, nb)
+        p = x @ R
+        cat = np.concatenate([p, -p], axis=1)
+        assert np.array_equal(b, np.argmax(cat, axis=1)), (d, nb)
+        srt = np.sort(cat, axis=1)
+        assert np.allclose(m, srt[:, -1] - srt[:, -2], rtol=1e-12, atol=1e-12)
+
+
+def pin_hash_simhash_closed_form(orc):
+    """With 2 buckets the hash is the sign of one random projection (SimHash): two vectors at
+    angle theta share a bucket with probability 1 - theta/pi.  Monte Carlo, 4 sigma."""
+    rng = _rng(2)
+    d, n = 16, 20000
+    R = rng.standard_normal((n, d, 1))
+    e0 = np.zeros(d); e0[0] = 1.0
+    for theta in (math.pi / 6, math.pi / 3, math.pi / 2, 2 * math.pi / 3):
+        e1 = np.zeros(d); e1[0] = math.cos(theta); e1[1] = math.sin(theta)
+        b, _ = orc.hash_rounds(np.stack([e0, e1]), R, 2)
+        same = float(np.mean(b[:, 0] == b[:, 1]))
+        p = 1.0 - theta / math.pi
+        sigma = math.sqrt(p * (1 - p) / n)
+        assert abs(same - p) < 4 * sigma + 1e-9, (theta, same, p)
+
+
+def pin_hash_pages_bucket_sharing_statistic(orc):
+    """The glossary's worked example: dim 64, 16 buckets, 1000 rounds; a vector near the
+    query (cos 0.96) shares its bucket in 72 % of rounds, an unrelated one (cos 0.04) in 9 %.
+    Checked in distribution over our own seeds (tolerance band from the fixture)."""
+    with open(os.path.join(GOLDEN, "bucket_sharing.json")) as f:
+        g = json.load(f)
+    s, band = g["setup"], g["band"]
+    near_rates, far_rates = [], []
+    for seed in range(band["seeds"]):
+        rng = _rng(10_000 + seed)
+        q = rng.standard_normal(s["dim"])
+        near = q + 0.3 * rng.standard_normal(s["dim"])
+        far = rng.standard_normal(s["dim"])
+        R = rng.standard_normal((s["rounds"], s["dim"], s["n_buckets"] // 2))
+        b, _ = orc.hash_rounds(np.stack([q, near, far]), R, s["n_buckets"])
+        near_rates.append(np.mean(b[:, 1] == b[:, 0]))
+        far_rates.append(np.mean(b[:, 2] == b[:, 0]))
+        assert near_rates[-1] > far_rates[-1], seed
+    pn, pf = g["printed"]["near"]["shared_fraction"], g["printed"]["far"]["shared_fraction"]
+    assert abs(np.mean(near_rates) - pn) <= band["near_tolerance"], np.mean(near_rates)
+    assert abs(np.mean(far_rates) - pf) <= band["far_tolerance"], np.mean(far_rates)
+
+
+def pin_hash_positive_rescaling(orc):
+    """hash(a x) = hash(x) for a > 0: exactly for powers of two (exact scaling in binary
+    floating point), and outside a relative near-tie band for other factors."""
+    rng = _rng(3)
+    x = rng.standard_normal((300, 32))
+    R = rng.standard_normal((32, 16))
+    b0, m0 = orc.hash(x, R, 32)
+    for k in (-6, -1, 1, 5):
+        b, _ = orc.hash(x * 2.0 ** k, R, 32)
+        assert np.array_equal(b, b0), k
+    for a in (0.37, 3.3, 1234.5):
+        b, _ = orc.hash(x * a, R, 32)
+        safe = m0 > 1e-9 * np.linalg.norm(x, axis=1) * np.linalg.norm(R, axis=0).max()
+        assert np.array_equal(b[safe], b0[safe]), a
+
+
+def pin_hash_zero_rotation(orc):
+    """R = 0 makes every entry of [xR, -xR] zero; the first index wins: bucket 0."""
+    rng = _rng(4)
+    b, m = orc.hash(rng.standard_normal((50, 16)), np.zeros((16, 8)), 16)
+    assert np.all(b == 0) and np.all(m == 0)
+
+
+def pin_hash_antipodal_and_relabel(orc):
+    """hash(-x) = hash(x) + nb/2 (mod nb), and permuting R's columns by pi relabels the
+    bucket j -> pi^-1(j) in each half (symmetry of the [p, -p] construction)."""
+    rng = _rng(5)
+    d, nb = 32, 24
+    half = nb // 2
+    x = rng.standard_normal((400, d))
+    R = rng.standard_normal((d, half))
+    b, m = orc.hash(x, R, nb)
+    bn, _ = orc.hash(-x, R, nb)
+    ok = m > 0
+    assert np.array_equal(bn[ok], (b[ok] + half) % nb)
+    pi = rng.permutation(half)
+    bp, _ = orc.hash(x, R[:, pi], nb)
+    inv_pi = np.argsort(pi)
+    expect = np.where(b < half, inv_pi[b % half], half + inv_pi[b % half])
+    assert np.array_equal(bp[ok], expect[ok])
+
+
+# --------------------------------------------------------------------------
+# Sorting
+# --------------------------------------------------------------------------
+
+def pin_sort_stable_by_bucket(orc):
+    """perm orders positions by (bucket, position): it is a bijection, inv is its inverse,
+    it equals numpy's stable argsort, and bstart is the running count of smaller buckets."""
+    rng = _rng(6)
+    for L, nb in ((1, 4), (17, 2), (1000, 32), (4096, 1024), (3000, 7)):
+        bucket = rng.integers(0, nb, size=L).astype(np.int32)
+        if L > 50:
+            bucket[: L // 3] = rng.integers(0, 2, size=L // 3)   # heavy buckets
+        perm, inv, bstart = orc.sort(bucket, nb)
+        assert np.array_equal(np.sort(perm), np.arange(L))
+        assert np.array_equal(inv[perm], np.arange(L))
+        assert np.array_equal(perm, np.argsort(bucket, kind="stable"))
+        sb = bucket[perm]
+        assert np.all(np.diff(sb) >= 0)
+        same = np.diff(sb) == 0
+        assert np.all(np.diff(perm)[same] > 0)
+        counts = np.bincount(bucket, minlength=nb)
+        assert np.array_equal(bstart, np.concatenate([[0], np.cumsum(counts)]))
+
+
+# --------------------------------------------------------------------------
+# Attention
+# --------------------------------------------------------------------------
+
+def _sdpa(qk, v, allowed, scale):
+    """Shared-QK softmax attention with unit-norm keys through torch's SDPA (fp64).
+
+    Returns (out, lse) with lse from torch.logsumexp of the same masked scores."""
+    q = torch.from_numpy(qk)
+    k = q / q.norm(dim=-1, keepdim=True)
+    m = torch.from_numpy(allowed)
+    out = torch.nn.functional.scaled_dot_product_attention(
+        q[None], k[None], torch.from_numpy(v)[None], attn_mask=m[None], scale=scale)[0]
+    s = (q @ k.T) * scale
+    s = s.masked_fill(~m, float("-inf"))
+    return out.numpy(), torch.logsumexp(s, dim=-1).numpy()
+
+
+def _self_masked(allowed_with_self):
+    """Remove the diagonal except in rows where it is the only allowed entry."""
+    a = allowed_with_self.copy()
+    L = a.shape[0]
+    diag = np.eye(L, dtype=bool)
+    only_self = (a & ~diag).sum(1) == 0
+    a &= ~diag
+    a[only_self, np.arange(L)[only_self]] = True
+    return a, only_self
+
+
+def _check_rows(orc, out, lse, ref_out, ref_lse, only_self, n_rounds, v):
+    assert np.allclose(out[~only_self], ref_out[~only_self], rtol=1e-10, atol=1e-10)
+    assert np.allclose(lse[~only_self], ref_lse[~only_self], rtol=1e-10, atol=1e-10)
+    if n_rounds == 1:
+        assert np.array_equal(out[only_self], v[only_self])
+    assert np.allclose(out[only_self], v[only_self], rtol=0, atol=1e-9)
+    assert np.allclose(lse[only_self], orc.SELF_LOGIT + math.log(n_rounds), rtol=0, atol=1e-9)
+
+
+def pin_attention_one_bucket_one_chunk_is_full_attention(orc):
+    """With one bucket (R = 0) and one chunk covering the sequence, LSH attention is full
+    shared-QK softmax attention with the self-mask, causal or not (library SDPA)."""
+    rng = _rng(7)
+    L, d = 24, 16
+    qk = rng.standard_normal((L, d))
+    v = rng.standard_normal((L, d))
+    for causal in (False, True):
+        for n_rounds, scale in ((1, 0.25), (2, 1.0)):
+            R = np.zeros((n_rounds, d, 4))
+            out, lse = orc.forward(qk[None], v[None], R, 8, L, causal, scale)
+            allowed = np.tril(np.ones((L, L), bool)) if causal else np.ones((L, L), bool)
+            allowed, only_self = _self_masked(allowed)
+            ref_out, ref_lse = _sdpa(qk, v, allowed, scale)
+            _check_rows(orc, out[0], lse[0], ref_out, ref_lse + math.log(n_rounds),
+                        only_self, n_rounds, v)
+
+
+def pin_attention_one_bucket_is_local_lookback_window(orc):
+    """With one bucket, sorting is the identity and the method reduces to local attention
+    over the own and previous chunk (glossary "Atencion LSH"), no look-ahead, no wrap."""
+    rng = _rng(8)
+    L, d, c = 40, 8, 8
+    qk = rng.standard_normal((L, d))
+    v = rng.standard_normal((L, d))
+    idx = np.arange(L)
+    kq, kk = (idx // c)[:, None], (idx // c)[None, :]
+    window = (kk == kq) | (kk == kq - 1)
+    for causal in (False, True):
+        allowed = window & (idx[None, :] <= idx[:, None]) if causal else window
+        allowed, only_self = _self_masked(allowed)
+        out, lse = orc.forward(qk[None], v[None], np.zeros((1, d, 2)), 4, c, causal, 0.7)
+        ref_out, ref_lse = _sdpa(qk, v, allowed, 0.7)
+        _check_rows(orc, out[0], lse[0], ref_out, ref_lse, only_self, 1, v)
+
+
+def pin_attention_single_candidate_rows(orc):
+    """A row with one candidate copies that value exactly; the causal first token has no
+    candidate and gets its own value with lse = self logit + ln(rounds)."""
+    rng = _rng(9)
+    L, d = 16, 8
+    qk = rng.standard_normal((L, d))
+    v = rng.standard_normal((L, d))
+    for n_rounds in (1, 3):
+        out, lse = orc.forward(qk[None], v[None], np.zeros((n_rounds, d, 1)), 2, 4, True, 0.5)
+        if n_rounds == 1:
+            assert np.array_equal(out[0, 0], v[0]) and np.array_equal(out[0, 1], v[0])
+        assert np.allclose(out[0, 0], v[0], rtol=0, atol=1e-9)
+        assert abs(lse[0, 0] - (orc.SELF_LOGIT + math.log(n_rounds))) < 1e-9
+        assert np.allclose(out[0, 1], v[0], rtol=0, atol=1e-12)
+
+
+def pin_attention_zero_scale_is_candidate_mean(orc):
+    """scale = 0 gives equal weights: every row is the plain mean of its candidates'
+    values, and lse_r = ln(count); the candidate sets are enumerated by brute force."""
+    rng = _rng(10)
+    L, d, nb, c = 48, 8, 6, 8
+    qk = rng.standard_normal((L, d))
+    v = rng.standard_normal((L, d))
+    R = rng.standard_normal((1, d, nb // 2))
+    for causal in (False, True):
+        out, lse, it = orc.forward(qk[None], v[None], R, nb, c, causal, 0.0, intermediates=True)
+        bucket = it["bucket"][0, 0]
+        for i in range(L):
+            cands = _brute_candidates(bucket, i, c, causal)
+            if cands:
+                assert np.allclose(out[0, i], v[cands].mean(0), rtol=1e-12, atol=1e-12)
+                assert abs(lse[0, i] - math.log(len(cands))) < 1e-12
+            else:
+                assert np.array_equal(out[0, i], v[i])
+
+
+def _brute_candidates(bucket, i, c, causal):
+    """Candidates of token i straight from the definition: rank tokens by (bucket, pos)."""
+    order = sorted(range(len(bucket)), key=lambda t: (bucket[t], t))
+    s = order.index(i)
+    k = s // c
+    out = []
+    for t in range(max(0, (k - 1) * c), min(len(bucket), (k + 1) * c)):
+        j = order[t]
+        if j == i or bucket[j] != bucket[i] or (causal and j >= i):
+            continue
+        out.append(j)
+    return out
+
+
+def pin_attention_brute_force_tiny(orc):
+    """For L <= 16, several buckets and rounds: candidate sets enumerated from the definition,
+    softmax and round combination evaluated directly with numpy, match the oracle."""
+    rng = _rng(11)
+    for L, d, nb, c, n_rounds in ((16, 4, 4, 4, 2), (12, 8, 2, 2, 3), (16, 4, 8, 8, 1)):
+        for causal in (False, True):
+            qk = rng.standard_normal((L, d))
+            v = rng.standard_normal((L, d))
+            R = rng.standard_normal((n_rounds, d, nb // 2))
+            scale = 0.8
+            out, lse, it = orc.forward(qk[None], v[None], R, nb, c, causal, scale,
+                                       intermediates=True)
+            kn = qk / np.linalg.norm(qk, axis=1, keepdims=True)
+            for i in range(L):
+                ls, os_ = [], []
+                for r in range(n_rounds):
+                    p = qk[i] @ R[r]
+                    bucket = np.argmax(np.concatenate([qk @ R[r], -(qk @ R[r])], 1), 1)
+                    assert bucket[i] == np.argmax(np.concatenate([p, -p]))
+                    cands = _brute_candidates(bucket, i, c, causal)
+                    if not cands:
+                        ls.append(orc.SELF_LOGIT); os_.append(v[i]); continue
+                    sc = scale * (kn[cands] @ qk[i])
+                    w = np.exp(sc - sc.max())
+                    ls.append(sc.max() + math.log(w.sum()))
+                    os_.append((w[:, None] * v[cands]).sum(0) / w.sum())
+                ls = np.array(ls)
+                W = np.exp(ls - ls.max())
+                ref_lse = ls.max() + math.log(W.sum())
+                ref = (W[:, None] * np.array(os_)).sum(0) / W.sum()
+                assert np.allclose(out[0, i], ref, rtol=1e-10, atol=1e-10), (L, i, causal)
+                assert abs(lse[0, i] - ref_lse) < 1e-9
+
+
+# --------------------------------------------------------------------------
+# Round combination
+# --------------------------------------------------------------------------
+
+def pin_combine_identical_rounds(orc):
+    """Equal rotations in every round give the single-round output, and the combined lse is
+    the single-round lse plus ln(rounds)."""
+    rng = _rng(12)
+    L, d, nb, c = 64, 8, 8, 8
+    qk = rng.standard_normal((2, L, d))
+    v = rng.standard_normal((2, L, d))
+    R1 = rng.standard_normal((1, d, nb // 2))
+    o1, l1 = orc.forward(qk, v, R1, nb, c, True, 0.6)
+    for n in (2, 5):
+        on, ln = orc.forward(qk, v, np.repeat(R1, n, 0), nb, c, True, 0.6)
+        assert np.allclose(on, o1, rtol=1e-9, atol=1e-9)
+        assert np.allclose(ln, l1 + math.log(n), rtol=0, atol=1e-9)
+
+
+def pin_combine_one_round_is_unsort(orc):
+    """With one round the combination is the identity: out is the sorted-order output moved
+    back to original order (numpy fancy indexing by inv)."""
+    rng = _rng(13)
+    L, d, nb, c = 64, 8, 8, 8
+    qk = rng.standard_normal((1, L, d))
+    v = rng.standard_normal((1, L, d))
+    R = rng.standard_normal((1, d, nb // 2))
+    out, lse, it = orc.forward(qk, v, R, nb, c, False, 0.9, intermediates=True)
+    inv = it["inv"][0, 0]
+    assert not np.array_equal(inv, np.arange(L))
+    assert np.array_equal(out[0], it["o_r"][0, 0][inv])
+    assert np.array_equal(lse[0], it["lse_r"][0, 0][inv])
+
+
+def pin_combine_closed_form_two_rounds(orc):
+    """Two rounds with given per-round (o, lse): out = (e^l1 o1 + e^l2 o2) / (e^l1 + e^l2),
+    lse = ln(e^l1 + e^l2); includes a self-only round (lse = -1e5) that must get ~0 weight."""
+    rng = _rng(14)
+    L, d = 5, 3
+    o = rng.standard_normal((2, L, d))
+    l = np.array([[0.3, 2.0, -1.0, 5.0, 0.0], [1.1, -4.0, -1e5, 5.0, 0.0]])
+    inv = np.stack([rng.permutation(L), rng.permutation(L)]).astype(np.int32)
+    out, lse = orc.combine(o, l, inv)
+    for i in range(L):
+        l1, l2 = l[0, inv[0, i]], l[1, inv[1, i]]
+        o1, o2 = o[0, inv[0, i]], o[1, inv[1, i]]
+        e1, e2 = math.exp(l1), math.exp(l2)
+        assert np.allclose(out[i], (e1 * o1 + e2 * o2) / (e1 + e2), rtol=1e-12, atol=1e-12)
+        assert abs(lse[i] - math.log(e1 + e2)) < 1e-12
+
+
+def pin_combine_self_only_round_has_no_weight(orc):
+    """Self is attended only when nothing else is left (modulabs-hub notes, "LSH attention"):
+    a round in which a token has no candidate must not dilute a round in which it has some.
+    Round 1 puts every token in one bucket; in round 2 many tokens are alone in their
+    bucket window (found by brute force).  Their output equals the round-1-only output."""
+    rng = _rng(15)
+    L, d, nb, c = 64, 8, 32, 8
+    qk = rng.standard_normal((1, L, d))
+    v = rng.standard_normal((1, L, d))
+    R2 = rng.standard_normal((d, nb // 2))
+    both, _ = orc.forward(qk, v, np.stack([np.zeros((d, nb // 2)), R2]), nb, c, True, 0.5)
+    first, _ = orc.forward(qk, v, np.zeros((1, d, nb // 2)), nb, c, True, 0.5)
+    p = qk[0] @ R2
+    bucket2 = np.argmax(np.concatenate([p, -p], 1), 1)
+    lonely = [i for i in range(1, L) if not _brute_candidates(bucket2, i, c, True)]
+    assert len(lonely) >= 10
+    assert np.allclose(both[0, lonely], first[0, lonely], rtol=0, atol=1e-12)
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

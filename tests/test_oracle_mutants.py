@@ -1,0 +1,79 @@
+"""Plant plausible mistakes in copies of the oracle's C source and check that the pins
+catch every one of them (CPU only).  The real oracle source is never modified: each
+mutant is a patched copy compiled into a temporary library and exercised in a
+child process."""
+import os
+import subprocess
+import sys
+import tempfile
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+# (name, original text, replacement) -- each replacement is one plausible slip.
+MUTANTS = [
+    ("hash_sign_dropped", "cat[half + j] = -p;", "cat[half + j] = p;"),
+    ("hash_R_transposed", "Rr[(size_t)k * half + j]", "Rr[(size_t)j * d + k]"),
+    ("hash_last_index_ties", "if (cat[t] > cat[best]) best = t;", "if (cat[t] >= cat[best]) best = t;"),
+    ("hash_margin_wrong", "cat[best] - second", "cat[best]"),
+    ("sort_positions_descending", "return x->pos < y->pos ? -1 : 1;", "return x->pos < y->pos ? 1 : -1;"),
+    ("sort_bstart_off_by_one", "bstart[bucket[i] + 1] += 1;", "bstart[bucket[i]] += 1;"),
+    ("attend_self_not_masked", "if (t == s) continue;", ""),
+    ("attend_bucket_not_masked", "if (bucket[j] != bucket[i]) continue;", ""),
+    ("attend_causal_reversed", "if (causal && !(j < i)) continue;", "if (causal && !(j > i)) continue;"),
+    ("attend_no_lookback", "int lo = (k - 1) * chunk;", "int lo = k * chunk;"),
+    ("attend_next_chunk_instead",
+     "int lo = (k - 1) * chunk;\n        if (lo < 0) lo = 0;\n        int hi = (k + 1) * chunk;",
+     "int lo = k * chunk;\n        if (lo < 0) lo = 0;\n        int hi = (k + 2) * chunk;"),
+    ("attend_keys_not_normalised", "score[a] = scale * dot * inv_norm[j];", "score[a] = scale * dot;"),
+    ("attend_scale_dropped", "score[a] = scale * dot * inv_norm[j];", "score[a] = dot * inv_norm[j];"),
+    ("attend_lse_unshifted", "lse_sorted[s] = mx + log(sum);", "lse_sorted[s] = log(sum);"),
+    ("attend_self_logit_zero", "#define ORACLE_SELF_LOGIT (-1.0e5)", "#define ORACLE_SELF_LOGIT (0.0)"),
+    ("combine_uniform_weights", "double w = exp(l[r] - LSE);", "double w = 1.0 / n_rounds;"),
+    ("combine_not_unsorted",
+     "int s = inv[(size_t)r * L + i];\n            double w",
+     "int s = i;\n            double w"),
+]
+
+RUNNER = r"""
+import sys, traceback
+sys.path.insert(0, {root!r})
+import oracle
+from tests import pins
+orc = oracle.Oracle({lib!r})
+for pin in pins.ALL_PINS:
+    try:
+        pin(orc)
+    except Exception:
+        print("CAUGHT_BY", pin.__name__)
+        sys.exit(0)
+print("SURVIVED")
+"""
+
+
+def test_mutant_table_applies():
+    with open(oracle._SRC) as f:
+        src = f.read()
+    for name, old, new in MUTANTS:
+        assert src.count(old) == 1, name
+
+
+@pytest.mark.parametrize("mutant", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(mutant):
+    name, old, new = mutant
+    with open(oracle._SRC) as f:
+        src = f.read()
+    with tempfile.TemporaryDirectory() as tmp:
+        c = os.path.join(tmp, "mutant.c")
+        so = os.path.join(tmp, "libmutant.so")
+        with open(c, "w") as f:
+            f.write(src.replace(old, new))
+        oracle.compile_source(c, so)
+        res = subprocess.run([sys.executable, "-c", RUNNER.format(root=ROOT, lib=so)],
+                             capture_output=True, text=True, timeout=300)
+    # a crash of the child is also a detection; a clean run of every pin is not
+    assert "SURVIVED" not in res.stdout, f"{name}: no pin failed"
+    assert res.returncode != 0 or "CAUGHT_BY" in res.stdout, res.stderr[-2000:]
