@@ -1,0 +1,399 @@
+#!/usr/bin/env python
+"""Forward throughput of multi-round LSH attention on B300 (tokens/s = B*H*L per second).
+
+    python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference] [--workload NAME]
+
+Default workload: the long-text shape B=1, H=8, L=65536, d=128, bf16, 1024 buckets,
+8 rounds, chunk 64, causal (the headline L = 64K, 8-round configuration).  Each rank runs
+its own copy of the workload (independent heads: weak scaling, no data-path collective).
+Rank 0 prints one JSON line.  ``--impl reference`` times the fp64 CPU oracle on a bounded
+sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "LSH-attention fwd tokens/s (B·H·L per sec) at L=64K, 8 rounds; % of roofline"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+L2_BYTES = 126 * 2 ** 20
+# fp32 FFMA peak from unit counts: 148 SMs x 128 lanes x 2 flop x 2.032 GHz
+FP32_ALU_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
+
+
+# What bounds each kernel of the forward pass, per input dtype: the bf16 contractions
+# run on the tensor cores, the fp32 ones on the CUDA cores' FFMA lanes; sort and
+# combine move data.
+KERNEL_BOUND = {
+    "bf16": {"hash": "alu", "sort": "hbm", "attn": "alu", "combine": "hbm"},
+    "f32": {"hash": "alu", "sort": "hbm", "attn": "alu", "combine": "hbm"},
+}
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return FALLBACK, "fallback"
+
+
+# ------------------------------------------------------------------ algorithmic work
+
+
+def work(w):
+    """Algorithmic FLOPs and bytes per kernel for one forward pass of workload w."""
+    N, R, d, nb, c = w.tokens, w.n_rounds, w.d, w.n_buckets, w.chunk
+    e = 2 if w.dtype == "bf16" else 4
+    wr = e                                   # o_r element width
+    S = w.B * w.H * R
+    k = {}
+    k["hash"] = dict(flops=N * R * d * nb,   # N*R*(nb/2) dot products of length d
+                     bytes=N * d * e + R * d * (nb // 2) * e + N * R * 4 + N * 4)
+    k["sort"] = dict(flops=0, bytes=N * R * 4 + N * R * 8 + S * (nb + 1) * 4)
+    k["attn"] = dict(flops=8 * N * R * c * d,  # QK^T and PV over the c x 2c window
+                     bytes=2 * N * d * e + N * R * (d * wr + 4) + N * R * 8 + N * 4)
+    k["combine"] = dict(flops=0, bytes=N * R * (d * wr + 8) + N * (4 * d + 4))
+    return k
+
+
+# ------------------------------------------------------------------ clocks
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMES, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+
+def oracle_sample(w):
+    """A bounded sample of workload w for the fp64 oracle: head 0, the first
+    min(L, 32768) tokens, all rounds, the workload's bucket count and chunk."""
+    from lsh_attention_04_b300 import inputs as gen
+    Ls = min(w.L, 32768)
+    sub = w.replace(B=1, H=1, L=Ls)
+    qk, v, R = gen.make_inputs(sub, seed=w.seed)
+    desc = (f"head 0 of {w.name}: first {Ls} tokens, {w.n_rounds} rounds, "
+            f"{w.n_buckets} buckets, chunk {w.chunk} (same per-token hash work)")
+    return sub, qk, v, R, desc
+
+
+def time_oracle(w, threads, steps=1):
+    import oracle
+    sub, qk, v, R, desc = oracle_sample(w)
+    oracle.build()
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        oracle.forward(qk, v, R, sub.n_buckets, sub.chunk, sub.causal, sub.scale, threads=threads)
+        times.append(time.perf_counter() - t0)
+    used = min(threads, sub.B * sub.H * sub.n_rounds)
+    return sub.tokens, times, used, desc
+
+
+# ------------------------------------------------------------------ runs
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        return world, rank, local, dist
+    return world, rank, local, None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def allmax(dist, x):
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args, w):
+    # the CPU oracle runs on rank 0 only; other ranks have nothing to do
+    if int(os.environ.get("RANK", "0")) != 0:
+        return 0
+    threads = os.cpu_count() or 1
+    tokens, times, used, desc = time_oracle(w, threads, steps=args.warmup + args.steps)
+    timed = times[args.warmup:]
+    t = sum(timed) / len(timed)
+    value = tokens / t
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * t, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": used, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w):
+    return {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "d": w.d,
+            "n_buckets": w.n_buckets, "n_rounds": w.n_rounds, "chunk": w.chunk,
+            "causal": w.causal, "scale": "1/sqrt(d)", "qk": "clustered" if w.clusters else "gauss",
+            "clusters": w.clusters}
+
+
+def run_ours(args, w):
+    import torch
+    import lsh_attention_04_b300 as lsh
+    from lsh_attention_04_b300 import inputs as gen
+
+    world, rank, local, dist = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lib = lsh.load()
+    dt_code = lsh.LSH_BF16 if w.dtype == "bf16" else lsh.LSH_F32
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+
+    qk, v, R = gen.make_inputs(w, seed=w.seed + 7919 * rank)
+    h_qk = torch.from_numpy(qk).to(tdt).pin_memory()
+    h_v = torch.from_numpy(v).to(tdt).pin_memory()
+    h_R = torch.from_numpy(R).to(tdt).pin_memory()
+    d_qk = h_qk.to(dev)
+    d_v = h_v.to(dev)
+    d_R = h_R.to(dev)
+    out = torch.empty((w.B, w.H, w.L, w.d), dtype=torch.float32, device=dev)
+    lse = torch.empty((w.B, w.H, w.L), dtype=torch.float32, device=dev)
+    ws = lsh.workspace(w.B, w.H, w.L, w.d, w.n_buckets, w.n_rounds, w.chunk, dt_code, dev)
+    stream = torch.cuda.current_stream(dev)
+    K, Wm = args.steps, args.warmup
+
+    def fwd(events=None):
+        if events is None:
+            lsh.lsh_attn_forward(d_qk, d_v, d_R, w.n_buckets, w.chunk, w.causal, w.scale,
+                                 out=out, lse=lse, ws=ws)
+        else:
+            lsh.lsh_attn_forward_timed(d_qk, d_v, d_R, w.n_buckets, w.chunk, w.causal, w.scale,
+                                       out, lse, ws, events)
+
+    for _ in range(Wm):
+        fwd()
+    torch.cuda.synchronize()
+    st, dd = lsh.lsh_workspace_status(ws)
+    if st != lsh.LSH_OK:
+        raise RuntimeError(f"device check failed after warm-up: {lsh.lsh_status_string(st)} {dd}")
+
+    # ---- device-resident timed region: K forward calls, stage events inside each call
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    for evs in events:          # create the events (torch creates them on first record)
+        for e in evs:
+            e.record(stream)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    clocks = ClockSampler(uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
+    torch.cuda.synchronize()
+    barrier(dist)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t0.record(stream)
+    for k in range(K):
+        fwd(events[k])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1) / K
+    ms_max = allmax(dist, ms)
+    stage_names = ("hash", "sort", "attn", "combine")
+    stage_ms = {n: statistics.mean(events[k][i].elapsed_time(events[k][i + 1]) for k in range(K))
+                for i, n in enumerate(stage_names)}
+    st, dd = lsh.lsh_workspace_status(ws)
+    if st != lsh.LSH_OK:
+        raise RuntimeError(f"device check failed: {lsh.lsh_status_string(st)} {dd}")
+
+    # ---- end to end through host buffers: H2D inputs, forward, D2H outputs
+    h_out = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        d_qk.copy_(h_qk, non_blocking=True)
+        d_v.copy_(h_v, non_blocking=True)
+        d_R.copy_(h_R, non_blocking=True)
+        fwd()
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(dist)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = allmax(dist, e0.elapsed_time(e1) / K)
+    barrier(dist)
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    tokens = w.tokens * world
+    value = tokens / (ms_max / 1e3)
+    peaks, peak_src = load_peaks()
+    wk = work(w)
+    # dominant kernel and its roofline
+    dom = max(stage_ms, key=stage_ms.get)
+    kern_bound = dict(KERNEL_BOUND[w.dtype])
+
+    def roof(name):
+        t = stage_ms[name] / 1e3
+        b = kern_bound[name]
+        if b == "hbm":
+            ach = wk[name]["bytes"] / t / 1e9
+            peak = peaks["hbm_gbs"]
+            unit = "GB/s"
+        elif b == "tensor":
+            ach = wk[name]["flops"] / t / 1e12
+            peak = peaks["bf16_tflops"]
+            unit = "TFLOP/s"
+        else:
+            ach = wk[name]["flops"] / t / 1e12
+            peak = FP32_ALU_TFLOPS
+            unit = "TFLOP/s"
+        return {"bound": b, "achieved": ach, "peak": peak, "unit": unit, "frac": ach / peak,
+                "traffic": None, "kernel": name, "ms": stage_ms[name],
+                "algorithmic_flops": wk[name]["flops"], "algorithmic_bytes": wk[name]["bytes"],
+                "peak_source": peak_src if b != "alu" else "fp32 lanes x clock"}
+
+    F = sum(k["flops"] for k in wk.values())
+    Bts = sum(k["bytes"] for k in wk.values())
+    t_roof = max(F / (peaks["bf16_tflops"] * 1e12), Bts / (peaks["hbm_gbs"] * 1e9))
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": Wm, "ms_per_step": ms_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": dict(config_of(w), parallelism=f"replicas{world}",
+                       l2=f"inputs larger than L2: qk+v {2 * w.tokens * w.d * (2 if w.dtype == 'bf16' else 4) / 2**20:.0f} MiB, "
+                          f"per-round outputs {w.tokens * w.n_rounds * w.d * (2 if w.dtype == 'bf16' else 4) / 2**20:.0f} MiB "
+                          f"> L2 126 MiB; no flush"),
+        "roofline": roof(dom),
+        "kernels": {n: roof(n) for n in stage_names},
+        "path_roofline": {"flops": F, "bytes": Bts, "t_roof_ms": 1e3 * t_roof,
+                          "frac": 1e3 * t_roof / ms_max, "peaks": peak_src},
+        "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(h_qk.nbytes + h_v.nbytes + h_R.nbytes),
+                "d2h_bytes_per_step": int(h_out.nbytes + h_lse.nbytes), "ms_per_step": e2e_ms},
+        "clocks": clk,
+        "gpu_launches": int(lib.lsh_attn_kernel_launches(w.B, w.H, w.L, w.d, w.n_buckets,
+                                                         w.n_rounds, w.chunk, dt_code)) * K,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        threads = os.cpu_count() or 1
+        tok, times, used, desc = time_oracle(w, threads, steps=1)
+        line["cpu_baseline"] = {"value": tok / times[0], "unit": "tokens/s", "cores": used,
+                                "kind": "oracle", "sample": desc}
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    from lsh_attention_04_b300 import inputs as gen
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=gen.HEADLINE, choices=sorted(gen.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
+    w = gen.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

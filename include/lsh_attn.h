@@ -1,0 +1,196 @@
+/*
+ * lsh_attn.h -- C ABI of the B300 (sm_103a) multi-round LSH-attention forward pass.
+ *
+ * The method is Reformer's LSH attention over a shared query/key projection
+ * (Kitaev, Kaiser & Levskaya, "Reformer: The Efficient Transformer", ICLR 2020), as
+ * described by the "Reformer" glossary entry of ultralytics.com, section "Atencion
+ * LSH", and the modulabs-hub Reformer notes, sections "Locality sensitive hashing",
+ * "LSH attention" and "Multi-round LSH attention":
+ *
+ *   1. hash     bucket = argmax([xR_r, -xR_r]) for every token and round r;
+ *   2. sort     order the tokens of each (batch, head, round) by (bucket, position);
+ *   3. chunk    cut the sorted sequence into equal chunks of `chunk` tokens;
+ *   4. attend   every token attends to its own chunk and the previous one, only to
+ *               keys of its own bucket, only to earlier positions when causal, and to
+ *               itself only when no other key is left;
+ *   5. un-sort  move each round's result back to the original order;
+ *   6. combine  weight the rounds by exp(lse_r - logsumexp_r lse_r).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every array pointer is DEVICE memory owned by the caller.  The library never
+ *    allocates or frees memory and keeps no global state; calls on different
+ *    streams with different buffers are independent.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and never synchronise the host.  The return code reports argument
+ *    validation and launch errors only; faults inside a kernel surface at the
+ *    caller's next synchronisation.
+ *  - Layouts are dense, row-major:
+ *        qk, v     [B][H][L][d]        element type `dtype`
+ *        R         [n_rounds][d][n_buckets/2]   element type `dtype`, shared by all (b, h)
+ *        buckets   int32 [B][H][n_rounds][L]
+ *        inv_norm  fp32  [B][H][L]     1/|qk_j| (0 for a zero row)
+ *        perm      int32 [B][H][n_rounds][L]   sorted index -> original position
+ *        inv       int32 [B][H][n_rounds][L]   original position -> sorted index
+ *        bstart    int32 [B][H][n_rounds][n_buckets+1]  first sorted index of each
+ *                  bucket; bstart[n_buckets] = L
+ *        o_r       [B][H][n_rounds][L][d] in SORTED order; bf16 when dtype is
+ *                  LSH_BF16, fp32 when dtype is LSH_F32
+ *        lse_r     fp32 [B][H][n_rounds][L] in sorted order (natural log)
+ *        out       fp32 [B][H][L][d];  lse fp32 [B][H][L]
+ *  - Keys are L2-normalised and queries are not: the score of query i and key j is
+ *    scale * (qk_i . qk_j) / |qk_j|.  The usual choice is scale = 1/sqrt(d).
+ *  - A token with no key left gets o = v_i and lse_r = -1e5 for that round, so the
+ *    round combination gives that round a weight of about exp(-1e5) unless every
+ *    round is like that.  This assumes |scale * |qk|| is far below 1e5.
+ *  - Results for NaN or Inf inputs are undefined.
+ *  - Workspaces are device buffers of at least the size the matching
+ *    *_workspace_bytes() call returns, 256-byte aligned.  Their first 256 bytes hold
+ *    a status block that kernels with bounded waits write when a wait gives up;
+ *    lsh_workspace_status() reads it.
+ */
+#ifndef LSH_ATTN_H
+#define LSH_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LSH_OK = 0,
+    LSH_ERR_INVALID_ARGUMENT = 1,  /* null pointer, non-positive size, L % chunk != 0, odd n_buckets */
+    LSH_ERR_UNSUPPORTED = 2,       /* valid but outside what the kernels implement (see below) */
+    LSH_ERR_WORKSPACE_TOO_SMALL = 3,
+    LSH_ERR_CUDA = 4,              /* a CUDA runtime call or kernel launch failed */
+    LSH_ERR_DEVICE_CHECK = 5       /* a kernel gave up a bounded wait (from lsh_workspace_status) */
+} lsh_status_t;
+
+typedef enum {
+    LSH_F32 = 0,   /* fp32 inputs; CUDA-core arithmetic in fp32 */
+    LSH_BF16 = 1   /* bf16 inputs; tensor-core products with fp32 accumulation */
+} lsh_dtype_t;
+
+/*
+ * Supported range (anything else returns LSH_ERR_UNSUPPORTED):
+ *   d in {64, 128};  chunk in {32, 64};  2 <= n_buckets <= 2048;
+ *   n_buckets % 16 == 0 for LSH_BF16;  B*H*n_rounds*L < 2^31.
+ */
+
+/* Human-readable name of a status code (static storage). */
+const char *lsh_status_string(lsh_status_t status);
+
+/*
+ * Bytes of device workspace lsh_attn_forward needs for this problem (0 when the
+ * arguments are invalid or unsupported).
+ */
+size_t lsh_attn_workspace_bytes(int B, int H, int L, int d, int n_buckets, int n_rounds,
+                                int chunk, lsh_dtype_t dtype);
+
+/*
+ * The whole forward pass: steps 1-6 above, on `stream`, through the caller's
+ * workspace (which then holds buckets, perm, inv, bstart, o_r and lse_r; see
+ * lsh_attn_workspace_layout).
+ *   qk, v     [B][H][L][d] dtype;  R [n_rounds][d][n_buckets/2] dtype
+ *   causal    0 or 1;  scale  multiplies every score (see conventions)
+ *   out       fp32 [B][H][L][d];  lse  fp32 [B][H][L]: logsumexp over rounds of lse_r
+ * out and lse must not alias the inputs or the workspace.
+ */
+lsh_status_t lsh_attn_forward(const void *qk, const void *v, const void *R, lsh_dtype_t dtype,
+                              int B, int H, int L, int d, int n_buckets, int n_rounds,
+                              int chunk, int causal, float scale, float *out, float *lse,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * lsh_attn_forward that also records five caller-created CUDA events (cudaEvent_t) on
+ * `stream` at the stage boundaries: stage_events[0] before the hash, [1] before the
+ * sort, [2] before the attention, [3] before the combination and [4] after it.  For
+ * timing each kernel inside the real call.  A NULL array or event is
+ * LSH_ERR_INVALID_ARGUMENT.
+ */
+lsh_status_t lsh_attn_forward_timed(const void *qk, const void *v, const void *R,
+                                    lsh_dtype_t dtype, int B, int H, int L, int d,
+                                    int n_buckets, int n_rounds, int chunk, int causal,
+                                    float scale, float *out, float *lse, void *workspace,
+                                    size_t workspace_bytes, void *stream,
+                                    void *const *stage_events);
+
+/*
+ * Number of kernels one lsh_attn_forward call launches for this problem (0 when the
+ * arguments are invalid or unsupported).  The workspace status clear is a memset, not
+ * a kernel, and is not counted.
+ */
+int lsh_attn_kernel_launches(int B, int H, int L, int d, int n_buckets, int n_rounds,
+                             int chunk, lsh_dtype_t dtype);
+
+/*
+ * Byte offsets of the intermediates inside lsh_attn_forward's workspace, for
+ * callers that want to inspect them.  Any pointer may be NULL.
+ */
+lsh_status_t lsh_attn_workspace_layout(int B, int H, int L, int d, int n_buckets, int n_rounds,
+                                       int chunk, lsh_dtype_t dtype, size_t *off_buckets,
+                                       size_t *off_inv_norm, size_t *off_perm, size_t *off_inv,
+                                       size_t *off_bstart, size_t *off_o_r, size_t *off_lse_r);
+
+/* ---------------------------------------------------------------- stages */
+
+/*
+ * Step 1, angular LSH ("Atencion LSH": the bucket is the position of the largest
+ * entry of [xR, -xR]; modulabs-hub "Locality sensitive hashing": R has half as many
+ * columns as there are buckets).  Ties go to the first index of the concatenation.
+ * Writes buckets [B][H][n_rounds][L] and inv_norm [B][H][L].
+ */
+size_t lsh_hash_workspace_bytes(int n_rounds, int d, int n_buckets, lsh_dtype_t dtype);
+lsh_status_t lsh_hash(const void *qk, const void *R, lsh_dtype_t dtype, int B, int H, int L,
+                      int d, int n_buckets, int n_rounds, int32_t *buckets, float *inv_norm,
+                      void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Step 2, stable sort of each (b, h, r) segment by bucket (ai-scholar.tech article,
+ * "LSH attention": sort each LSH bucket; modulabs-hub: "ordering" the bucketed
+ * keys).  Ties keep position order.  Writes perm, inv and bstart (layouts above).
+ */
+size_t lsh_bucket_sort_workspace_bytes(int B, int H, int L, int n_buckets, int n_rounds);
+lsh_status_t lsh_bucket_sort(const int32_t *buckets, int B, int H, int L, int n_buckets,
+                             int n_rounds, int32_t *perm, int32_t *inv, int32_t *bstart,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Steps 3-4, chunked attention of every round ("Atencion LSH": equal chunks, each
+ * token attends to its own and the previous chunk; modulabs-hub "LSH attention":
+ * same-bucket, self and causal masks).  Sorted row s sees the sorted rows
+ * [(s/chunk - 1)*chunk, (s/chunk + 1)*chunk) clipped to [0, L); chunk 0 has no
+ * previous chunk.  Writes o_r and lse_r in sorted order (layouts above).
+ */
+size_t lsh_chunk_attn_workspace_bytes(void);
+lsh_status_t lsh_chunk_attn(const void *qk, const void *v, lsh_dtype_t dtype,
+                            const int32_t *buckets, const int32_t *perm, const int32_t *bstart,
+                            const float *inv_norm, int B, int H, int L, int d, int n_buckets,
+                            int n_rounds, int chunk, int causal, float scale, void *o_r,
+                            float *lse_r, void *workspace, size_t workspace_bytes,
+                            void *stream);
+
+/*
+ * Steps 5-6, un-sort and combine rounds: for token i,
+ * lse_i = logsumexp_r lse_r[inv_r[i]] and out_i = sum_r exp(lse_r[inv_r[i]] - lse_i)
+ * o_r[inv_r[i]].  o_r is bf16 when dtype is LSH_BF16 and fp32 when LSH_F32.
+ */
+lsh_status_t lsh_unsort_combine(const void *o_r, const float *lse_r, const int32_t *inv,
+                                lsh_dtype_t dtype, int B, int H, int L, int d, int n_rounds,
+                                float *out, float *lse, void *stream);
+
+/*
+ * Waits for `stream`, then reads the status block at the start of `workspace`:
+ * LSH_OK, or LSH_ERR_DEVICE_CHECK when a kernel gave up a bounded wait since the
+ * block was last cleared (each entry point that takes a workspace clears it).
+ * `detail`, when not NULL, receives the kernel's code for where it gave up.
+ */
+lsh_status_t lsh_workspace_status(const void *workspace, int *detail, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LSH_ATTN_H */

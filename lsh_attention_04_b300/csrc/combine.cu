@@ -1,0 +1,108 @@
+// combine.cu -- un-sort the per-round outputs and combine the rounds.
+//
+// Each round r produced, in sorted order, an output row o_r and its log-normaliser
+// lse_r.  For token i the row of round r sits at sorted index inv_r[i].  The rounds are
+// weighted by their share of the total softmax mass:
+//   lse_i = logsumexp_r lse_r(i),   out_i = sum_r exp(lse_r(i) - lse_i) * o_r(i).
+// (Rounds run in parallel per the "Reformer" glossary, section "Atencion LSH"; the
+// logsumexp weighting is the standard way to merge softmax results computed over
+// separate key sets.)
+//
+// One warp per token; each lane owns D/32 consecutive elements, read with one 4- to
+// 16-byte vector load, so every row is read in one coalesced access.
+#include <math.h>
+
+#include "internal.cuh"
+
+namespace lsh {
+namespace {
+
+constexpr int kWarps = 8;
+
+__device__ __forceinline__ void load_row(const float *p, float (&x)[2]) {
+    const float2 t = *reinterpret_cast<const float2 *>(p);
+    x[0] = t.x; x[1] = t.y;
+}
+__device__ __forceinline__ void load_row(const float *p, float (&x)[4]) {
+    const float4 t = *reinterpret_cast<const float4 *>(p);
+    x[0] = t.x; x[1] = t.y; x[2] = t.z; x[3] = t.w;
+}
+__device__ __forceinline__ void load_row(const __nv_bfloat16 *p, float (&x)[2]) {
+    const __nv_bfloat162 t = *reinterpret_cast<const __nv_bfloat162 *>(p);
+    const float2 f = __bfloat1622float2(t);
+    x[0] = f.x; x[1] = f.y;
+}
+__device__ __forceinline__ void load_row(const __nv_bfloat16 *p, float (&x)[4]) {
+    const uint2 t = *reinterpret_cast<const uint2 *>(p);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&t.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&t.y));
+    x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kWarps * 32)
+combine_kernel(const T *__restrict__ o_r, const float *__restrict__ lse_r,
+               const int32_t *__restrict__ inv, long n_tok, int L, int n_rounds,
+               float *__restrict__ out, float *__restrict__ lse)
+{
+    constexpr int EPL = D / 32;  // elements per lane, contiguous
+    const int lane = threadIdx.x & 31;
+    const long tok = (long)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (tok >= n_tok) return;
+    const long bh = tok / L;
+    const int i = (int)(tok % L);
+    const size_t seg0 = (size_t)bh * n_rounds;
+
+    float mx = -INFINITY;
+    for (int r = 0; r < n_rounds; ++r) {
+        const size_t base = (seg0 + r) * L;
+        mx = fmaxf(mx, lse_r[base + inv[base + i]]);
+    }
+    float acc[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+    float sum = 0.f;
+    for (int r = 0; r < n_rounds; ++r) {
+        const size_t base = (seg0 + r) * L;
+        const int s = inv[base + i];
+        const float w = expf(lse_r[base + s] - mx);
+        sum += w;
+        float x[EPL];
+        load_row(o_r + (base + s) * D + lane * EPL, x);
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[e] = fmaf(w, x[e], acc[e]);
+    }
+    const float rs = 1.0f / sum;
+    float *dst = out + (size_t)tok * D + lane * EPL;
+    if constexpr (EPL == 4) {
+        *reinterpret_cast<float4 *>(dst) = make_float4(acc[0] * rs, acc[1] * rs, acc[2] * rs, acc[3] * rs);
+    } else {
+        *reinterpret_cast<float2 *>(dst) = make_float2(acc[0] * rs, acc[1] * rs);
+    }
+    if (lane == 0) lse[tok] = mx + logf(sum);
+}
+
+template <typename T, int D>
+cudaError_t launch(const Problem &p, const void *o_r, const float *lse_r, const int32_t *inv,
+                   float *out, float *lse, cudaStream_t st)
+{
+    const long n = p.n_tok();
+    const unsigned grid = (unsigned)((n + kWarps - 1) / kWarps);
+    combine_kernel<T, D><<<grid, kWarps * 32, 0, st>>>((const T *)o_r, lse_r, inv, n, p.L,
+                                                       p.n_rounds, out, lse);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t combine_launch(const Problem &p, const void *o_r, const float *lse_r,
+                           const int32_t *inv, float *out, float *lse, cudaStream_t st)
+{
+    if (p.dtype == LSH_F32)
+        return p.d == 64 ? launch<float, 64>(p, o_r, lse_r, inv, out, lse, st)
+                         : launch<float, 128>(p, o_r, lse_r, inv, out, lse, st);
+    return p.d == 64 ? launch<__nv_bfloat16, 64>(p, o_r, lse_r, inv, out, lse, st)
+                     : launch<__nv_bfloat16, 128>(p, o_r, lse_r, inv, out, lse, st);
+}
+
+}  // namespace lsh

@@ -1,0 +1,87 @@
+// internal.cuh -- shared declarations of the LSH-attention CUDA library (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "lsh_attn.h"
+
+namespace lsh {
+
+// Logit given to a token's own key when it is the only key left (the "self only when
+// nothing else exists" rule of the modulabs-hub notes, section "LSH attention").
+constexpr float kSelfLogit = -1.0e5f;
+
+// First 256 bytes of every workspace.  Kernels that wait on hardware barriers give up
+// after a bounded time, record where in `detail`, and set `code` to 1.
+struct StatusBlock {
+    int code;
+    int detail;
+    int pad[62];
+};
+static_assert(sizeof(StatusBlock) == 256, "status block is 256 bytes");
+
+constexpr size_t kAlign = 1024;
+inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
+
+// Sort tile: keys per CTA of the counting-sort passes.
+constexpr int kSortTile = 4096;
+inline int sort_tiles(int L) { return (L + kSortTile - 1) / kSortTile; }
+
+// Element loads widened to fp32.
+__device__ __forceinline__ float ld_f32(const float *p, size_t i) { return p[i]; }
+__device__ __forceinline__ float ld_f32(const __nv_bfloat16 *p, size_t i) {
+    return __bfloat162float(p[i]);
+}
+__device__ __forceinline__ void st_elem(float *p, size_t i, float x) { p[i] = x; }
+__device__ __forceinline__ void st_elem(__nv_bfloat16 *p, size_t i, float x) {
+    p[i] = __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// Problem description passed to every launcher.
+struct Problem {
+    int B, H, L, d, nb, n_rounds, chunk, causal;
+    float scale;
+    lsh_dtype_t dtype;
+    long n_tok() const { return (long)B * H * L; }
+    long n_seg() const { return (long)B * H * n_rounds; }
+};
+
+// ---- launchers (each returns the launch error, if any) ----
+cudaError_t hash_simt(const Problem &p, const void *qk, const void *R, int32_t *buckets,
+                      float *inv_norm, cudaStream_t st);
+// tensor-core hash: R is first packed into `rpack` (bytes from hash_tc_pack_bytes)
+size_t hash_tc_pack_bytes(const Problem &p);
+cudaError_t hash_tc(const Problem &p, const void *qk, const void *R, void *rpack,
+                    int32_t *buckets, float *inv_norm, StatusBlock *status, cudaStream_t st);
+bool hash_tc_supported(const Problem &p);
+int hash_tc_launches(const Problem &p);
+
+cudaError_t sort_launch(const Problem &p, const int32_t *buckets, int32_t *perm, int32_t *inv,
+                        int32_t *bstart, int32_t *counts, cudaStream_t st);
+
+cudaError_t attn_simt(const Problem &p, const void *qk, const void *v, const int32_t *buckets,
+                      const int32_t *perm, const int32_t *bstart, const float *inv_norm,
+                      void *o_r, float *lse_r, cudaStream_t st);
+bool attn_tc_supported(const Problem &p);
+cudaError_t attn_tc(const Problem &p, const void *qk, const void *v, const int32_t *buckets,
+                    const int32_t *perm, const int32_t *bstart, const float *inv_norm, void *o_r,
+                    float *lse_r, StatusBlock *status, cudaStream_t st);
+
+cudaError_t combine_launch(const Problem &p, const void *o_r, const float *lse_r,
+                           const int32_t *inv, float *out, float *lse, cudaStream_t st);
+
+}  // namespace lsh

@@ -1,0 +1,154 @@
+"""The C-ABI library loads, exports every symbol its header declares, and validates
+arguments on the host (no GPU needed: every call here fails validation or only
+computes sizes, so no kernel is launched)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import lsh_attention_04_b300 as lsh
+from lsh_attention_04_b300 import build as lbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    lbuild.build()
+    return lsh.load()
+
+
+def header_functions():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", f)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(lsh_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_header_declares_the_entry_points():
+    names = header_functions()
+    for n in ("lsh_attn_forward", "lsh_hash", "lsh_bucket_sort", "lsh_chunk_attn",
+              "lsh_unsort_combine", "lsh_attn_workspace_bytes", "lsh_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in header_functions():
+        assert hasattr(lib, n), n
+    nm = subprocess.run(["nm", "-D", "--defined-only", lsh.LIB_PATH], capture_output=True,
+                        text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (lsh_\w+)", nm))
+    assert set(header_functions()) <= exported
+    assert set(lsh.EXPORTS) == set(header_functions())
+
+
+def test_library_is_built_for_sm103a(lib):
+    out = subprocess.run(["/usr/local/cuda/bin/cuobjdump", "--list-elf", lsh.LIB_PATH],
+                         capture_output=True, text=True).stdout
+    assert "sm_103a" in out
+
+
+def test_status_strings(lib):
+    assert lsh.lsh_status_string(0) == "LSH_OK"
+    assert lsh.lsh_status_string(5) == "LSH_ERR_DEVICE_CHECK"
+    assert lsh.lsh_status_string(77) == "LSH_ERR_UNKNOWN"
+
+
+def test_workspace_sizing(lib):
+    f = lib.lsh_attn_workspace_bytes
+    n = f(1, 8, 65536, 128, 1024, 8, 64, lsh.LSH_BF16)
+    # o_r alone is B*H*R*L*d*2 bytes
+    assert n > 1 * 8 * 8 * 65536 * 128 * 2
+    assert n % 256 == 0
+    assert f(1, 8, 65536, 128, 1024, 8, 64, lsh.LSH_F32) > n
+    # invalid or unsupported -> 0
+    assert f(1, 1, 100, 64, 32, 1, 64, lsh.LSH_F32) == 0      # L % chunk
+    assert f(1, 1, 1024, 64, 31, 1, 32, lsh.LSH_F32) == 0     # odd n_buckets
+    assert f(1, 1, 1024, 96, 32, 1, 32, lsh.LSH_F32) == 0     # d
+    assert f(1, 1, 1024, 64, 4096, 1, 32, lsh.LSH_F32) == 0   # n_buckets > 2048
+    assert f(0, 1, 1024, 64, 32, 1, 32, lsh.LSH_F32) == 0
+    assert lib.lsh_chunk_attn_workspace_bytes() >= 256
+    assert lib.lsh_bucket_sort_workspace_bytes(1, 1, 1024, 32, 1) >= 256
+
+
+def test_workspace_layout_is_disjoint(lib):
+    args = (8, 8, 4096, 64, 64, 4, 64, lsh.LSH_BF16)
+    lay = lsh.lsh_attn_workspace_layout(*args)
+    total = lsh.lsh_attn_workspace_bytes(*args)
+    SL = 8 * 8 * 4 * 4096
+    sizes = dict(buckets=4 * SL, inv_norm=4 * 8 * 8 * 4096, perm=4 * SL, inv=4 * SL,
+                 bstart=4 * 8 * 8 * 4 * 65, o_r=2 * SL * 64, lse_r=4 * SL)
+    spans = sorted((lay[k], lay[k] + sizes[k]) for k in sizes)
+    assert spans[0][0] >= 256
+    for (a0, a1), (b0, b1) in zip(spans, spans[1:]):
+        assert a1 <= b0
+    assert spans[-1][1] <= total
+    assert all(lay[k] % 256 == 0 for k in lay)
+
+
+# The validation tests below pass made-up pointer values.  They are meant to be
+# rejected before any CUDA call; on a machine with a GPU a validation bug would hand
+# such a pointer to the device, so these tests only run where no GPU exists.
+no_device = pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                               reason="fake pointers are only passed where no GPU exists")
+
+
+def _fwd(lib, **kw):
+    a = dict(qk=1, v=1, R=1, dtype=lsh.LSH_BF16, B=1, H=1, L=1024, d=64, nb=32, R_=1,
+             chunk=64, causal=1, scale=0.125, out=1, lse=1, ws=256, wsb=1 << 30, st=None)
+    a.update(kw)
+    P = ctypes.c_void_p
+    return lib.lsh_attn_forward(P(a["qk"]), P(a["v"]), P(a["R"]), a["dtype"], a["B"], a["H"],
+                                a["L"], a["d"], a["nb"], a["R_"], a["chunk"], a["causal"],
+                                a["scale"], P(a["out"]), P(a["lse"]), P(a["ws"]), a["wsb"],
+                                a["st"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(qk=0), lsh.LSH_ERR_INVALID_ARGUMENT),
+    (dict(out=0), lsh.LSH_ERR_INVALID_ARGUMENT),
+    (dict(ws=0), lsh.LSH_ERR_INVALID_ARGUMENT),
+    (dict(ws=4), lsh.LSH_ERR_INVALID_ARGUMENT),          # misaligned workspace
+    (dict(L=1000), lsh.LSH_ERR_INVALID_ARGUMENT),        # not a multiple of chunk
+    (dict(nb=33), lsh.LSH_ERR_INVALID_ARGUMENT),
+    (dict(B=0), lsh.LSH_ERR_INVALID_ARGUMENT),
+    (dict(R_=-1), lsh.LSH_ERR_INVALID_ARGUMENT),
+    (dict(causal=2), lsh.LSH_ERR_INVALID_ARGUMENT),
+    (dict(dtype=7), lsh.LSH_ERR_INVALID_ARGUMENT),
+    (dict(d=96), lsh.LSH_ERR_UNSUPPORTED),
+    (dict(chunk=128, L=1024), lsh.LSH_ERR_UNSUPPORTED),
+    (dict(nb=4096), lsh.LSH_ERR_UNSUPPORTED),
+    (dict(nb=40), lsh.LSH_ERR_UNSUPPORTED),              # bf16 needs n_buckets % 16 == 0
+    (dict(B=1 << 12, H=1 << 12, L=1 << 10, R_=1 << 2), lsh.LSH_ERR_UNSUPPORTED),
+    (dict(wsb=1024), lsh.LSH_ERR_WORKSPACE_TOO_SMALL),
+])
+@no_device
+def test_forward_validation(lib, kw, expect):
+    assert _fwd(lib, **kw) == expect
+
+
+@no_device
+def test_stage_validation(lib):
+    P = ctypes.c_void_p
+    # null outputs
+    assert lib.lsh_hash(P(1), P(1), lsh.LSH_F32, 1, 1, 64, 64, 32, 1, None, P(1), P(256), 1 << 20,
+                        None) == lsh.LSH_ERR_INVALID_ARGUMENT
+    assert lib.lsh_bucket_sort(P(1), 1, 1, 64, 32, 1, None, P(1), P(1), P(256), 1 << 20,
+                               None) == lsh.LSH_ERR_INVALID_ARGUMENT
+    assert lib.lsh_bucket_sort(P(1), 1, 1, 64, 4096, 1, P(1), P(1), P(1), P(256), 1 << 20,
+                               None) == lsh.LSH_ERR_UNSUPPORTED
+    assert lib.lsh_bucket_sort(P(1), 1, 1, 64, 32, 1, P(1), P(1), P(1), P(256), 8,
+                               None) == lsh.LSH_ERR_WORKSPACE_TOO_SMALL
+    assert lib.lsh_unsort_combine(P(1), P(1), None, lsh.LSH_F32, 1, 1, 64, 64, 1, P(1), P(1),
+                                  None) == lsh.LSH_ERR_INVALID_ARGUMENT
+    assert lib.lsh_unsort_combine(P(1), P(1), P(1), lsh.LSH_F32, 1, 1, 64, 32, 1, P(1), P(1),
+                                  None) == lsh.LSH_ERR_UNSUPPORTED
+    assert lib.lsh_chunk_attn(P(1), P(1), lsh.LSH_F32, P(1), P(1), P(1), P(1), 1, 1, 100, 64, 32,
+                              1, 32, 1, ctypes.c_float(1.0), P(1), P(1), P(256), 1 << 20,
+                              None) == lsh.LSH_ERR_INVALID_ARGUMENT   # L % chunk
+    assert lib.lsh_workspace_status(None, None, None) == lsh.LSH_ERR_INVALID_ARGUMENT
