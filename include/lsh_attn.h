@@ -158,6 +158,25 @@ lsh_status_t lsh_bucket_sort(const int32_t *buckets, int B, int H, int L, int n_
                              void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * lsh_bucket_sort for callers that cannot allocate device memory (frameworks whose
+ * allocator they do not own, runtimes that forbid allocation after start-up, code that
+ * must not risk cudaMalloc's implicit synchronisation or failure).  The paper has no
+ * counterpart: this is a packaging choice of this library.  Same inputs, outputs and
+ * results as lsh_bucket_sort, but the sort's scratch comes from an 8 MiB array that
+ * the library holds on every GPU that loads it, until the process exits.
+ *  - Needs 4 * B*H*n_rounds * n_buckets * ceil(L/4096) <= 8 MiB; larger problems return
+ *    LSH_ERR_WORKSPACE_TOO_SMALL and launch nothing.
+ *  - All calls on a device share that array: calls that overlap on the GPU race and
+ *    corrupt each other; order them on one stream.
+ *  - The first call on a device looks the array's address up with that device
+ *    current; make it before any stream capture, with the stream's device current.
+ *  - Allocates nothing and takes no workspace.
+ */
+lsh_status_t lsh_bucket_sort_noalloc(const int32_t *buckets, int B, int H, int L, int n_buckets,
+                                     int n_rounds, int32_t *perm, int32_t *inv, int32_t *bstart,
+                                     void *stream);
+
+/*
  * Steps 3-4, chunked attention of every round ("Atencion LSH": equal chunks, each
  * token attends to its own and the previous chunk; modulabs-hub "LSH attention":
  * same-bucket, self and causal masks).  Sorted row s sees the sorted rows

@@ -32,7 +32,7 @@ EXPORTS = (
     "lsh_attn_workspace_layout", "lsh_hash_workspace_bytes", "lsh_hash",
     "lsh_bucket_sort_workspace_bytes", "lsh_bucket_sort", "lsh_chunk_attn_workspace_bytes",
     "lsh_chunk_attn", "lsh_unsort_combine", "lsh_workspace_status", "lsh_attn_forward_timed",
-    "lsh_attn_kernel_launches",
+    "lsh_attn_kernel_launches", "lsh_bucket_sort_noalloc",
 )
 
 _lib = None
