@@ -1,10 +1,451 @@
-// hash_tc.cu -- tensor-core angular LSH (tcgen05).  Placeholder until the kernel lands.
-#include "internal.cuh"
+// hash_tc.cu -- angular LSH on the tcgen05 tensor cores (bf16 inputs, fp32 accumulation).
+//
+// "Reformer" glossary (ultralytics.com), section "Atencion LSH": project every token
+// with a random matrix R and take the position of the largest entry of [xR, -xR] as the
+// bucket.  modulabs-hub Reformer notes, "Locality sensitive hashing": R_r has
+// n_buckets/2 columns; the + and - halves are concatenated.  Several rounds use
+// independent R_r ("Multi-round LSH attention").
+//
+// The projection x.R_r is a dense contraction, so it runs on the tensor cores:
+//  * The columns of all rounds are laid out one round after another (each round padded
+//    to a multiple of 32 columns with zero columns that never win) and cut into MMA
+//    chunks of at most 256 columns: several whole rounds per chunk when a round has at
+//    most 256 columns, otherwise 256-column parts of one round.
+//  * Consecutive rounds form a "group" whose packed R image (<= 128 KB) stays resident in
+//    shared memory for the whole kernel.  A pre-pass (lsh_rpack_kernel) writes that image
+//    in the canonical K-major 128-byte-swizzled layout, so one bulk TMA copy stages it.
+//  * Persistent CTAs: ctas_per_group CTAs per group walk the 128-token tiles in the same
+//    order, so the CTAs of all groups read a tile of qk within a short time window and
+//    only the first one fetches it from HBM (the others hit L2).
+//  * Warp roles: warp 8 issues TMA loads of the qk tile (2-D tensor map, 128-byte
+//    swizzle, 2 stages); warp 9 (one thread) issues tcgen05.mma M=128 x N=chunk x K=16
+//    into one of two 256-column TMEM accumulators; warps 0-3 and 4-7 (two epilogue
+//    warpgroups, one per accumulator) read the projections with tcgen05.ld and keep, per
+//    token and round, the entry of largest magnitude (first index on ties); warp 10
+//    computes 1/|x| of each token from the staged tile (first group only).
+//  * Bucket rule: the largest entry of [p, -p] is the entry of p with the largest |p_j|,
+//    taken with its sign: bucket = j if p_j >= 0, n_buckets/2 + j otherwise.  Scanning j
+//    in order with a strict comparison keeps the first index.  Two entries of equal
+//    magnitude and opposite sign have a zero top-1/top-2 margin, i.e. they are a near-tie.
+//  * When a round spans chunks of both warpgroups, each keeps its partial (value, index)
+//    in shared memory (double-buffered by tile parity) and warpgroup 0 merges them; two
+//    mbarriers per buffer (full: both warpgroups flushed; empty: merged) order it.
+// Every wait is bounded (see sm100::wait); on a timeout the kernel records the place in
+// the workspace status block and winds down.
+#include <math.h>
+
+#include "sm100.cuh"
 
 namespace lsh {
-bool hash_tc_supported(const Problem &) { return false; }
-size_t hash_tc_pack_bytes(const Problem &) { return 0; }
-int hash_tc_launches(const Problem &) { return 0; }
-cudaError_t hash_tc(const Problem &, const void *, const void *, void *, int32_t *, float *,
-                    StatusBlock *, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
+
+using namespace sm100;
+
+constexpr int kTileM = 128;          // tokens per tile = MMA M = TMEM lanes
+constexpr int kChunkMax = 256;       // MMA N per chunk (TMEM columns per accumulator)
+constexpr int kRCapBytes = 128 * 1024;
+constexpr int kXStages = 2;
+constexpr int kThreads = 11 * 32;    // 8 epilogue warps, producer, MMA, norm
+constexpr int kMaxSplitRounds = 3;   // rounds per group when rounds span chunks
+
+struct HashPlan {
+    long long n_tok;
+    int L, d, half, hp, n_rounds;
+    int split;            // 0: chunk = rpc whole rounds; 1: round = cpr chunks
+    int rpc, cpr, rpg;    // rounds per chunk, chunks per round, rounds per group
+    int n_groups, ctas_per_group, n_tiles;
+    int group_bytes;      // bytes of one group's packed R image (stride in rpack)
+};
+
+// ---- geometry of chunk k of a group with nr rounds (host and device) ----
+__host__ __device__ __forceinline__ int n_chunks(const HashPlan &P, int nr) {
+    return P.split ? nr * P.cpr : (nr + P.rpc - 1) / P.rpc;
+}
+__host__ __device__ __forceinline__ int chunk_col0(const HashPlan &P, int k) {
+    return P.split ? (k / P.cpr) * P.hp + kChunkMax * (k % P.cpr) : k * P.rpc * P.hp;
+}
+__host__ __device__ __forceinline__ int chunk_width(const HashPlan &P, int nr, int k) {
+    if (P.split) return min(kChunkMax, P.hp - kChunkMax * (k % P.cpr));
+    return min(P.rpc, nr - k * P.rpc) * P.hp;
+}
+
+// ---- R pre-pack: R [n_rounds][d][half] -> per-group K-major SW128 images ----
+__global__ void __launch_bounds__(256)
+lsh_rpack_kernel(const __nv_bfloat16 *__restrict__ R, HashPlan P, uint8_t *__restrict__ rpack)
+{
+    const int kch = P.d / 8;  // 16-byte pieces per packed row
+    const long long total = (long long)P.n_rounds * P.hp * kch;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int c = (int)(i % kch);
+        const int jp = (int)((i / kch) % P.hp);
+        const int r = (int)(i / ((long long)kch * P.hp));
+        const int g = r / P.rpg, r_in = r % P.rpg;
+        const int nr = min(P.rpg, P.n_rounds - g * P.rpg);
+        int k, n;
+        if (P.split) { k = r_in * P.cpr + jp / kChunkMax; n = jp % kChunkMax; }
+        else { k = r_in / P.rpc; n = (r_in % P.rpc) * P.hp + jp; }
+        const int width = chunk_width(P, nr, k);
+        const size_t dst = (size_t)g * P.group_bytes + (size_t)chunk_col0(P, k) * P.d * 2 +
+                           kmajor_sw128_off(n, c * 8, width);
+        __align__(16) __nv_bfloat16 v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            v[e] = jp < P.half ? R[((size_t)r * P.d + c * 8 + e) * P.half + jp] : __float2bfloat16_rn(0.f);
+        *reinterpret_cast<uint4 *>(rpack + dst) = *reinterpret_cast<const uint4 *>(v);
+    }
+}
+
+// ---- the hash kernel ----
+struct __align__(8) HashBarriers {
+    uint64_t x_full[kXStages], x_empty[kXStages];
+    uint64_t tm_full[2], tm_empty[2];
+    uint64_t parts_full[2], parts_empty[2];
+    uint64_t r_full, mma_done;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+__device__ __forceinline__ void write_bucket(int32_t *buckets, const HashPlan &P, long long tok,
+                                             int r, float best, int bidx) {
+    const long long bh = tok / P.L, l = tok - bh * P.L;
+    buckets[((size_t)bh * P.n_rounds + r) * P.L + l] = best >= 0.f ? bidx : P.half + bidx;
+}
+
+// Keep the entry of largest magnitude of 32 projections (columns j0 .. j0+31 of a round),
+// first index on ties; only the first `nvalid` columns count.
+__device__ __forceinline__ void scan32(const uint32_t (&v)[32], int j0, int nvalid, float &best,
+                                       int &bidx) {
+    if (nvalid >= 32) {
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+            const float x = __uint_as_float(v[jj]);
+            if (fabsf(x) > fabsf(best)) { best = x; bidx = j0 + jj; }
+        }
+    } else {
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+            const float x = __uint_as_float(v[jj]);
+            if (jj < nvalid && fabsf(x) > fabsf(best)) { best = x; bidx = j0 + jj; }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__restrict__ rpack,
+                   const HashPlan P, int32_t *__restrict__ buckets, float *__restrict__ inv_norm,
+                   StatusBlock *status)
+{
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ HashBarriers sb;
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const int x_bytes = kTileM * P.d * 2;
+    uint8_t *Rs = smem;
+    uint8_t *Xs = smem + P.group_bytes;  // group_bytes is a multiple of 1024
+    float *part_best = (float *)(Xs + kXStages * x_bytes);          // [2][2][kMaxSplitRounds][128]
+    int *part_idx = (int *)(part_best + 2 * 2 * kMaxSplitRounds * kTileM);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = blockIdx.x / P.ctas_per_group;
+    const int cj = blockIdx.x % P.ctas_per_group;
+    const int r0 = g * P.rpg;
+    const int nr = min(P.rpg, P.n_rounds - r0);
+    const int nch = n_chunks(P, nr);
+    volatile int *abort_flag = &sb.abort_flag;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kXStages; ++s) {
+            mbar_init(&sb.x_full[s], 1);
+            mbar_init(&sb.x_empty[s], g == 0 ? 2 : 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sb.tm_full[b], 1);
+            mbar_init(&sb.tm_empty[b], 128);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sb.parts_full[b], 256);
+            mbar_init(&sb.parts_empty[b], 128);
+        }
+        mbar_init(&sb.r_full, 1);
+        mbar_init(&sb.mma_done, 1);
+        sb.abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == 8) tmem_alloc(&sb.tmem_base, 512);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = sb.tmem_base;
+
+    if (warp == 8) {
+        // ---------------- producer: R group once, then qk tiles ----------------
+        if (lane == 0) {
+            prefetch_tmap(&xmap);
+            const int rbytes = nr * P.hp * P.d * 2;
+            mbar_expect_tx(&sb.r_full, (uint32_t)rbytes);
+            const uint8_t *src = rpack + (size_t)g * P.group_bytes;
+            for (int off = 0; off < rbytes; off += 32768)
+                bulk_g2s(Rs + off, src + off, (uint32_t)min(32768, rbytes - off), &sb.r_full);
+            uint32_t pending = 0;  // stages with a fill in flight (for the wind-down)
+            int it = 0;
+            for (int t = cj; t < P.n_tiles; t += P.ctas_per_group, ++it) {
+                const int s = it % kXStages;
+                const uint32_t ph = (it / kXStages) & 1;
+                if (!wait(&sb.x_empty[s], ph ^ 1, abort_flag, status, 0x101)) break;
+                mbar_expect_tx(&sb.x_full[s], (uint32_t)x_bytes);
+                for (int kb = 0; kb < P.d / 64; ++kb)
+                    tma_load_2d(Xs + s * x_bytes + kb * kTileM * 128, &xmap, kb * 64, t * kTileM,
+                                &sb.x_full[s]);
+                pending |= 1u << s;
+            }
+            // wind-down: every issued copy has landed before the CTA exits
+            int last = it - 1;
+            for (int k = 0; k < kXStages && last - k >= 0; ++k) {
+                const int i2 = last - k, s = i2 % kXStages;
+                if (pending & (1u << s)) {
+                    const uint32_t ph = (i2 / kXStages) & 1;
+                    int dummy = 0;
+                    wait(&sb.x_full[s], ph, &dummy, status, 0x102);
+                }
+            }
+            int dummy = 0;
+            wait(&sb.r_full, 0, &dummy, status, 0x103);
+        }
+    } else if (warp == 9) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            bool ok = wait(&sb.r_full, 0, abort_flag, status, 0x201);
+            fence_after_sync();
+            uint32_t chunk_ctr = 0;
+            int it = 0;
+            const uint32_t rs = smem_u32(Rs), xs = smem_u32(Xs);
+            for (int t = cj; ok && t < P.n_tiles; t += P.ctas_per_group, ++it) {
+                const int s = it % kXStages;
+                if (!(ok = wait(&sb.x_full[s], (it / kXStages) & 1, abort_flag, status, 0x202))) break;
+                fence_after_sync();
+                for (int k = 0; k < nch; ++k, ++chunk_ctr) {
+                    const int b = chunk_ctr & 1;
+                    if (!(ok = wait(&sb.tm_empty[b], ((chunk_ctr >> 1) & 1) ^ 1, abort_flag, status,
+                                    0x203)))
+                        break;
+                    fence_after_sync();
+                    const int width = chunk_width(P, nr, k);
+                    const uint32_t idesc = idesc_bf16(kTileM, width, 0, 0);
+                    const uint32_t rbase = rs + chunk_col0(P, k) * P.d * 2;
+                    for (int ks = 0; ks < P.d / 16; ++ks) {
+                        const int kb = ks >> 2, ko = (ks & 3) * 32;
+                        const uint64_t a = smem_desc(xs + s * x_bytes + kb * kTileM * 128 + ko, 16, 1024);
+                        const uint64_t bd = smem_desc(rbase + kb * width * 128 + ko, 16, 1024);
+                        mma_ss(tmem + b * kChunkMax, a, bd, idesc, ks > 0);
+                    }
+                    mma_commit(smem_u32(&sb.tm_full[b]));
+                }
+                if (!ok) break;
+                mma_commit(smem_u32(&sb.x_empty[s]));
+            }
+            // wind-down: all issued MMAs complete before TMEM is released
+            mma_commit(smem_u32(&sb.mma_done));
+            int dummy = 0;
+            wait(&sb.mma_done, 0, &dummy, status, 0x204);
+        }
+    } else if (warp == 10) {
+        // ---------------- 1/|x| of each token (first group only) ----------------
+        if (g == 0) {
+            int it = 0;
+            for (int t = cj; t < P.n_tiles; t += P.ctas_per_group, ++it) {
+                const int s = it % kXStages;
+                bool ok = wait(&sb.x_full[s], (it / kXStages) & 1, abort_flag, status, 0x301);
+                if (!__all_sync(0xffffffffu, ok)) break;
+                const uint8_t *xt = Xs + s * x_bytes;
+                for (int rr = 0; rr < 4; ++rr) {
+                    const int row = lane + 32 * rr;
+                    float acc = 0.f;
+                    for (int kb = 0; kb < P.d / 64; ++kb) {
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const uint4 q = *reinterpret_cast<const uint4 *>(
+                                xt + kb * kTileM * 128 + row * 128 + ((c ^ (row & 7)) << 4));
+                            const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&q);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 f = __bfloat1622float2(h[e]);
+                                acc = fmaf(f.x, f.x, acc);
+                                acc = fmaf(f.y, f.y, acc);
+                            }
+                        }
+                    }
+                    const long long tok = (long long)t * kTileM + row;
+                    if (tok < P.n_tok) inv_norm[tok] = acc > 0.f ? 1.0f / sqrtf(acc) : 0.f;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sb.x_empty[s]);
+            }
+        }
+    } else {
+        // ---------------- epilogue warpgroups (warps 0-3: buffer 0, 4-7: buffer 1) --------
+        const int e = warp >> 2, q = warp & 3;
+        const int row = q * 32 + lane;
+        const uint32_t tlane = tmem + ((uint32_t)(q * 32) << 16) + e * kChunkMax;
+        uint32_t chunk_ctr = 0;
+        int it = 0;
+        bool ok = true;
+        for (int t = cj; ok && t < P.n_tiles; t += P.ctas_per_group, ++it) {
+            const long long tok = (long long)t * kTileM + row;
+            const bool live = tok < P.n_tok;
+            int cur = -1;
+            float best = 0.f;
+            int bidx = 0;
+            const int par = it & 1;
+            if (P.split) {
+                // parts[par] of two tiles ago must have been merged by warpgroup 0
+                bool w = wait(&sb.parts_empty[par], ((it >> 1) & 1) ^ 1, abort_flag, status, 0x402);
+                if (!(ok = __all_sync(0xffffffffu, w))) break;
+            }
+            for (int k = 0; k < nch; ++k, ++chunk_ctr) {
+                if ((int)(chunk_ctr & 1) != e) continue;
+                bool w = wait(&sb.tm_full[e], (chunk_ctr >> 1) & 1, abort_flag, status, 0x401);
+                if (!(ok = __all_sync(0xffffffffu, w))) break;
+                fence_after_sync();
+                const int width = chunk_width(P, nr, k);
+                for (int c = 0; c < width; c += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(tlane + c, v);
+                    tmem_wait_ld();
+                    int r, j0;
+                    if (P.split) { r = k / P.cpr; j0 = kChunkMax * (k % P.cpr) + c; }
+                    else {
+                        const int col = chunk_col0(P, k) + c;
+                        r = col / P.hp;
+                        j0 = col - r * P.hp;
+                    }
+                    if (r != cur) {
+                        if (P.split && cur >= 0) {
+                            const int o = ((par * 2 + e) * kMaxSplitRounds + cur) * kTileM + row;
+                            part_best[o] = best;
+                            part_idx[o] = bidx;
+                        }
+                        cur = r;
+                        best = 0.f;
+                        bidx = 0;
+                    }
+                    scan32(v, j0, P.half - j0, best, bidx);
+                    if (!P.split && j0 + 32 >= P.hp && live)
+                        write_bucket(buckets, P, tok, r0 + r, best, bidx);
+                }
+                fence_before_sync();
+                mbar_arrive(&sb.tm_empty[e]);
+            }
+            if (!ok) break;
+            if (P.split) {
+                if (cur >= 0) {
+                    const int o = ((par * 2 + e) * kMaxSplitRounds + cur) * kTileM + row;
+                    part_best[o] = best;
+                    part_idx[o] = bidx;
+                }
+                mbar_arrive(&sb.parts_full[par]);
+                if (e == 0) {
+                    bool w = wait(&sb.parts_full[par], (it >> 1) & 1, abort_flag, status, 0x403);
+                    if (!(ok = __all_sync(0xffffffffu, w))) break;
+                    for (int r = 0; live && r < nr; ++r) {
+                        const int o0 = ((par * 2 + 0) * kMaxSplitRounds + r) * kTileM + row;
+                        const int o1 = ((par * 2 + 1) * kMaxSplitRounds + r) * kTileM + row;
+                        const float b0 = part_best[o0], b1 = part_best[o1];
+                        const int i0 = part_idx[o0], i1 = part_idx[o1];
+                        const bool take1 = fabsf(b1) > fabsf(b0) || (fabsf(b1) == fabsf(b0) && i1 < i0);
+                        write_bucket(buckets, P, tok, r0 + r, take1 ? b1 : b0, take1 ? i1 : i0);
+                    }
+                    mbar_arrive(&sb.parts_empty[par]);
+                }
+            }
+        }
+    }
+
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 8) {
+        __syncwarp();
+        fence_after_sync();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+bool make_plan(const Problem &p, HashPlan &P, int num_sms)
+{
+    P.n_tok = p.n_tok();
+    P.L = p.L;
+    P.d = p.d;
+    P.half = p.nb / 2;
+    P.hp = (P.half + 31) / 32 * 32;
+    P.n_rounds = p.n_rounds;
+    const int cap = kRCapBytes / (p.d * 2);
+    if (P.hp > cap) return false;
+    P.split = P.hp > kChunkMax;
+    P.rpc = P.split ? 1 : kChunkMax / P.hp;
+    P.cpr = P.split ? (P.hp + kChunkMax - 1) / kChunkMax : 1;
+    const int rpg_max = cap / P.hp;
+    P.n_groups = (p.n_rounds + rpg_max - 1) / rpg_max;
+    P.rpg = (p.n_rounds + P.n_groups - 1) / P.n_groups;
+    if (P.split && P.rpg > kMaxSplitRounds) return false;
+    P.n_tiles = (int)((P.n_tok + kTileM - 1) / kTileM);
+    P.ctas_per_group = num_sms / P.n_groups;
+    if (P.ctas_per_group < 1) P.ctas_per_group = 1;
+    if (P.ctas_per_group > P.n_tiles) P.ctas_per_group = P.n_tiles;
+    P.group_bytes = P.rpg * P.hp * p.d * 2;  // multiple of 32*64*2 = 4096
+    return true;
+}
+
+size_t smem_bytes(const HashPlan &P)
+{
+    return 1024 + (size_t)P.group_bytes + (size_t)kXStages * kTileM * P.d * 2 +
+           (size_t)2 * 2 * kMaxSplitRounds * kTileM * 8;
+}
+
+int num_sms_current()
+{
+    int dev = 0, n = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n;
+}
+
+}  // namespace
+
+bool hash_tc_supported(const Problem &p)
+{
+    if (p.dtype != LSH_BF16) return false;
+    HashPlan P;
+    return make_plan(p, P, 148);
+}
+
+size_t hash_tc_pack_bytes(const Problem &p)
+{
+    HashPlan P;
+    if (!make_plan(p, P, 148)) return 0;
+    return (size_t)P.n_groups * P.group_bytes;
+}
+
+int hash_tc_launches(const Problem &) { return 2; }
+
+cudaError_t hash_tc(const Problem &p, const void *qk, const void *R, void *rpack, int32_t *buckets,
+                    float *inv_norm, StatusBlock *status, cudaStream_t st)
+{
+    HashPlan P;
+    if (!make_plan(p, P, num_sms_current())) return cudaErrorNotSupported;
+    CUtensorMap xmap;
+    if (!make_tmap_2d_bf16(&xmap, qk, (uint64_t)P.n_tok, (uint64_t)p.d, 64, kTileM))
+        return cudaErrorNotSupported;
+    const long long pack_items = (long long)P.n_rounds * P.hp * (p.d / 8);
+    const long long want = (pack_items + 255) / 256;
+    const int pack_blocks = (int)(want < 4096 ? want : 4096);
+    lsh_rpack_kernel<<<pack_blocks, 256, 0, st>>>((const __nv_bfloat16 *)R, P, (uint8_t *)rpack);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const size_t smem = smem_bytes(P);
+    e = cudaFuncSetAttribute(lsh_hash_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    lsh_hash_tc_kernel<<<P.n_groups * P.ctas_per_group, kThreads, smem, st>>>(
+        xmap, (const uint8_t *)rpack, P, buckets, inv_norm, status);
+    return cudaGetLastError();
+}
+
 }  // namespace lsh

@@ -74,7 +74,23 @@ def _x_norm(qk):
 # ---------------------------------------------------------------- stage parity
 
 
-@pytest.mark.parametrize("w", SMALL, ids=ids)
+# Geometries of the tensor-core hash: rounds packed several per MMA chunk, rounds split
+# over 2 or 3 chunks (both epilogue warpgroups merge), several resident groups of rounds,
+# a ragged last 128-token tile, d = 64 and d = 128.
+HASH_CASES = SMALL + [
+    W("hash_split2_nb1024_d128_R3", 1, 2, 2048, 128, "bf16", 1024, 3, 64, True, 32, 31),
+    W("hash_split_nb768_d128_R2", 1, 1, 1920, 128, "bf16", 768, 2, 64, True, 16, 32),
+    W("hash_split3_nb1536_d64_R2", 1, 1, 1152, 64, "bf16", 1536, 2, 64, True, 16, 33),
+    W("hash_split2_nb640_d64_R5", 1, 3, 640, 64, "bf16", 640, 5, 64, True, 8, 34),
+    W("hash_pack8_nb16_d64_R8", 3, 1, 1000, 64, "bf16", 16, 8, 8, True, 4, 35),
+    W("hash_pack2_nb192_d128_R8", 1, 1, 1088, 128, "bf16", 192, 8, 64, True, 16, 36),
+    W("hash_groups_nb512_d64_R8", 2, 1, 960, 64, "bf16", 512, 8, 64, True, 16, 37),
+    W("hash_ragged_nb96_d128_R1", 1, 1, 200, 128, "bf16", 96, 1, 8, True, 0, 38),
+]
+hash_ids = [w.name for w in HASH_CASES]
+
+
+@pytest.mark.parametrize("w", HASH_CASES, ids=hash_ids)
 def test_hash_parity(w):
     qk, v, R = _inputs(w)
     dqk, _, dR = _dev(w, qk, v, R)
