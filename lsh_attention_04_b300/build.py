@@ -21,6 +21,10 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 
 
+# Per-file extra flags (none at present).
+EXTRA = {}
+
+
 def sources():
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
@@ -46,7 +50,7 @@ def build(verbose: bool = False, force: bool = False) -> str:
         obj = os.path.join(OBJ, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if force or _stale(obj, [src] + hdrs):
-            cmd = [NVCC] + ARCH + FLAGS + ["-c", src, "-o", obj]
+            cmd = [NVCC] + ARCH + FLAGS + EXTRA.get(os.path.basename(src), []) + ["-c", src, "-o", obj]
             if verbose:
                 cmd += ["-Xptxas", "-v"]
             jobs.append(cmd)

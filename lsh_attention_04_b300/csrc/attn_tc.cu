@@ -11,24 +11,40 @@
 // Tile = 128 consecutive sorted rows (chunks 2t and 2t+1 of one (batch, head, round)
 // segment).  Their keys live in the 192-row window of chunks 2t-1, 2t, 2t+1: rows of
 // chunk 2t use window columns 0-127, rows of chunk 2t+1 use columns 64-191.
-//   S = Q K^T     tcgen05.mma M=128, N=64 (chunk 2t-1) + N=128 (chunks 2t, 2t+1), K=d,
-//                 A and B K-major from shared memory, fp32 into TMEM (2 x 192 columns).
-//   P             written back over S in TMEM as packed bf16 pairs.
-//   O = P V       tcgen05.mma M=128, N=d, K=192 with A read from TMEM and V as an MN-major
-//                 shared-memory operand (the same 128-byte-swizzled row layout as Q/K).
+//   S = Q K^T     one chain of tcgen05.mma M=128, N=192, K=16 steps over d; A (window
+//                 rows 64-191) and B (all 192 rows) come from the tile's own Q/K window
+//                 buffer in shared memory; fp32 into TMEM (2 x 192 columns).
+//   P             packed bf16 pairs written into TMEM over S: the 32 keys of S columns
+//                 32j..32j+31 go to columns 32j..32j+15, so every warp overwrites only
+//                 S columns it has already read.
+//   O = P V       tcgen05.mma M=128, N=d, K=16 steps with A read from TMEM and V as an
+//                 MN-major shared-memory operand (the same 128-byte-swizzled row layout
+//                 as Q/K).
+// One thread issues a tcgen05.mma only every few hundred cycles whatever N is, so the S
+// chain and the P V chain are issued from two different warps and overlap.
+// Masks: sorted order keeps each bucket in one run, so the keys of sorted row s form one
+// interval of window columns: [max(window start, bucket start), causal ? s : min(window
+// end, bucket end)), minus s itself when not causal.  The loaders fetch the bucket's run
+// bounds; the softmax needs no per-key bucket test.  A row with no key but itself gives
+// its own column weight 1, so P V returns v_i exactly; its lse is the self logit -1e5.
 // Softmax without a running maximum: with unit keys every score of query i is bounded
 // by m_i = |scale| * |q_i| (Cauchy-Schwarz), so p = exp(s - m_i) cannot overflow.  If
 // m_i is so large that every p could underflow (|scale| |q_i| log2 e > 64), the warp
 // first takes the exact row maximum instead.  lse = m_i + log(sum p).
 // Rows are gathered through the sort permutation by TMA tile::gather4 (4 rows per
-// instruction, 128-byte swizzle) into a ring of 6 chunk slots; chunk c sits in slot
-// c mod 6, which keeps the two query chunks of a tile in adjacent slots.
-// Warp roles: 0-3 softmax + output epilogue (one TMEM lane quarter each), 4-9 loaders
-// (warp 4+s fills slot s: permutation, buckets and 1/|k| of the rows, then the
-// gathers), 10 MMA issuer and TMEM owner.  Persistent CTAs take contiguous ranges of tiles of a
-// group of heads small enough for L2, so all rounds of those heads share cached rows.
-// Every wait is bounded (sm100::wait); on a timeout the kernel records where in the
-// workspace status block and winds down.
+// instruction, 128-byte swizzle): each tile's 192 Q/K rows into one of two window
+// buffers (the look-back chunk is gathered again for the next tile, which keeps the
+// window contiguous for the single N=192 MMA), and V rows with the row metadata into a
+// ring of 6 chunk slots (chunk c in slot c mod 6), released after the last P V that
+// reads them.
+// Warp roles: 0-7 softmax + output epilogue (warps w and w+4 share TMEM lane quarter w
+// and split the row's columns and O's columns), 8 V loader (one owner for all slots, so
+// each slot's fills, and the parity waits on its barrier, happen in order), 9 Q/K window
+// loader, 10 S issuer and TMEM owner, 11 P V issuer.
+// Persistent CTAs take contiguous ranges of tiles of a group of heads small enough for
+// L2, so all rounds of those heads share cached rows.  Every wait is bounded
+// (sm100::wait); on a timeout the kernel records where in the workspace status block and
+// winds down.
 #include <math.h>
 
 #include "sm100.cuh"
@@ -40,12 +56,16 @@ using namespace sm100;
 
 constexpr int kC = 64;            // chunk length
 constexpr int kRows = 128;        // rows per tile
-constexpr int kWin = 192;         // S columns per tile
-constexpr int kSlots = 6;         // chunk ring
-constexpr int kLoaders = kSlots;  // loader warps: warp 4+s owns slot s
-constexpr int kThreads = (4 + kLoaders + 1) * 32;
-constexpr int kMmaWarp = 4 + kLoaders;
+constexpr int kWin = 192;         // S columns per tile (window rows)
+constexpr int kSlots = 6;         // V ring
+constexpr int kSmWarps = 8;       // softmax / epilogue warps
+constexpr int kVLoaders = 1;      // V loader warps (12 warps in all: 3 per scheduler keeps 168 registers per thread)
+constexpr int kQkWarp = kSmWarps + kVLoaders;
+constexpr int kSWarp = kQkWarp + 1;
+constexpr int kPvWarp = kSWarp + 1;
+constexpr int kThreads = (kPvWarp + 1) * 32;
 constexpr int kTmemO = 2 * kWin;  // O accumulator column (384)
+constexpr int kLBufs = 4;         // tiles of partial row sums kept in shared memory
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kExactMaxLog2 = 64.f;
@@ -61,20 +81,21 @@ struct AttnPlan {
 struct SlotMeta {
     float cs[kC];    // key column scale: scale * log2(e) / |k_j|
     float m2[kC];    // query bound in log2 units: |scale| * log2(e) * |q_i|
-    int sb[kC];      // bucket of the sorted row
-    int j[kC];       // original position of the sorted row
+    int blo[kC];     // sorted index where the row's bucket starts
+    int bhi[kC];     // sorted index where the row's bucket ends
 };
 
 struct __align__(8) AttnBarriers {
-    uint64_t chunk_full[kSlots], slot_empty[kSlots];
+    uint64_t qk_full[2], qk_empty[2];             // Q/K window buffers (free after S)
+    uint64_t v_full[kSlots], v_empty[kSlots];     // V rows + metadata (free after P V)
     uint64_t s_full[2], p_full[2], pv_done[2];
     uint64_t o_full, o_empty, mma_done;
     uint32_t tmem_base;
     int abort_flag;
 };
 
-// The tiles of head group `grp` are split into ncta contiguous ranges of global units
-// u = seg * tps + tile (seg = bh * n_rounds + r).
+// The tiles of head group `grp` are split into gridDim.x contiguous ranges of global
+// units u = seg * tps + tile (seg = bh * n_rounds + r).
 __device__ __forceinline__ void group_range(const AttnPlan &P, int grp, long long &lo,
                                             long long &hi) {
     const int h0 = grp * P.heads_per_group;
@@ -119,7 +140,7 @@ __device__ __forceinline__ void gather4(uint32_t dst, const CUtensorMap *map, in
     (((unsigned long long)(idx) < (unsigned long long)(bound))                           \
          ? (idx) : (sm100::report(status, abort_flag, (code)), decltype(idx)(0)))
 #else
-#define LSH_IDX(idx, bound, code) (idx)
+#define LSH_IDX(idx, bound, code) ((void)(bound), (idx))
 #endif
 
 __device__ __forceinline__ float ex2(float x) {
@@ -133,59 +154,100 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+__device__ __forceinline__ void st_global_v8(void *p, const uint32_t *r) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 :: "l"(p), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+                    "r"(r[6]), "r"(r[7]) : "memory");
+}
+
+// TMEM column of the packed P values of keys 16m .. 16m+15 (relative to the S buffer).
+__host__ __device__ __forceinline__ int p_col(int m) { return 32 * (m >> 1) + 8 * (m & 1); }
+
+// Softmax of one 32-key batch: key jj is a candidate iff jj + off lies in [0, len) (and,
+// not causal, jj != skip); candidates get p = 2^(s cs - m2), the rest 0 -- except column
+// one_at, which gets weight 1 (the self fallback).  Returns the sum of the p.
+template <bool kSelfCol>
+__device__ __forceinline__ float softmax_batch(const uint32_t (&s32)[32], const float *cs, int off,
+                                               unsigned len, int skip, int one_at, float m2,
+                                               uint32_t (&pk)[16]) {
+    float l = 0.f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        float p2[2];
+#pragma unroll
+        for (int e2 = 0; e2 < 2; ++e2) {
+            const int jj = 2 * k + e2;
+            bool ok = (unsigned)(jj + off) < len;
+            if (kSelfCol) ok = ok && jj != skip;
+            const float x = fmaf(__uint_as_float(s32[jj]), cs[jj], -m2);
+            float p = ok ? ex2(x) : 0.f;
+            if (kSelfCol) p = jj == one_at ? 1.f : p;
+            p2[e2] = p;
+        }
+        pk[k] = pack_bf16(p2[0], p2[1]);
+        l += p2[0] + p2[1];
+    }
+    return l;
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
 lsh_attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap vmap,
                    const AttnPlan P, const int32_t *__restrict__ buckets,
-                   const int32_t *__restrict__ perm, const float *__restrict__ inv_norm,
-                   const __nv_bfloat16 *__restrict__ v, __nv_bfloat16 *__restrict__ o_r,
+                   const int32_t *__restrict__ perm, const int32_t *__restrict__ bstart,
+                   const float *__restrict__ inv_norm, __nv_bfloat16 *__restrict__ o_r,
                    float *__restrict__ lse_r, StatusBlock *status)
 {
     extern __shared__ uint8_t smem_raw[];
     __shared__ AttnBarriers sb;
-    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    __shared__ float l_part[kLBufs][2][kRows];   // partial row sums of the two column halves
+    // 1024-byte aligned base, derived from the shared array by pointer arithmetic so the
+    // compiler keeps the shared state space (shared loads, not generic ones)
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int nkb = P.d / 64;                      // 64-column blocks of a row
-    const int kb_stride = kSlots * kC * 128;       // Q/K: [kb][slot][64 rows][128 B]
-    const int vslot = nkb * kC * 128;              // V:   [slot][kb][64 rows][128 B]
-    uint8_t *QK = smem;
-    uint8_t *V = QK + nkb * kb_stride;
+    const int wkb = kWin * 128;                    // Q/K window: [w][kb][192 rows][128 B]
+    const int wstride = nkb * wkb;
+    const int vslot = nkb * kC * 128;              // V ring: [slot][kb][64 rows][128 B]
+    uint8_t *QKW = smem;
+    uint8_t *V = QKW + 2 * wstride;
     SlotMeta *meta = (SlotMeta *)(V + kSlots * vslot);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int *abort_flag = &sb.abort_flag;
     const uint32_t FULL = 0xffffffffu;
-    uint32_t loader_armed = 0, loader_armed_par = 0;
+    uint32_t armed = 0, armed_par = 0;   // loaders: last fill per slot / window (wind-down)
 
     if (threadIdx.x == 0) {
+        for (int w = 0; w < 2; ++w) {
+            mbar_init(&sb.qk_full[w], 1);           // expect_tx arrive
+            mbar_init(&sb.qk_empty[w], 1);
+        }
         for (int s = 0; s < kSlots; ++s) {
-            mbar_init(&sb.chunk_full[s], 1 + 32);   // expect_tx arrive + 32 metadata lanes
-            mbar_init(&sb.slot_empty[s], 1);
+            mbar_init(&sb.v_full[s], 1 + 32);       // expect_tx arrive + 32 metadata lanes
+            mbar_init(&sb.v_empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&sb.s_full[b], 1);
-            mbar_init(&sb.p_full[b], 128);
+            mbar_init(&sb.p_full[b], 32 * kSmWarps);
             mbar_init(&sb.pv_done[b], 1);
         }
         mbar_init(&sb.o_full, 1);
-        mbar_init(&sb.o_empty, 128);
-        mbar_init(&sb.mma_done, 1);
+        mbar_init(&sb.o_empty, 32 * kSmWarps);
+        mbar_init(&sb.mma_done, 2);
         sb.abort_flag = 0;
         mbar_fence_init();
     }
-    if (warp == kMmaWarp) tmem_alloc(&sb.tmem_base, 512);
+    if (warp == kSWarp) tmem_alloc(&sb.tmem_base, 512);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = sb.tmem_base;
+    const size_t n_rows = (size_t)P.n_heads * P.n_rounds * P.L;
+    const long long n_tok = (long long)P.n_heads * P.L;
 
-    if (warp >= 4 && warp < 4 + kLoaders) {
-        // ------------------------------------------------------------- loaders
-        const int lw = warp - 4;
-        if (lane == 0) { prefetch_tmap(&qmap); prefetch_tmap(&vmap); }
-        uint32_t empty_bits = (1u << kSlots) - 1;   // parity to wait per slot
-        uint32_t armed = 0;                          // slots this warp filled (wind-down)
-        uint32_t armed_par = 0;
+    if (warp >= kSmWarps && warp < kSmWarps + kVLoaders) {
+        // ------------------------------------------------------------- V loaders
+        const int lw = warp - kSmWarps;
+        if (lane == 0) prefetch_tmap(&vmap);
+        uint32_t v_bits = (1u << kSlots) - 1;        // parity to wait per slot
         const float ascale = fabsf(P.scale) * kLog2e, cscale = P.scale * kLog2e;
         for_items(P, [&](long long seg, int tb, int te) -> bool {
             const long long bh = seg / P.n_rounds;
@@ -193,31 +255,14 @@ lsh_attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
             const int c_end = min(2 * te, P.nchunks);
             for (int c = c_begin; c < c_end; ++c) {
                 const int s = c % kSlots;
-                // Each slot has one owning warp, so its fills (and the parity waits on its
-                // slot_empty barrier) happen strictly in order: a parity wait cannot tell a
-                // phase from the one two fills later.
-                if (s != lw) continue;
-                const uint32_t par = (empty_bits >> s) & 1u;
-                empty_bits ^= 1u << s;
+                if (s % kVLoaders != lw) continue;
+                const uint32_t pv = (v_bits >> s) & 1u;
+                v_bits ^= 1u << s;
+                // metadata first (it does not need the slot): rows lane and lane + 32
                 const size_t row0 = (size_t)seg * P.L + (size_t)c * kC;
-                const size_t n_rows = (size_t)P.n_heads * P.n_rounds * P.L;
                 const int j0 = perm[LSH_IDX(row0 + lane, n_rows, 0x511)];
                 const int j1 = perm[LSH_IDX(row0 + 32 + lane, n_rows, 0x512)];
-                const int b0 = buckets[LSH_IDX((size_t)seg * P.L + j0, n_rows, 0x513)];
-                const int b1 = buckets[LSH_IDX((size_t)seg * P.L + j1, n_rows, 0x514)];
-                const long long n_tok = (long long)P.n_heads * P.L;
-                const float n0 = inv_norm[LSH_IDX(bh * P.L + j0, n_tok, 0x515)];
-                const float n1 = inv_norm[LSH_IDX(bh * P.L + j1, n_tok, 0x516)];
-#ifdef LSH_CHECKED
-                if ((unsigned)j0 >= (unsigned)P.L || (unsigned)j1 >= (unsigned)P.L) report(status, abort_flag, 0x517);
-                if ((unsigned)b0 >= (unsigned)P.nb || (unsigned)b1 >= (unsigned)P.nb) report(status, abort_flag, 0x518);
-#endif
-                bool ok = wait(&sb.slot_empty[s], par, abort_flag, status, 0x501);
-                if (!__all_sync(FULL, ok)) return false;
-                if (lane == 0) mbar_expect_tx(&sb.chunk_full[s], (uint32_t)(kC * P.d * 2 * 2));
-                __syncwarp();
-                // rows 4*lane .. 4*lane+3 of the chunk (lanes 0-15 issue the gathers)
-                int g[4];
+                int g[4];   // rows 4*lane .. 4*lane+3 of the chunk (lanes 0-15 gather)
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int row = (4 * lane + k) & 63;
@@ -225,183 +270,219 @@ lsh_attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                     const int b = __shfl_sync(FULL, j1, row & 31);
                     g[k] = (int)(bh * P.L) + (row < 32 ? a : b);
                 }
-#ifdef LSH_CHECKED
-                for (int k = 0; k < 4; ++k)
-                    if (lane < 16 && (unsigned)g[k] >= (unsigned)(P.n_heads * P.L)) {
-                        report(status, abort_flag, 0x519);
-                        g[k] = 0;
-                    }
-#endif
-                if (lane < 16) {
-                    const uint32_t bar = smem_u32(&sb.chunk_full[s]);
-                    for (int kb = 0; kb < nkb; ++kb) {
-                        gather4(smem_u32(QK + kb * kb_stride + s * kC * 128 + 4 * lane * 128), &qmap,
-                                kb * 64, g[0], g[1], g[2], g[3], bar);
+                const int b0 = buckets[LSH_IDX((size_t)seg * P.L + j0, n_rows, 0x513)];
+                const int b1 = buckets[LSH_IDX((size_t)seg * P.L + j1, n_rows, 0x514)];
+                const float n0 = inv_norm[LSH_IDX(bh * P.L + j0, n_tok, 0x515)];
+                const float n1 = inv_norm[LSH_IDX(bh * P.L + j1, n_tok, 0x516)];
+                const size_t bs0 = (size_t)seg * (P.nb + 1);
+                const size_t n_bs = (size_t)P.n_heads * P.n_rounds * (P.nb + 1);
+                const int lo0 = bstart[LSH_IDX(bs0 + b0, n_bs, 0x517)];
+                const int hi0 = bstart[LSH_IDX(bs0 + b0 + 1, n_bs, 0x518)];
+                const int lo1 = bstart[LSH_IDX(bs0 + b1, n_bs, 0x519)];
+                const int hi1 = bstart[LSH_IDX(bs0 + b1 + 1, n_bs, 0x51a)];
+                bool ok = wait(&sb.v_empty[s], pv, abort_flag, status, 0x503);
+                if (!__all_sync(FULL, ok)) return false;
+                if (lane == 0) mbar_expect_tx(&sb.v_full[s], (uint32_t)(kC * P.d * 2));
+                __syncwarp();
+                if (lane < 16)
+                    for (int kb = 0; kb < nkb; ++kb)
                         gather4(smem_u32(V + s * vslot + kb * kC * 128 + 4 * lane * 128), &vmap,
-                                kb * 64, g[0], g[1], g[2], g[3], bar);
-                    }
-                }
+                                kb * 64, g[0], g[1], g[2], g[3], smem_u32(&sb.v_full[s]));
                 SlotMeta &m = meta[s];
                 m.cs[lane] = cscale * n0;
                 m.cs[lane + 32] = cscale * n1;
                 m.m2[lane] = n0 > 0.f ? ascale / n0 : 0.f;
                 m.m2[lane + 32] = n1 > 0.f ? ascale / n1 : 0.f;
-                m.sb[lane] = b0;
-                m.sb[lane + 32] = b1;
-                m.j[lane] = j0;
-                m.j[lane + 32] = j1;
-                mbar_arrive(&sb.chunk_full[s]);
+                m.blo[lane] = lo0;
+                m.blo[lane + 32] = lo1;
+                m.bhi[lane] = hi0;
+                m.bhi[lane + 32] = hi1;
+                mbar_arrive(&sb.v_full[s]);
                 armed |= 1u << s;
-                armed_par = (armed_par & ~(1u << s)) | (par << s);
+                armed_par = (armed_par & ~(1u << s)) | (pv << s);
             }
             return true;
         });
-        loader_armed = armed;
-        loader_armed_par = armed_par;
-    } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            uint32_t full_bits = 0;
-            int ctr = 0;
-            int pt = 0, ptb = 0, pte = 0;    // the tile whose P V is still to be issued
-            const uint32_t qk_base = smem_u32(QK), v_base = smem_u32(V);
-            const uint32_t idesc64 = idesc_bf16(kRows, 64, 0, 0);
-            const uint32_t idesc128 = idesc_bf16(kRows, 128, 0, 0);
-            const uint32_t idesc_pv = idesc_bf16(kRows, P.d, 0, 1);
-
-            auto need = [&](int c) -> bool {
-                const int s = c % kSlots;
-                const bool ok = wait(&sb.chunk_full[s], (full_bits >> s) & 1u, abort_flag, status, 0x601);
-                full_bits ^= 1u << s;
-                return ok;
-            };
-            auto do_pv = [&](int t, int tb, int te, int q) -> bool {
-                const int b = q & 1;
-                if (!wait(&sb.p_full[b], (q >> 1) & 1, abort_flag, status, 0x602)) return false;
-                if (!wait(&sb.o_empty, (q & 1) ^ 1, abort_flag, status, 0x603)) return false;
-                fence_after_sync();
-                uint32_t acc = 0;
-                for (int w = 0; w < 3; ++w) {
-                    const int kc = 2 * t - 1 + w;
-                    if (kc < 0 || kc >= P.nchunks) continue;
-                    const int s = kc % kSlots;
-                    for (int m4 = 0; m4 < 4; ++m4) {
-                        const int m = 4 * w + m4;
-                        const uint64_t bd = smem_desc(v_base + s * vslot + m4 * 2048, kC * 128, 1024);
-                        mma_ts(tmem + kTmemO, tmem + b * kWin + m * 8, bd, idesc_pv, acc);
-                        acc = 1;
-                    }
+    } else if (warp == kQkWarp) {
+        // ------------------------------------------------------------- Q/K window loader
+        if (lane == 0) prefetch_tmap(&qmap);
+        int ctr = 0;
+        for_items(P, [&](long long seg, int tb, int te) -> bool {
+            const long long bh = seg / P.n_rounds;
+            for (int t = tb; t < te; ++t, ++ctr) {
+                const int w = ctr & 1;
+                const bool has_lb = t > 0, has_hi = 2 * t + 1 < P.nchunks;
+                int j[3][2];
+#pragma unroll
+                for (int ci = 0; ci < 3; ++ci) {
+                    const int c = 2 * t - 1 + ci;
+                    const bool present = ci == 1 || (ci == 0 ? has_lb : has_hi);
+                    const size_t row0 = (size_t)seg * P.L + (size_t)(present ? c : 0) * kC;
+                    j[ci][0] = present ? perm[LSH_IDX(row0 + lane, n_rows, 0x521)] : 0;
+                    j[ci][1] = present ? perm[LSH_IDX(row0 + 32 + lane, n_rows, 0x522)] : 0;
                 }
-                mma_commit(smem_u32(&sb.o_full));
-                mma_commit(smem_u32(&sb.pv_done[b]));
-                // release the chunks whose last use was this tile
-                if (t > 0) mma_commit(smem_u32(&sb.slot_empty[(2 * t - 1) % kSlots]));
-                mma_commit(smem_u32(&sb.slot_empty[(2 * t) % kSlots]));
-                if (t == te - 1 && 2 * t + 1 < P.nchunks)
-                    mma_commit(smem_u32(&sb.slot_empty[(2 * t + 1) % kSlots]));
-                return true;
-            };
-
-            bool pending = false;             // P V of tile (pt, ptb, pte) not issued yet
-            bool ok = for_items(P, [&](long long seg, int tb, int te) -> bool {
-                for (int t = tb; t < te; ++t) {
-                    // The first chunks of a new item may reuse slots that the previous item's
-                    // last tile releases only after its P V: issue that P V first.
-                    if (t == tb && pending) {
-                        if (!do_pv(pt, ptb, pte, ctr - 1)) return false;
-                        pending = false;
+                const uint32_t par = ((ctr >> 1) & 1) ^ 1;
+                bool ok = wait(&sb.qk_empty[w], par, abort_flag, status, 0x501);
+                if (!__all_sync(FULL, ok)) return false;
+                const int n_present = 1 + (has_lb ? 1 : 0) + (has_hi ? 1 : 0);
+                if (lane == 0) mbar_expect_tx(&sb.qk_full[w], (uint32_t)(n_present * kC * P.d * 2));
+                __syncwarp();
+#pragma unroll
+                for (int ci = 0; ci < 3; ++ci) {
+                    const bool present = ci == 1 || (ci == 0 ? has_lb : has_hi);
+                    if (!present) continue;
+                    int g[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int row = (4 * lane + k) & 63;
+                        const int a = __shfl_sync(FULL, j[ci][0], row & 31);
+                        const int b = __shfl_sync(FULL, j[ci][1], row & 31);
+                        g[k] = (int)(bh * P.L) + (row < 32 ? a : b);
                     }
-                    if (t == tb && tb > 0 && !need(2 * t - 1)) return false;
-                    if (!need(2 * t)) return false;
-                    const bool hi = 2 * t + 1 < P.nchunks;
-                    if (hi && !need(2 * t + 1)) return false;
-                    const int b = ctr & 1;
-                    if (ctr >= 2 && !wait(&sb.pv_done[b], ((ctr - 2) >> 1) & 1, abort_flag, status, 0x604))
+                    if (lane < 16)
+                        for (int kb = 0; kb < nkb; ++kb)
+                            gather4(smem_u32(QKW + w * wstride + kb * wkb + (ci * kC + 4 * lane) * 128),
+                                    &qmap, kb * 64, g[0], g[1], g[2], g[3], smem_u32(&sb.qk_full[w]));
+                }
+                armed |= 1u << w;
+                armed_par = (armed_par & ~(1u << w)) | (par << w);
+            }
+            return true;
+        });
+    } else if (warp == kSWarp) {
+        // ------------------------------------------------------------- S issuer
+        {
+            const uint32_t qk_base = smem_u32(QKW);
+            const uint32_t idesc = idesc_bf16(kRows, kWin, 0, 0);
+            int ctr = 0;
+            for_items(P, [&](long long, int tb, int te) -> bool {
+                for (int t = tb; t < te; ++t, ++ctr) {
+                    const int w = ctr & 1, b = ctr & 1;
+                    if (!wait_w(&sb.qk_full[w], (ctr >> 1) & 1, abort_flag, status, 0x601)) return false;
+                    if (ctr >= 2 && !wait_w(&sb.pv_done[b], ((ctr - 2) >> 1) & 1, abort_flag, status, 0x604))
                         return false;
                     fence_after_sync();
-                    const int sq = (2 * t) % kSlots;
-                    const int sl = (2 * t + kSlots - 1) % kSlots;
                     for (int ks = 0; ks < P.d / 16; ++ks) {
                         const int kb = ks >> 2, ko = (ks & 3) * 32;
-                        const uint32_t kbase = qk_base + kb * kb_stride + ko;
-                        const uint64_t a = smem_desc(kbase + sq * kC * 128, 16, 1024);
-                        if (t > 0)
-                            mma_ss(tmem + b * kWin, a, smem_desc(kbase + sl * kC * 128, 16, 1024),
-                                   idesc64, ks > 0);
-                        mma_ss(tmem + b * kWin + 64, a, smem_desc(kbase + sq * kC * 128, 16, 1024),
-                               hi ? idesc128 : idesc64, ks > 0);
+                        const uint32_t wb = qk_base + w * wstride + kb * wkb + ko;
+                        mma_ss(tmem + b * kWin, smem_desc(wb + kC * 128, 16, 1024),
+                               smem_desc(wb, 16, 1024), idesc, ks > 0);
                     }
                     mma_commit(smem_u32(&sb.s_full[b]));
-                    if (pending && !do_pv(pt, ptb, pte, ctr - 1)) return false;
-                    pt = t; ptb = tb; pte = te;
-                    pending = true;
-                    ++ctr;
+                    mma_commit(smem_u32(&sb.qk_empty[w]));
                 }
                 return true;
             });
-            if (ok && pending) do_pv(pt, ptb, pte, ctr - 1);
             mma_commit(smem_u32(&sb.mma_done));
             int dummy = 0;
-            wait(&sb.mma_done, 0, &dummy, status, 0x605);
+            wait_w(&sb.mma_done, 0, &dummy, status, 0x605);
         }
-    } else if (warp < 4) {
+    } else if (warp == kPvWarp) {
+        // ------------------------------------------------------------- P V issuer
+        {
+            const uint32_t v_base = smem_u32(V);
+            const uint32_t idesc = idesc_bf16(kRows, P.d, 0, 1);
+            uint32_t v_bits = 0;
+            int ctr = 0;
+            auto needv = [&](int c) -> bool {
+                const int s = c % kSlots;
+                const bool ok = wait_w(&sb.v_full[s], (v_bits >> s) & 1u, abort_flag, status, 0x606);
+                v_bits ^= 1u << s;
+                return ok;
+            };
+            for_items(P, [&](long long, int tb, int te) -> bool {
+                for (int t = tb; t < te; ++t, ++ctr) {
+                    const int q = ctr, b = q & 1;
+                    if (t == tb && tb > 0 && !needv(2 * t - 1)) return false;
+                    if (!needv(2 * t)) return false;
+                    if (2 * t + 1 < P.nchunks && !needv(2 * t + 1)) return false;
+                    if (!wait_w(&sb.p_full[b], (q >> 1) & 1, abort_flag, status, 0x602)) return false;
+                    if (!wait_w(&sb.o_empty, (q & 1) ^ 1, abort_flag, status, 0x603)) return false;
+                    fence_after_sync();
+                    uint32_t acc = 0;
+                    for (int wc = 0; wc < 3; ++wc) {
+                        const int kc = 2 * t - 1 + wc;
+                        if (kc < 0 || kc >= P.nchunks) continue;
+                        const int s = kc % kSlots;
+                        for (int m4 = 0; m4 < 4; ++m4) {
+                            const uint64_t bd = smem_desc(v_base + s * vslot + m4 * 2048, kC * 128, 1024);
+                            mma_ts(tmem + kTmemO, tmem + b * kWin + p_col(4 * wc + m4), bd, idesc, acc);
+                            acc = 1;
+                        }
+                    }
+                    mma_commit(smem_u32(&sb.o_full));
+                    mma_commit(smem_u32(&sb.pv_done[b]));
+                    // release the V rows whose last use was this tile
+                    if (t > 0) mma_commit(smem_u32(&sb.v_empty[(2 * t - 1) % kSlots]));
+                    mma_commit(smem_u32(&sb.v_empty[(2 * t) % kSlots]));
+                    if (t == te - 1 && 2 * t + 1 < P.nchunks)
+                        mma_commit(smem_u32(&sb.v_empty[(2 * t + 1) % kSlots]));
+                }
+                return true;
+            });
+            mma_commit(smem_u32(&sb.mma_done));
+            int dummy = 0;
+            wait_w(&sb.mma_done, 0, &dummy, status, 0x607);
+        }
+    } else if (warp < kSmWarps) {
         // ------------------------------------------------------------- softmax + epilogue
-        const int i = warp * 32 + lane;            // tile row = TMEM lane
+        const int q4 = warp & 3;                   // TMEM lane quarter
+        const int half = warp >> 2;                // which half of the row's columns
+        const int i = q4 * 32 + lane;              // tile row = TMEM lane
         const int hi_half = i >= kC;               // row of chunk 2t+1
-        const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
-        const int col0 = hi_half ? kC : 0;         // first S column this row may use
+        const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
+        const int colA = (hi_half ? kC : 0) + 64 * half;   // this warp's 64 S columns
+        // the third of the window outside the row's reach, zeroed by one of the halves
+        const int colZ = (hi_half ? 0 : 2 * kC) + 32 * half;
+        const int self_c0 = kC + 32 * q4;          // batch holding the rows' own columns
+        const int dh = P.d / 2;                    // O columns of this warp
         uint32_t full_bits = 0;
         int ctr = 0;
         // epilogue state of the previous tile
-        long long e_row = -1, e_vrow = 0;
-        float e_l = 0.f, e_lse = 0.f;
-        bool e_live = false;
+        long long e_row = -1;
+        float e_m2 = 0.f;
+        bool e_live = false, e_self = false;
         bool ok = true;
+        const uint32_t zero16[16] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
 
         auto epilogue = [&](int q) -> bool {
             bool w = wait(&sb.o_full, q & 1, abort_flag, status, 0x702);
+            // p_full of tile q (complete by now) orders the partner warp's partial sum
+            w = w && wait(&sb.p_full[q & 1], (q >> 1) & 1, abort_flag, status, 0x704);
             if (!__all_sync(FULL, w)) return false;
             fence_after_sync();
-            const float inv_l = e_l > 0.f ? 1.f / e_l : 0.f;
-            for (int c = 0; c < P.d; c += 32) {
+            LSH_SPAN_BEGIN(t_ep);
+            const float l = l_part[q % kLBufs][0][i] + l_part[q % kLBufs][1][i];
+            const float inv_l = l > 0.f ? 1.f / l : 0.f;
+            __nv_bfloat16 *dst = o_r + LSH_IDX(e_row, (long long)n_rows, 0x712) * P.d + half * dh;
+            for (int c = 0; c < dh; c += 32) {
                 uint32_t o[32];
-                tmem_ld32(tl + kTmemO + c, o);
-                tmem_wait_ld();
+                tmem_ld32(tl + kTmemO + half * dh + c, o);
+                tmem_wait_ld(o);
                 if (e_live) {
                     uint32_t pk[16];
-                    if (e_l > 0.f) {
 #pragma unroll
-                        for (int k = 0; k < 16; ++k)
-                            pk[k] = pack_bf16(__uint_as_float(o[2 * k]) * inv_l,
-                                              __uint_as_float(o[2 * k + 1]) * inv_l);
-                    } else {
-                        const uint4 *src = reinterpret_cast<const uint4 *>(
-                            v + LSH_IDX(e_vrow, (long long)P.n_heads * P.L, 0x711) * P.d + c);
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const uint4 x = src[k];
-                            pk[4 * k] = x.x; pk[4 * k + 1] = x.y; pk[4 * k + 2] = x.z; pk[4 * k + 3] = x.w;
-                        }
-                    }
-                    uint4 *dst = reinterpret_cast<uint4 *>(
-                        o_r + LSH_IDX(e_row, (long long)P.n_heads * P.n_rounds * P.L, 0x712) * P.d + c);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+                    for (int k = 0; k < 16; ++k)
+                        pk[k] = pack_bf16(__uint_as_float(o[2 * k]) * inv_l,
+                                          __uint_as_float(o[2 * k + 1]) * inv_l);
+                    st_global_v8(dst + c, pk);
+                    st_global_v8(dst + c + 16, pk + 8);
                 }
             }
-            if (e_live) lse_r[LSH_IDX(e_row, (long long)P.n_heads * P.n_rounds * P.L, 0x713)] = e_lse;
+            if (e_live && half == 0)
+                lse_r[LSH_IDX(e_row, (long long)n_rows, 0x713)] =
+                    e_self ? kSelfLogit : (e_m2 + __log2f(l)) * kLn2;
+            LSH_SPAN_END(t_ep, 0x783);
             fence_before_sync();
             mbar_arrive(&sb.o_empty);
             return true;
         };
 
         ok = for_items(P, [&](long long seg, int tb, int te) -> bool {
-            const long long bh = seg / P.n_rounds;
             for (int t = tb; t < te; ++t) {
                 auto need = [&](int c) -> bool {
                     const int s = c % kSlots;
-                    bool w = wait(&sb.chunk_full[s], (full_bits >> s) & 1u, abort_flag, status, 0x701);
+                    bool w = wait(&sb.v_full[s], (full_bits >> s) & 1u, abort_flag, status, 0x701);
                     full_bits ^= 1u << s;
                     return __all_sync(FULL, w);
                 };
@@ -413,96 +494,103 @@ lsh_attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                 if (!__all_sync(FULL, w)) return false;
                 fence_after_sync();
 
-                // this row
-                const int cq = 2 * t + hi_half;                 // its chunk
-                const long long srow = (long long)t * kRows + i;  // sorted index
+                // this row: its keys are the sorted indices [klo, khi) (minus itself when
+                // not causal); the window of a row of chunk cq is chunks cq-1 and cq
+                const int cq = 2 * t + hi_half;
+                const int srow = t * kRows + i;
                 const bool live = cq < P.nchunks;
                 const SlotMeta &mq = meta[cq % kSlots];
                 const int r = i & (kC - 1);
-                const int bq = live ? mq.sb[r] : -1;
-                const int jq = live ? mq.j[r] : 0;
-                float m2 = live ? mq.m2[r] : 0.f;
-                const long long tk0 = (long long)(2 * t - 1) * kC;  // sorted index of column 0
+                int klo = 0, khi = 0;
+                float m2 = 0.f;
+                if (live) {
+                    const int wlo = cq > 0 ? (cq - 1) * kC : 0;
+                    klo = max(wlo, mq.blo[r]);
+                    khi = P.causal ? srow : min((cq + 1) * kC, mq.bhi[r]);
+                    m2 = mq.m2[r];
+                }
+                // keys other than the row itself?
+                const bool self_only = live && (P.causal ? klo >= khi : khi - klo <= 1);
+                const int tk0 = (2 * t - 1) * kC;          // sorted index of S column 0
                 const uint32_t sbase = tl + b * kWin;
 
-                // per 32-column batch: does any row of the warp have a candidate in it?
                 auto batch_needed = [&](int c0) -> bool {
-                    const long long t0 = tk0 + c0;
-                    const int kc = 2 * t - 1 + c0 / kC;
-                    bool need_b = false;
-                    if (live && kc >= 0 && kc < P.nchunks) {
-                        const SlotMeta &mk = meta[kc % kSlots];
-                        const int rk = c0 & (kC - 1);
-                        need_b = mk.sb[rk] <= bq && bq <= mk.sb[rk + 31] &&
-                                 (!P.causal || t0 < srow);
-                    }
-                    return __any_sync(FULL, need_b);
+                    const int t0 = tk0 + c0;
+                    const bool nb = (live && klo < t0 + 32 && khi > t0 && klo < khi) ||
+                                    (self_only && c0 == self_c0);
+                    return __any_sync(FULL, nb);
                 };
 
-                // optional exact maximum (huge |scale| |q|)
+                // optional exact maximum (huge |scale| |q|): both halves must agree on m2,
+                // so the warp pair computes it over the row's whole range
                 if (__any_sync(FULL, live && m2 > kExactMaxLog2)) {
                     float mx = -INFINITY;
-                    for (int c0 = col0; c0 < col0 + 2 * kC; c0 += 32) {
+                    const int cfull = hi_half ? kC : 0;
+                    for (int c0 = cfull; c0 < cfull + 2 * kC; c0 += 32) {
                         if (!batch_needed(c0)) continue;
                         uint32_t s32[32];
                         tmem_ld32(sbase + c0, s32);
-                        tmem_wait_ld();
+                        tmem_wait_ld(s32);
                         const SlotMeta &mk = meta[(2 * t - 1 + c0 / kC + kSlots) % kSlots];
                         const int rk = c0 & (kC - 1);
 #pragma unroll
                         for (int jj = 0; jj < 32; ++jj) {
-                            const long long tj = tk0 + c0 + jj;
-                            const bool ok_j = mk.sb[rk + jj] == bq &&
-                                              (P.causal ? tj < srow : tj != srow);
-                            if (ok_j) mx = fmaxf(mx, __uint_as_float(s32[jj]) * mk.cs[rk + jj]);
+                            const int tj = tk0 + c0 + jj;
+                            const bool okj = tj >= klo && tj < khi && (P.causal || tj != srow);
+                            if (okj) mx = fmaxf(mx, __uint_as_float(s32[jj]) * mk.cs[rk + jj]);
                         }
                     }
                     m2 = mx == -INFINITY ? 0.f : mx;
+                    // The pass read the partner warp's S columns: both warps of the lane
+                    // quarter (which take this branch together: same rows, same bound)
+                    // finish reading before either overwrites S with P.
+                    named_bar_sync(1 + q4, 64);
                 }
 
+                LSH_SPAN_BEGIN(t_sm);
                 float l = 0.f;
-                const uint32_t zero16[16] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
-                if (hi_half) tmem_st16(sbase + 0, zero16), tmem_st16(sbase + 16, zero16);
-                for (int c0 = col0; c0 < col0 + 2 * kC; c0 += 32) {
-                    if (!batch_needed(c0)) {
-                        tmem_st16(sbase + c0 / 2, zero16);
-                        continue;
-                    }
-                    uint32_t s32[32];
-                    tmem_ld32(sbase + c0, s32);
-                    tmem_wait_ld();
-                    const SlotMeta &mk = meta[(2 * t - 1 + c0 / kC + kSlots) % kSlots];
-                    const int rk = c0 & (kC - 1);
-                    const long long tbase = tk0 + c0;
-                    uint32_t pk[16];
+                const unsigned len = live ? (unsigned)(khi - klo) : 0u;
+                // both 32-column batches in flight before one wait
+                const bool nb0 = batch_needed(colA), nb1 = batch_needed(colA + 32);
+                uint32_t s32[2][32];
+                if (nb0) tmem_ld32(sbase + colA, s32[0]);
+                if (nb1) tmem_ld32(sbase + colA + 32, s32[1]);
+                if (nb0 || nb1) tmem_wait_ld(s32[0], s32[1]);
+                LSH_SPAN_END(t_sm, 0x784);
+                LSH_SPAN_BEGIN(t_c);
+                uint32_t pkk[2][16];
+                bool wr[2] = {false, false};
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        float p2[2];
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const int jj = 2 * k + h;
-                            const long long tj = tbase + jj;
-                            const bool ok_j = live && mk.sb[rk + jj] == bq &&
-                                              (P.causal ? tj < srow : tj != srow);
-                            const float x = fmaf(__uint_as_float(s32[jj]), mk.cs[rk + jj], -m2);
-                            p2[h] = ok_j ? ex2(x) : 0.f;
-                        }
-                        pk[k] = pack_bf16(p2[0], p2[1]);
-                        l += bf16_lo(pk[k]) + bf16_hi(pk[k]);
-                    }
-                    tmem_st16(sbase + c0 / 2, pk);
+                for (int h = 0; h < 2; ++h) {
+                    const int cc = colA + 32 * h;
+                    if (!(h ? nb1 : nb0)) continue;
+                    const SlotMeta &mk = meta[(2 * t - 1 + cc / kC + kSlots) % kSlots];
+                    const float *cs = mk.cs + (cc & (kC - 1));
+                    const int off = tk0 + cc - klo;        // key jj is valid iff jj + off in [0, len)
+                    if (cc == self_c0)   // the rows' own columns are in this batch: self rules
+                        l += softmax_batch<true>(s32[h], cs, off, len, P.causal ? -1 : lane,
+                                                 self_only ? lane : -1, m2, pkk[h]);
+                    else
+                        l += softmax_batch<false>(s32[h], cs, off, len, -1, -1, m2, pkk[h]);
+                    wr[h] = true;
                 }
-                if (!hi_half) tmem_st16(sbase + 64, zero16), tmem_st16(sbase + 80, zero16);
+                LSH_SPAN_END(t_c, 0x785);
+                LSH_SPAN_BEGIN(t_st2);
+                if (wr[0]) tmem_st16(sbase + colA, pkk[0]); else tmem_st16(sbase + colA, zero16);
+                if (wr[1]) tmem_st16(sbase + colA + 32, pkk[1]); else tmem_st16(sbase + colA + 32, zero16);
+                LSH_SPAN_END(t_st2, 0x786);
+                LSH_SPAN_END(t_sm, 0x781);
+                tmem_st16(sbase + colZ, zero16);
+                l_part[ctr % kLBufs][half][i] = l;
                 tmem_wait_st();
                 fence_before_sync();
                 mbar_arrive(&sb.p_full[b]);
 
                 if (ctr >= 1 && !epilogue(ctr - 1)) return false;
                 e_live = live;
-                e_row = (long long)seg * P.L + srow;
-                e_vrow = bh * P.L + jq;
-                e_l = l;
-                e_lse = l > 0.f ? (m2 + __log2f(l)) * kLn2 : kSelfLogit;
+                e_row = seg * P.L + srow;
+                e_m2 = m2;
+                e_self = self_only;
                 ++ctr;
             }
             return true;
@@ -512,21 +600,23 @@ lsh_attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
 
     fence_before_sync();
     __syncthreads();
-    if (warp == kMmaWarp) {
+    if (warp == kSWarp) {
         __syncwarp();
         fence_after_sync();
         tmem_dealloc(tmem, 512);
     }
-    if (*abort_flag && warp >= 4 && warp < 4 + kLoaders) {
-        // Wind-down after a timeout: the gathers this warp issued last into each slot may
-        // still be in flight (no consumer waited for them); let them land before the CTA
-        // exits.  A fill that was consumed and refilled has landed already; its stale
-        // phase is skipped by the bounded wait.
-        for (int s = 0; s < kSlots; ++s) {
-            if (!(loader_armed & (1u << s))) continue;
+    if (*abort_flag && warp >= kSmWarps && warp <= kQkWarp) {
+        // Wind-down after a timeout: the gathers a loader issued last into each of its
+        // slots (or windows) may still be in flight (no consumer waited for them); let
+        // them land before the CTA exits.  A fill that was consumed and refilled has
+        // landed already; its stale phase is skipped by the bounded wait.
+        const bool qk = warp == kQkWarp;
+        for (int s = 0; s < (qk ? 2 : kSlots); ++s) {
+            if (!(armed & (1u << s))) continue;
             int dummy = 0;
-            const uint32_t fp = ((loader_armed_par >> s) & 1u) ^ 1u;  // chunk_full parity of that fill
-            wait(&sb.chunk_full[s], fp, &dummy, nullptr, 0x502);
+            // a fill waited on parity p of the empty barrier; its full phase has parity p ^ 1
+            const uint32_t fp = ((armed_par >> s) & 1u) ^ 1u;
+            wait(qk ? &sb.qk_full[s] : &sb.v_full[s], fp, &dummy, nullptr, 0x502);
         }
     }
 }
@@ -550,7 +640,8 @@ bool make_plan(const Problem &p, AttnPlan &P)
 size_t smem_bytes(const AttnPlan &P)
 {
     const int nkb = P.d / 64;
-    return 1024 + (size_t)nkb * kSlots * kC * 128 * 2 + (size_t)kSlots * sizeof(SlotMeta);
+    return 1024 + (size_t)2 * nkb * kWin * 128 + (size_t)kSlots * nkb * kC * 128 +
+           (size_t)kSlots * sizeof(SlotMeta);
 }
 
 }  // namespace
@@ -564,7 +655,6 @@ cudaError_t attn_tc(const Problem &p, const void *qk, const void *v, const int32
                     const int32_t *perm, const int32_t *bstart, const float *inv_norm, void *o_r,
                     float *lse_r, StatusBlock *status, cudaStream_t st)
 {
-    (void)bstart;
     AttnPlan P;
     make_plan(p, P);
     CUtensorMap qmap, vmap;
@@ -577,9 +667,8 @@ cudaError_t attn_tc(const Problem &p, const void *qk, const void *v, const int32
     cudaError_t e = cudaFuncSetAttribute(lsh_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    lsh_attn_tc_kernel<<<sms, kThreads, smem, st>>>(qmap, vmap, P, buckets, perm, inv_norm,
-                                                    (const __nv_bfloat16 *)v, (__nv_bfloat16 *)o_r,
-                                                    lse_r, status);
+    lsh_attn_tc_kernel<<<sms, kThreads, smem, st>>>(qmap, vmap, P, buckets, perm, bstart, inv_norm,
+                                                    (__nv_bfloat16 *)o_r, lse_r, status);
     return cudaGetLastError();
 }
 

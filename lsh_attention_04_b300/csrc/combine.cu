@@ -8,8 +8,11 @@
 // logsumexp weighting is the standard way to merge softmax results computed over
 // separate key sets.)
 //
-// One warp per token; each lane owns D/32 consecutive elements, read with one 4- to
-// 16-byte vector load, so every row is read in one coalesced access.
+// One warp per token.  Lane r fetches inv_r[i] and lse_r of round r (all rounds at
+// once, so the index lookups cost one dependent round trip, not one per round), the
+// warp reduces the weights with shuffles, and then every round's row is requested
+// before any is accumulated (up to 8 rows in flight per warp).  Each lane owns D/32
+// consecutive elements of a row: one 4- to 16-byte vector load per row.
 #include <math.h>
 
 #include "internal.cuh"
@@ -18,25 +21,30 @@ namespace lsh {
 namespace {
 
 constexpr int kWarps = 8;
+constexpr int kRowsInFlight = 8;
 
-__device__ __forceinline__ void load_row(const float *p, float (&x)[2]) {
-    const float2 t = *reinterpret_cast<const float2 *>(p);
-    x[0] = t.x; x[1] = t.y;
+template <int EPL>
+__device__ __forceinline__ void load_row(const float *p, float (&x)[EPL]) {
+    if constexpr (EPL == 4) {
+        const float4 t = __ldg(reinterpret_cast<const float4 *>(p));
+        x[0] = t.x; x[1] = t.y; x[2] = t.z; x[3] = t.w;
+    } else {
+        const float2 t = __ldg(reinterpret_cast<const float2 *>(p));
+        x[0] = t.x; x[1] = t.y;
+    }
 }
-__device__ __forceinline__ void load_row(const float *p, float (&x)[4]) {
-    const float4 t = *reinterpret_cast<const float4 *>(p);
-    x[0] = t.x; x[1] = t.y; x[2] = t.z; x[3] = t.w;
-}
-__device__ __forceinline__ void load_row(const __nv_bfloat16 *p, float (&x)[2]) {
-    const __nv_bfloat162 t = *reinterpret_cast<const __nv_bfloat162 *>(p);
-    const float2 f = __bfloat1622float2(t);
-    x[0] = f.x; x[1] = f.y;
-}
-__device__ __forceinline__ void load_row(const __nv_bfloat16 *p, float (&x)[4]) {
-    const uint2 t = *reinterpret_cast<const uint2 *>(p);
-    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&t.x));
-    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&t.y));
-    x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+template <int EPL>
+__device__ __forceinline__ void load_row(const __nv_bfloat16 *p, float (&x)[EPL]) {
+    if constexpr (EPL == 4) {
+        const uint2 t = __ldg(reinterpret_cast<const uint2 *>(p));
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&t.x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&t.y));
+        x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+    } else {
+        const uint32_t t = __ldg(reinterpret_cast<const unsigned int *>(p));
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&t));
+        x[0] = a.x; x[1] = a.y;
+    }
 }
 
 template <typename T, int D>
@@ -53,31 +61,60 @@ combine_kernel(const T *__restrict__ o_r, const float *__restrict__ lse_r,
     const int i = (int)(tok % L);
     const size_t seg0 = (size_t)bh * n_rounds;
 
+    // pass 1: lane r looks up round r (rounds beyond 32 are folded in 32 at a time)
     float mx = -INFINITY;
-    for (int r = 0; r < n_rounds; ++r) {
-        const size_t base = (seg0 + r) * L;
-        mx = fmaxf(mx, lse_r[base + inv[base + i]]);
+    for (int r0 = 0; r0 < n_rounds; r0 += 32) {
+        const int r = r0 + lane;
+        if (r < n_rounds) {
+            const size_t base = (seg0 + r) * L;
+            mx = fmaxf(mx, __ldg(lse_r + base + __ldg(inv + base + i)));
+        }
     }
+    mx = warp_max(mx);
     float acc[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
     float sum = 0.f;
-    for (int r = 0; r < n_rounds; ++r) {
-        const size_t base = (seg0 + r) * L;
-        const int s = inv[base + i];
-        const float w = expf(lse_r[base + s] - mx);
-        sum += w;
-        float x[EPL];
-        load_row(o_r + (base + s) * D + lane * EPL, x);
+    for (int r0 = 0; r0 < n_rounds; r0 += 32) {
+        const int r = r0 + lane;
+        int s = 0;
+        float w = 0.f;
+        if (r < n_rounds) {
+            const size_t base = (seg0 + r) * L;
+            s = __ldg(inv + base + i);
+            w = expf(__ldg(lse_r + base + s) - mx);
+        }
+        sum += warp_sum(w);
+        const int nr = min(32, n_rounds - r0);
+        // pass 2: rows of up to kRowsInFlight rounds requested before any is used
+        for (int q0 = 0; q0 < nr; q0 += kRowsInFlight) {
+            float x[kRowsInFlight][EPL];
+            float wq[kRowsInFlight];
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) acc[e] = fmaf(w, x[e], acc[e]);
+            for (int q = 0; q < kRowsInFlight; ++q) {
+                const int rr = q0 + q;
+                const int sq = __shfl_sync(0xffffffffu, s, rr & 31);
+                wq[q] = __shfl_sync(0xffffffffu, w, rr & 31);
+                if (rr < nr) {
+                    load_row<EPL>(o_r + ((seg0 + r0 + rr) * L + sq) * D + lane * EPL, x[q]);
+                } else {
+                    wq[q] = 0.f;
+#pragma unroll
+                    for (int e = 0; e < EPL; ++e) x[q][e] = 0.f;
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < kRowsInFlight; ++q)
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) acc[e] = fmaf(wq[q], x[q][e], acc[e]);
+        }
     }
     const float rs = 1.0f / sum;
     float *dst = out + (size_t)tok * D + lane * EPL;
     if constexpr (EPL == 4) {
-        *reinterpret_cast<float4 *>(dst) = make_float4(acc[0] * rs, acc[1] * rs, acc[2] * rs, acc[3] * rs);
+        __stcs(reinterpret_cast<float4 *>(dst), make_float4(acc[0] * rs, acc[1] * rs, acc[2] * rs, acc[3] * rs));
     } else {
-        *reinterpret_cast<float2 *>(dst) = make_float2(acc[0] * rs, acc[1] * rs);
+        __stcs(reinterpret_cast<float2 *>(dst), make_float2(acc[0] * rs, acc[1] * rs));
     }
     if (lane == 0) lse[tok] = mx + logf(sum);
 }

@@ -9,8 +9,8 @@
 // The projection x.R_r is a dense contraction, so it runs on the tensor cores:
 //  * The columns of all rounds are laid out one round after another (each round padded
 //    to a multiple of 32 columns with zero columns that never win) and cut into MMA
-//    chunks of at most 256 columns: several whole rounds per chunk when a round has at
-//    most 256 columns, otherwise 256-column parts of one round.
+//    chunks of at most 128 columns: several whole rounds per chunk when a round has at
+//    most 128 columns, otherwise 128-column parts of one round.
 //  * Consecutive rounds form a "group" whose packed R image (<= 128 KB) stays resident in
 //    shared memory for the whole kernel.  A pre-pass (lsh_rpack_kernel) writes that image
 //    in the canonical K-major 128-byte-swizzled layout, so one bulk TMA copy stages it.
@@ -18,18 +18,20 @@
 //    order, so the CTAs of all groups read a tile of qk within a short time window and
 //    only the first one fetches it from HBM (the others hit L2).
 //  * Warp roles: warp 8 issues TMA loads of the qk tile (2-D tensor map, 128-byte
-//    swizzle, 2 stages); warp 9 (one thread) issues tcgen05.mma M=128 x N=chunk x K=16
-//    into one of two 256-column TMEM accumulators; warps 0-3 and 4-7 (two epilogue
-//    warpgroups, one per accumulator) read the projections with tcgen05.ld and keep, per
-//    token and round, the entry of largest magnitude (first index on ties); warp 10
-//    computes 1/|x| of each token from the staged tile (first group only).
+//    swizzle, 2-4 stages); warps 10-13 (one thread each) issue tcgen05.mma M=128 x N=chunk
+//    x K=16 into four 128-column TMEM accumulators, warp 10+b owning accumulator b: one
+//    issuing thread manages about one MMA per few hundred cycles whatever N is, so the
+//    independent chains are issued from separate warps; warps 0-3 and 4-7 (two epilogue
+//    warpgroups, taking even and odd tiles) read the projections with tcgen05.ld and
+//    keep, per token and round, the entry of largest magnitude (first index on ties);
+//    warp 9 computes 1/|x| of each token from the staged tile (first group only).
 //  * Bucket rule: the largest entry of [p, -p] is the entry of p with the largest |p_j|,
 //    taken with its sign: bucket = j if p_j >= 0, n_buckets/2 + j otherwise.  Scanning j
 //    in order with a strict comparison keeps the first index.  Two entries of equal
 //    magnitude and opposite sign have a zero top-1/top-2 margin, i.e. they are a near-tie.
-//  * When a round spans chunks of both warpgroups, each keeps its partial (value, index)
-//    in shared memory (double-buffered by tile parity) and warpgroup 0 merges them; two
-//    mbarriers per buffer (full: both warpgroups flushed; empty: merged) order it.
+//  * Each 128-token tile goes to one epilogue warpgroup (alternating), which reads every
+//    chunk of it and so sees each round whole; its chunks alternate between the
+//    warpgroup's two accumulators, so the MMAs of one run while the other is scanned.
 // Every wait is bounded (see sm100::wait); on a timeout the kernel records the place in
 // the workspace status block and winds down.
 #include <math.h>
@@ -42,11 +44,13 @@ namespace {
 using namespace sm100;
 
 constexpr int kTileM = 128;          // tokens per tile = MMA M = TMEM lanes
-constexpr int kChunkMax = 256;       // MMA N per chunk (TMEM columns per accumulator)
+constexpr int kChunkMax = 128;       // MMA N per chunk (TMEM columns per accumulator)
+constexpr int kTmemBufs = 4;         // accumulators: 4 x 128 TMEM columns
 constexpr int kRCapBytes = 128 * 1024;
-constexpr int kXStages = 2;
-constexpr int kThreads = 11 * 32;    // 8 epilogue warps, producer, MMA, norm
-constexpr int kMaxSplitRounds = 3;   // rounds per group when rounds span chunks
+constexpr int kMaxXStages = 4;         // qk tile stages (as many as shared memory holds)
+constexpr size_t kSmemCap = 227 * 1024;
+constexpr int kMmaWarps = kTmemBufs; // one MMA-issuing warp per accumulator
+constexpr int kThreads = (10 + kMmaWarps) * 32;  // 8 epilogue warps, producer, norm, MMA
 
 struct HashPlan {
     long long n_tok;
@@ -55,6 +59,7 @@ struct HashPlan {
     int rpc, cpr, rpg;    // rounds per chunk, chunks per round, rounds per group
     int n_groups, ctas_per_group, n_tiles;
     int group_bytes;      // bytes of one group's packed R image (stride in rpack)
+    int x_stages;         // qk tile stages in shared memory
 };
 
 // ---- geometry of chunk k of a group with nr rounds (host and device) ----
@@ -98,9 +103,8 @@ lsh_rpack_kernel(const __nv_bfloat16 *__restrict__ R, HashPlan P, uint8_t *__res
 
 // ---- the hash kernel ----
 struct __align__(8) HashBarriers {
-    uint64_t x_full[kXStages], x_empty[kXStages];
-    uint64_t tm_full[2], tm_empty[2];
-    uint64_t parts_full[2], parts_empty[2];
+    uint64_t x_full[kMaxXStages], x_empty[kMaxXStages];
+    uint64_t tm_full[kTmemBufs], tm_empty[kTmemBufs];
     uint64_t r_full, mma_done;
     uint32_t tmem_base;
     int abort_flag;
@@ -112,22 +116,49 @@ __device__ __forceinline__ void write_bucket(int32_t *buckets, const HashPlan &P
     buckets[((size_t)bh * P.n_rounds + r) * P.L + l] = best >= 0.f ? bidx : P.half + bidx;
 }
 
-// Keep the entry of largest magnitude of 32 projections (columns j0 .. j0+31 of a round),
-// first index on ties; only the first `nvalid` columns count.
-__device__ __forceinline__ void scan32(const uint32_t (&v)[32], int j0, int nvalid, float &best,
-                                       int &bidx) {
-    if (nvalid >= 32) {
+// Entry of largest magnitude among 32 projections (columns j0 .. j0+31 of a round), first
+// index on ties, merged into the running (best, bidx).  A pairwise tree (depth 5) keeps the
+// dependency chains short; at every merge the left (earlier) operand wins ties, so the
+// result is the first index of the largest |p|.  Zero-padding columns project to exactly 0
+// and can never win against an earlier column.
+__device__ __forceinline__ void scan32(const uint32_t (&v)[32], int j0, float &best, int &bidx) {
+    float b[16];
+    int ix[16];
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-            const float x = __uint_as_float(v[jj]);
-            if (fabsf(x) > fabsf(best)) { best = x; bidx = j0 + jj; }
-        }
-    } else {
+    for (int k = 0; k < 16; ++k) {
+        const float x0 = __uint_as_float(v[2 * k]), x1 = __uint_as_float(v[2 * k + 1]);
+        const bool t = fabsf(x1) > fabsf(x0);
+        b[k] = t ? x1 : x0;
+        ix[k] = 2 * k + (t ? 1 : 0);
+    }
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-            const float x = __uint_as_float(v[jj]);
-            if (jj < nvalid && fabsf(x) > fabsf(best)) { best = x; bidx = j0 + jj; }
+    for (int w = 8; w >= 1; w >>= 1) {
+#pragma unroll
+        for (int k = 0; k < w; ++k) {
+            const bool t = fabsf(b[2 * k + 1]) > fabsf(b[2 * k]);
+            b[k] = t ? b[2 * k + 1] : b[2 * k];
+            ix[k] = t ? ix[2 * k + 1] : ix[2 * k];
         }
+    }
+    if (fabsf(b[0]) > fabsf(best)) { best = b[0]; bidx = j0 + ix[0]; }
+}
+
+// One 32-column batch of the epilogue: (r, j) is the round and the column within it of
+// the batch's first column; the bucket is written when the round's last batch is done.
+__device__ __forceinline__ void scan_batch(const uint32_t (&v)[32], const HashPlan &P, int &r, int &j,
+                                           int &cur, float &best, int &bidx, bool live,
+                                           int32_t *buckets, long long tok, int r0) {
+    if (r != cur) {
+        cur = r;
+        best = 0.f;
+        bidx = 0;
+    }
+    scan32(v, j, best, bidx);
+    j += 32;
+    if (j >= P.hp) {
+        if (live) write_bucket(buckets, P, tok, r0 + r, best, bidx);
+        j = 0;
+        ++r;
     }
 }
 
@@ -138,12 +169,12 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
 {
     extern __shared__ uint8_t smem_raw[];
     __shared__ HashBarriers sb;
-    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    // 1024-byte aligned base, derived from the shared array by pointer arithmetic so the
+    // compiler keeps the shared state space (shared loads, not generic ones)
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int x_bytes = kTileM * P.d * 2;
     uint8_t *Rs = smem;
     uint8_t *Xs = smem + P.group_bytes;  // group_bytes is a multiple of 1024
-    float *part_best = (float *)(Xs + kXStages * x_bytes);          // [2][2][kMaxSplitRounds][128]
-    int *part_idx = (int *)(part_best + 2 * 2 * kMaxSplitRounds * kTileM);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = blockIdx.x / P.ctas_per_group;
@@ -154,20 +185,16 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
     volatile int *abort_flag = &sb.abort_flag;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kXStages; ++s) {
+        for (int s = 0; s < P.x_stages; ++s) {
             mbar_init(&sb.x_full[s], 1);
-            mbar_init(&sb.x_empty[s], g == 0 ? 2 : 1);
+            mbar_init(&sb.x_empty[s], kMmaWarps + (g == 0 ? 1 : 0));
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kTmemBufs; ++b) {
             mbar_init(&sb.tm_full[b], 1);
             mbar_init(&sb.tm_empty[b], 128);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&sb.parts_full[b], 256);
-            mbar_init(&sb.parts_empty[b], 128);
-        }
         mbar_init(&sb.r_full, 1);
-        mbar_init(&sb.mma_done, 1);
+        mbar_init(&sb.mma_done, kMmaWarps);
         sb.abort_flag = 0;
         mbar_fence_init();
     }
@@ -189,8 +216,8 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
             uint32_t pending = 0;  // stages with a fill in flight (for the wind-down)
             int it = 0;
             for (int t = cj; t < P.n_tiles; t += P.ctas_per_group, ++it) {
-                const int s = it % kXStages;
-                const uint32_t ph = (it / kXStages) & 1;
+                const int s = it % P.x_stages;
+                const uint32_t ph = (it / P.x_stages) & 1;
                 if (!wait(&sb.x_empty[s], ph ^ 1, abort_flag, status, 0x101)) break;
                 mbar_expect_tx(&sb.x_full[s], (uint32_t)x_bytes);
                 for (int kb = 0; kb < P.d / 64; ++kb)
@@ -200,10 +227,10 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
             }
             // wind-down: every issued copy has landed before the CTA exits
             int last = it - 1;
-            for (int k = 0; k < kXStages && last - k >= 0; ++k) {
-                const int i2 = last - k, s = i2 % kXStages;
+            for (int k = 0; k < P.x_stages && last - k >= 0; ++k) {
+                const int i2 = last - k, s = i2 % P.x_stages;
                 if (pending & (1u << s)) {
-                    const uint32_t ph = (i2 / kXStages) & 1;
+                    const uint32_t ph = (i2 / P.x_stages) & 1;
                     int dummy = 0;
                     wait(&sb.x_full[s], ph, &dummy, status, 0x102);
                 }
@@ -211,50 +238,61 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
             int dummy = 0;
             wait(&sb.r_full, 0, &dummy, status, 0x103);
         }
-    } else if (warp == 9) {
-        // ---------------- MMA issuer ----------------
-        if (lane == 0) {
-            bool ok = wait(&sb.r_full, 0, abort_flag, status, 0x201);
+    } else if (warp >= 10) {
+        // ---------------- MMA issuers: warp 10+b owns accumulator b ----------------
+        // Each issuer is a whole converged warp (the MMA wrappers elect one lane).  Chains
+        // on separate accumulators issued from separate warps overlap.  Tile `it` belongs
+        // to epilogue warpgroup it & 1, whose chunks alternate between its accumulators
+        // 2(it & 1) and 2(it & 1) + 1.
+        {
+            const int mi = warp - 10;
+            const int me = mi >> 1, mp = mi & 1;
+            const int n_mine = (nch + 1 - mp) / 2;   // chunks of a tile that use this accumulator
+            bool ok = wait_w(&sb.r_full, 0, abort_flag, status, 0x201);
             fence_after_sync();
-            uint32_t chunk_ctr = 0;
             int it = 0;
             const uint32_t rs = smem_u32(Rs), xs = smem_u32(Xs);
             for (int t = cj; ok && t < P.n_tiles; t += P.ctas_per_group, ++it) {
-                const int s = it % kXStages;
-                if (!(ok = wait(&sb.x_full[s], (it / kXStages) & 1, abort_flag, status, 0x202))) break;
+                const int s = it % P.x_stages;
+                if (!(ok = wait_w(&sb.x_full[s], (it / P.x_stages) & 1, abort_flag, status, 0x202))) break;
                 fence_after_sync();
-                for (int k = 0; k < nch; ++k, ++chunk_ctr) {
-                    const int b = chunk_ctr & 1;
-                    if (!(ok = wait(&sb.tm_empty[b], ((chunk_ctr >> 1) & 1) ^ 1, abort_flag, status,
-                                    0x203)))
-                        break;
-                    fence_after_sync();
-                    const int width = chunk_width(P, nr, k);
-                    const uint32_t idesc = idesc_bf16(kTileM, width, 0, 0);
-                    const uint32_t rbase = rs + chunk_col0(P, k) * P.d * 2;
-                    for (int ks = 0; ks < P.d / 16; ++ks) {
-                        const int kb = ks >> 2, ko = (ks & 3) * 32;
-                        const uint64_t a = smem_desc(xs + s * x_bytes + kb * kTileM * 128 + ko, 16, 1024);
-                        const uint64_t bd = smem_desc(rbase + kb * width * 128 + ko, 16, 1024);
-                        mma_ss(tmem + b * kChunkMax, a, bd, idesc, ks > 0);
+                bool touched = false;
+                if ((it & 1) == me) {
+                    for (int k = mp; k < nch; k += 2) {
+                        const int use = (it >> 1) * n_mine + (k >> 1);
+                        if (!(ok = wait_w(&sb.tm_empty[mi], (use & 1) ^ 1, abort_flag, status, 0x203))) break;
+                        fence_after_sync();
+                        const int width = chunk_width(P, nr, k);
+                        const uint32_t idesc = idesc_bf16(kTileM, width, 0, 0);
+                        const uint32_t rbase = rs + chunk_col0(P, k) * P.d * 2;
+                        for (int ks = 0; ks < P.d / 16; ++ks) {
+                            const int kb = ks >> 2, ko = (ks & 3) * 32;
+                            const uint64_t a = smem_desc(xs + s * x_bytes + kb * kTileM * 128 + ko, 16, 1024);
+                            const uint64_t bd = smem_desc(rbase + kb * width * 128 + ko, 16, 1024);
+                            mma_ss(tmem + mi * kChunkMax, a, bd, idesc, ks > 0);
+                        }
+                        mma_commit(smem_u32(&sb.tm_full[mi]));
+                        touched = true;
                     }
-                    mma_commit(smem_u32(&sb.tm_full[b]));
                 }
                 if (!ok) break;
-                mma_commit(smem_u32(&sb.x_empty[s]));
+                // this warp is done with the staged tile once its MMAs (if any) complete
+                if (touched) mma_commit(smem_u32(&sb.x_empty[s]));
+                else if (lane == 0) mbar_arrive(&sb.x_empty[s]);
+                __syncwarp();
             }
             // wind-down: all issued MMAs complete before TMEM is released
             mma_commit(smem_u32(&sb.mma_done));
             int dummy = 0;
-            wait(&sb.mma_done, 0, &dummy, status, 0x204);
+            wait_w(&sb.mma_done, 0, &dummy, status, 0x204);
         }
-    } else if (warp == 10) {
+    } else if (warp == 9) {
         // ---------------- 1/|x| of each token (first group only) ----------------
         if (g == 0) {
             int it = 0;
             for (int t = cj; t < P.n_tiles; t += P.ctas_per_group, ++it) {
-                const int s = it % kXStages;
-                bool ok = wait(&sb.x_full[s], (it / kXStages) & 1, abort_flag, status, 0x301);
+                const int s = it % P.x_stages;
+                bool ok = wait(&sb.x_full[s], (it / P.x_stages) & 1, abort_flag, status, 0x301);
                 if (!__all_sync(0xffffffffu, ok)) break;
                 const uint8_t *xt = Xs + s * x_bytes;
                 for (int rr = 0; rr < 4; ++rr) {
@@ -282,80 +320,49 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
             }
         }
     } else {
-        // ---------------- epilogue warpgroups (warps 0-3: buffer 0, 4-7: buffer 1) --------
+        // ---------------- epilogue warpgroups: warpgroup e takes the tiles it & 1 == e ------
+        // It sees every chunk of its tile, hence every round whole: no merging between
+        // warpgroups.  Its chunks alternate between accumulators 2e and 2e + 1.
         const int e = warp >> 2, q = warp & 3;
         const int row = q * 32 + lane;
-        const uint32_t tlane = tmem + ((uint32_t)(q * 32) << 16) + e * kChunkMax;
-        uint32_t chunk_ctr = 0;
+        const uint32_t tlane0 = tmem + ((uint32_t)(q * 32) << 16);
+        const int n0 = (nch + 1) / 2, n1 = nch / 2;   // chunks per tile on each accumulator
         int it = 0;
         bool ok = true;
         for (int t = cj; ok && t < P.n_tiles; t += P.ctas_per_group, ++it) {
+            if ((it & 1) != e) continue;
             const long long tok = (long long)t * kTileM + row;
             const bool live = tok < P.n_tok;
             int cur = -1;
             float best = 0.f;
             int bidx = 0;
-            const int par = it & 1;
-            if (P.split) {
-                // parts[par] of two tiles ago must have been merged by warpgroup 0
-                bool w = wait(&sb.parts_empty[par], ((it >> 1) & 1) ^ 1, abort_flag, status, 0x402);
-                if (!(ok = __all_sync(0xffffffffu, w))) break;
-            }
-            for (int k = 0; k < nch; ++k, ++chunk_ctr) {
-                if ((int)(chunk_ctr & 1) != e) continue;
-                bool w = wait(&sb.tm_full[e], (chunk_ctr >> 1) & 1, abort_flag, status, 0x401);
+            for (int k = 0; k < nch; ++k) {
+                const int buf = 2 * e + (k & 1);
+                const int use = (it >> 1) * ((k & 1) ? n1 : n0) + (k >> 1);
+                const uint32_t tlane = tlane0 + buf * kChunkMax;
+                bool w = wait(&sb.tm_full[buf], use & 1, abort_flag, status, 0x401);
                 if (!(ok = __all_sync(0xffffffffu, w))) break;
                 fence_after_sync();
                 const int width = chunk_width(P, nr, k);
-                for (int c = 0; c < width; c += 32) {
-                    uint32_t v[32];
-                    tmem_ld32(tlane + c, v);
-                    tmem_wait_ld();
-                    int r, j0;
-                    if (P.split) { r = k / P.cpr; j0 = kChunkMax * (k % P.cpr) + c; }
-                    else {
-                        const int col = chunk_col0(P, k) + c;
-                        r = col / P.hp;
-                        j0 = col - r * P.hp;
-                    }
-                    if (r != cur) {
-                        if (P.split && cur >= 0) {
-                            const int o = ((par * 2 + e) * kMaxSplitRounds + cur) * kTileM + row;
-                            part_best[o] = best;
-                            part_idx[o] = bidx;
-                        }
-                        cur = r;
-                        best = 0.f;
-                        bidx = 0;
-                    }
-                    scan32(v, j0, P.half - j0, best, bidx);
-                    if (!P.split && j0 + 32 >= P.hp && live)
-                        write_bucket(buckets, P, tok, r0 + r, best, bidx);
+                // round and in-round column of the chunk's first column
+                int rr, jj;
+                if (P.split) { rr = k / P.cpr; jj = kChunkMax * (k % P.cpr); }
+                else { const int col = chunk_col0(P, k); rr = col / P.hp; jj = col - rr * P.hp; }
+                uint32_t va[32], vb[32];
+                for (int c = 0; c < width; c += 64) {
+                    const bool two = c + 32 < width;
+                    LSH_SPAN_BEGIN(t_ld);
+                    tmem_ld32(tlane + c, va);
+                    if (two) tmem_ld32(tlane + c + 32, vb);
+                    tmem_wait_ld(va, vb);
+                    LSH_SPAN_END(t_ld, 0x480);
+                    LSH_SPAN_BEGIN(t_sc);
+                    scan_batch(va, P, rr, jj, cur, best, bidx, live, buckets, tok, r0);
+                    if (two) scan_batch(vb, P, rr, jj, cur, best, bidx, live, buckets, tok, r0);
+                    LSH_SPAN_END(t_sc, 0x481);
                 }
                 fence_before_sync();
-                mbar_arrive(&sb.tm_empty[e]);
-            }
-            if (!ok) break;
-            if (P.split) {
-                if (cur >= 0) {
-                    const int o = ((par * 2 + e) * kMaxSplitRounds + cur) * kTileM + row;
-                    part_best[o] = best;
-                    part_idx[o] = bidx;
-                }
-                mbar_arrive(&sb.parts_full[par]);
-                if (e == 0) {
-                    bool w = wait(&sb.parts_full[par], (it >> 1) & 1, abort_flag, status, 0x403);
-                    if (!(ok = __all_sync(0xffffffffu, w))) break;
-                    for (int r = 0; live && r < nr; ++r) {
-                        const int o0 = ((par * 2 + 0) * kMaxSplitRounds + r) * kTileM + row;
-                        const int o1 = ((par * 2 + 1) * kMaxSplitRounds + r) * kTileM + row;
-                        const float b0 = part_best[o0], b1 = part_best[o1];
-                        const int i0 = part_idx[o0], i1 = part_idx[o1];
-                        const bool take1 = fabsf(b1) > fabsf(b0) || (fabsf(b1) == fabsf(b0) && i1 < i0);
-                        write_bucket(buckets, P, tok, r0 + r, take1 ? b1 : b0, take1 ? i1 : i0);
-                    }
-                    mbar_arrive(&sb.parts_empty[par]);
-                }
+                mbar_arrive(&sb.tm_empty[buf]);
             }
         }
     }
@@ -385,19 +392,22 @@ bool make_plan(const Problem &p, HashPlan &P, int num_sms)
     const int rpg_max = cap / P.hp;
     P.n_groups = (p.n_rounds + rpg_max - 1) / rpg_max;
     P.rpg = (p.n_rounds + P.n_groups - 1) / P.n_groups;
-    if (P.split && P.rpg > kMaxSplitRounds) return false;
     P.n_tiles = (int)((P.n_tok + kTileM - 1) / kTileM);
     P.ctas_per_group = num_sms / P.n_groups;
     if (P.ctas_per_group < 1) P.ctas_per_group = 1;
     if (P.ctas_per_group > P.n_tiles) P.ctas_per_group = P.n_tiles;
     P.group_bytes = P.rpg * P.hp * p.d * 2;  // multiple of 32*64*2 = 4096
+    const size_t x_bytes = (size_t)kTileM * p.d * 2;
+    const size_t room = kSmemCap - 1024 - (size_t)P.group_bytes;
+    P.x_stages = (int)(room / x_bytes);
+    if (P.x_stages > kMaxXStages) P.x_stages = kMaxXStages;
+    if (P.x_stages < 2) return false;
     return true;
 }
 
 size_t smem_bytes(const HashPlan &P)
 {
-    return 1024 + (size_t)P.group_bytes + (size_t)kXStages * kTileM * P.d * 2 +
-           (size_t)2 * 2 * kMaxSplitRounds * kTileM * 8;
+    return 1024 + (size_t)P.group_bytes + (size_t)P.x_stages * kTileM * P.d * 2;
 }
 
 int num_sms_current()

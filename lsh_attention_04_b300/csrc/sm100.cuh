@@ -62,23 +62,33 @@ __device__ __forceinline__ void fence_before_sync() {
 __device__ __forceinline__ void fence_after_sync() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
+// MMA issue.  Every wrapper below is executed by a whole, converged warp: one lane is
+// elected inside the instruction sequence and issues.  (Issuing from a lane-divergent
+// branch instead, e.g. under `if (lane == 0)`, measured about half the issue rate on
+// sm_103a: ~256 cycles per M=128 instruction against ~123 from a converged warp, which
+// reaches the full dense bf16 rate at N=256.)
+//
 // D (tmem) (+)= A (smem) * B (smem)
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
                                        uint32_t accumulate) {
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+    asm volatile("{\n\t.reg .pred p, e;\n\t.reg .b32 r;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "elect.sync r|e, 0xffffffff;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
                  :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
 }
 // D (tmem) (+)= A (tmem, packed 16-bit pairs) * B (smem)
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
                                        uint32_t accumulate) {
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+    asm volatile("{\n\t.reg .pred p, e;\n\t.reg .b32 r;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "elect.sync r|e, 0xffffffff;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
                  :: "r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
 }
-// Arrive once on an mbarrier when every tcgen05 op this thread issued so far completes.
+// Arrive once on an mbarrier when every tcgen05 op the warp's elected lane issued so far
+// completes (whole warp; the elected lane is the one that issued the MMAs).
 __device__ __forceinline__ void mma_commit(uint32_t mbar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+    asm volatile("{\n\t.reg .pred e;\n\t.reg .b32 r;\n\telect.sync r|e, 0xffffffff;\n\t"
+                 "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
                  :: "r"(mbar) : "memory");
 }
 
@@ -98,6 +108,20 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+#define LSH_RW32(p) "+r"(p[0]), "+r"(p[1]), "+r"(p[2]), "+r"(p[3]), "+r"(p[4]), "+r"(p[5]), \
+    "+r"(p[6]), "+r"(p[7]), "+r"(p[8]), "+r"(p[9]), "+r"(p[10]), "+r"(p[11]), "+r"(p[12]), \
+    "+r"(p[13]), "+r"(p[14]), "+r"(p[15]), "+r"(p[16]), "+r"(p[17]), "+r"(p[18]), "+r"(p[19]), \
+    "+r"(p[20]), "+r"(p[21]), "+r"(p[22]), "+r"(p[23]), "+r"(p[24]), "+r"(p[25]), "+r"(p[26]), \
+    "+r"(p[27]), "+r"(p[28]), "+r"(p[29]), "+r"(p[30]), "+r"(p[31])
+// tcgen05.wait::ld that also ties the destination registers of the loads it waits for:
+// the compiler sees them as written here, so no use of them is scheduled before the wait.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : LSH_RW32(r) :: "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32], uint32_t (&s)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : LSH_RW32(r) :: "memory");
+    asm volatile("" : LSH_RW32(s) :: "memory");
 }
 // 16 consecutive 32-bit columns into this thread's lane.  Completion needs tmem_wait_st().
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
@@ -133,6 +157,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
                  : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
     return ok != 0;
 }
+// try_wait with a suspend-time hint: a thread whose phase is not complete yet is parked
+// (up to `ns` nanoseconds, woken when the phase completes) instead of re-polling, so
+// waiting roles do not take issue slots from the warps doing the arithmetic.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(ns) : "memory");
+    return ok != 0;
+}
 // Arrive on `bar` once all cp.async copies this thread issued so far have landed.
 __device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(smem_u32(bar)) : "memory");
@@ -155,13 +189,35 @@ __device__ __forceinline__ void report(StatusBlock *st, volatile int *abort_flag
     if (st && atomicCAS(&st->code, 0, 1) == 0) st->detail = where;
 }
 
-static __device__ __noinline__ bool wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                  StatusBlock *st, int where) {
+#ifdef LSH_WAIT_PROF
+// Profiling build only: cycles spent in each wait, summed over threads, by wait code.
+extern __device__ unsigned long long g_wait_cycles[4096];
+extern __device__ unsigned long long g_wait_count[4096];
+#endif
+
+// Profiling build only: time spans inside compute loops (summed per warp by lane 0).
+#ifdef LSH_WAIT_PROF
+#define LSH_SPAN_BEGIN(v) const long long v = clock64()
+#define LSH_SPAN_END(v, code)                                                          \
+    do {                                                                               \
+        if ((threadIdx.x & 31) == 0) {                                                 \
+            atomicAdd(&::lsh::sm100::g_wait_cycles[(code) & 4095],                     \
+                      (unsigned long long)(clock64() - (v)));                          \
+            atomicAdd(&::lsh::sm100::g_wait_count[(code) & 4095], 1ull);               \
+        }                                                                              \
+    } while (0)
+#else
+#define LSH_SPAN_BEGIN(v) do {} while (0)
+#define LSH_SPAN_END(v, code) do {} while (0)
+#endif
+
+static __device__ __noinline__ bool wait_impl(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                       StatusBlock *st, int where) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63) == 0) {
+        if (mbar_try_wait_sleep(bar, parity, 20000)) return true;
+        if ((it & 7) == 0) {
             if (*abort_flag) return false;
             if (globaltimer() - t0 > kWaitLimitNs) {
                 report(st, abort_flag, where);
@@ -169,6 +225,27 @@ static __device__ __noinline__ bool wait(uint64_t *bar, uint32_t parity, volatil
             }
         }
     }
+}
+
+static __device__ __forceinline__ bool wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                            StatusBlock *st, int where) {
+#ifdef LSH_WAIT_PROF
+    const long long c0 = clock64();
+    const bool ok = wait_impl(bar, parity, abort_flag, st, where);
+    if ((threadIdx.x & 31) == 0) {
+        atomicAdd(&g_wait_cycles[where & 4095], (unsigned long long)(clock64() - c0));
+        atomicAdd(&g_wait_count[where & 4095], 1ull);
+    }
+    return ok;
+#else
+    return wait_impl(bar, parity, abort_flag, st, where);
+#endif
+}
+
+// Bounded wait by a whole warp, with a warp-uniform answer (false if any lane gave up).
+static __device__ __forceinline__ bool wait_w(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                              StatusBlock *st, int where) {
+    return __all_sync(0xffffffffu, wait(bar, parity, abort_flag, st, where));
 }
 
 // ------------------------------------------------------------------ copies

@@ -45,3 +45,23 @@ bool make_tmap_2d_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint64
 }
 
 }  // namespace lsh
+
+#ifdef LSH_WAIT_PROF
+namespace lsh {
+namespace sm100 {
+__device__ unsigned long long g_wait_cycles[4096];
+__device__ unsigned long long g_wait_count[4096];
+}  // namespace sm100
+}  // namespace lsh
+// Profiling build only: copy (and clear) the per-code wait cycles and counts.
+extern "C" int lsh_debug_wait_profile(unsigned long long *cycles, unsigned long long *counts)
+{
+    cudaDeviceSynchronize();
+    if (cudaMemcpyFromSymbol(cycles, lsh::sm100::g_wait_cycles, sizeof(unsigned long long) * 4096) != cudaSuccess) return 1;
+    if (cudaMemcpyFromSymbol(counts, lsh::sm100::g_wait_count, sizeof(unsigned long long) * 4096) != cudaSuccess) return 1;
+    static unsigned long long zero[4096];
+    cudaMemcpyToSymbol(lsh::sm100::g_wait_cycles, zero, sizeof(zero));
+    cudaMemcpyToSymbol(lsh::sm100::g_wait_count, zero, sizeof(zero));
+    return 0;
+}
+#endif
