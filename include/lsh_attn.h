@@ -92,7 +92,10 @@ size_t lsh_attn_workspace_bytes(int B, int H, int L, int d, int n_buckets, int n
 /*
  * The whole forward pass: steps 1-6 above, on `stream`, through the caller's
  * workspace (which then holds buckets, perm, inv, bstart, o_r and lse_r; see
- * lsh_attn_workspace_layout).
+ * lsh_attn_workspace_layout).  Inside this call the attention step writes o_r and
+ * lse_r in TOKEN order (round r's row of token i at position i, not at its sorted
+ * index), so the round combination reads them as a stream; lsh_chunk_attn alone
+ * keeps the sorted order documented above.
  *   qk, v     [B][H][L][d] dtype;  R [n_rounds][d][n_buckets/2] dtype
  *   causal    0 or 1;  scale  multiplies every score (see conventions)
  *   out       fp32 [B][H][L][d];  lse  fp32 [B][H][L]: logsumexp over rounds of lse_r

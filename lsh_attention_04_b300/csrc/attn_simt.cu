@@ -26,8 +26,8 @@ __global__ void __launch_bounds__(kWarps * 32)
 attn_simt_kernel(const T *__restrict__ qk, const T *__restrict__ v,
                  const int32_t *__restrict__ buckets, const int32_t *__restrict__ perm,
                  const int32_t *__restrict__ bstart, const float *__restrict__ inv_norm, int L,
-                 int n_rounds, int nb, int causal, float scale, T *__restrict__ o_r,
-                 float *__restrict__ lse_r)
+                 int n_rounds, int nb, int causal, float scale, int token_order,
+                 T *__restrict__ o_r, float *__restrict__ lse_r)
 {
     constexpr int KS = D + 1;  // padded key row: lanes reading different rows hit different banks
     extern __shared__ float smem[];
@@ -118,7 +118,7 @@ attn_simt_kernel(const T *__restrict__ qk, const T *__restrict__ v,
             for (int i = 0; i < EPL; ++i) o[i] *= rs;
             lse = mx + logf(sum);
         }
-        const size_t row = (size_t)seg * L + s;
+        const size_t row = (size_t)seg * L + (token_order ? P[s] : s);
 #pragma unroll
         for (int i = 0; i < EPL; ++i) st_elem(o_r, row * D + lane + 32 * i, o[i]);
         if (lane == 0) lse_r[row] = lse;
@@ -137,7 +137,7 @@ cudaError_t launch(const Problem &p, const void *qk, const void *v, const int32_
     dim3 grid((unsigned)(p.L / C), (unsigned)p.n_seg());
     k<<<grid, kWarps * 32, smem, st>>>((const T *)qk, (const T *)v, buckets, perm, bstart,
                                        inv_norm, p.L, p.n_rounds, p.nb, p.causal, p.scale,
-                                       (T *)o_r, lse_r);
+                                       p.token_order, (T *)o_r, lse_r);
     return cudaGetLastError();
 }
 

@@ -11,36 +11,42 @@
 // Tile = 128 consecutive sorted rows (chunks 2t and 2t+1 of one (batch, head, round)
 // segment).  Their keys live in the 192-row window of chunks 2t-1, 2t, 2t+1: rows of
 // chunk 2t use window columns 0-127, rows of chunk 2t+1 use columns 64-191.
-//   S = Q K^T     one chain of tcgen05.mma M=128, N=192, K=16 steps over d; A (window
-//                 rows 64-191) and B (all 192 rows) come from the tile's own Q/K window
-//                 buffer in shared memory; fp32 into TMEM (2 x 192 columns).
+//   S = Q K^T     tcgen05.mma M=128, K=16 steps over d; A = the tile's 128 rows, B = the
+//                 window's 192 rows, both from the chunk ring in shared memory, fp32 into
+//                 TMEM (2 x 192 columns).  One N=192 chain when the three chunks sit in
+//                 consecutive ring slots, else N=64 (look-back) + N=128.
 //   P             packed bf16 pairs written into TMEM over S: the 32 keys of S columns
 //                 32j..32j+31 go to columns 32j..32j+15, so every warp overwrites only
 //                 S columns it has already read.
 //   O = P V       tcgen05.mma M=128, N=d, K=16 steps with A read from TMEM and V as an
 //                 MN-major shared-memory operand (the same 128-byte-swizzled row layout
 //                 as Q/K).
-// One thread issues a tcgen05.mma only every few hundred cycles whatever N is, so the S
-// chain and the P V chain are issued from two different warps and overlap.
+// The S chain and the P V chain are issued from two different warps and overlap.
 // Masks: sorted order keeps each bucket in one run, so the keys of sorted row s form one
 // interval of window columns: [max(window start, bucket start), causal ? s : min(window
-// end, bucket end)), minus s itself when not causal.  The loaders fetch the bucket's run
-// bounds; the softmax needs no per-key bucket test.  A row with no key but itself gives
-// its own column weight 1, so P V returns v_i exactly; its lse is the self logit -1e5.
+// end, bucket end)), minus s itself when not causal.  A loader marks where runs start
+// and end inside its chunk (warp ballots over neighbouring rows' buckets); a softmax
+// lane turns the marks of its chunk and the previous one into its interval, so neither
+// needs the bucket-start table or a per-key bucket test.  A row with no key but itself
+// gives its own column weight 1, so P V returns v_i exactly; its lse is the self logit
+// -1e5.
 // Softmax without a running maximum: with unit keys every score of query i is bounded
 // by m_i = |scale| * |q_i| (Cauchy-Schwarz), so p = exp(s - m_i) cannot overflow.  If
 // m_i is so large that every p could underflow (|scale| |q_i| log2 e > 64), the warp
 // first takes the exact row maximum instead.  lse = m_i + log(sum p).
-// Rows are gathered through the sort permutation by TMA tile::gather4 (4 rows per
-// instruction, 128-byte swizzle): each tile's 192 Q/K rows into one of two window
-// buffers (the look-back chunk is gathered again for the next tile, which keeps the
-// window contiguous for the single N=192 MMA), and V rows with the row metadata into a
-// ring of 6 chunk slots (chunk c in slot c mod 6), released after the last P V that
-// reads them.
+// Data movement: a ring of 6 chunk slots (chunk c in slot c mod 6) holds each chunk's
+// Q/K rows, V rows and row metadata, loaded once and released after the last P V that
+// reads the chunk.  Rows are gathered through the sort permutation by 16-byte cp.async
+// pieces written straight into the 128-byte-swizzled operand layout, and (V rows
+// 0-31 of each chunk) by the tensor-map gather, 4 rows per operation.  Neither engine
+// alone keeps up: the tensor-map gather moves about 7 bytes per clock per SM at this
+// size (512 bytes per operation), one warp's cp.async stream about 10, so two loader
+// warps take alternate chunks and both engines run side by side.  The MMA warps fence the async proxy after each wait,
+// since the rows were written through the generic one.
 // Warp roles: 0-7 softmax + output epilogue (warps w and w+4 share TMEM lane quarter w
-// and split the row's columns and O's columns), 8 V loader (one owner for all slots, so
-// each slot's fills, and the parity waits on its barrier, happen in order), 9 Q/K window
-// loader, 10 S issuer and TMEM owner, 11 P V issuer.
+// and split the row's columns and O's columns), 8-9 loaders (warp 8 + (c & 1) fills
+// chunk c: one owner per slot, so each slot's fills and the parity waits on its barrier
+// happen in order), 10 S issuer and TMEM owner, 11 P V issuer.
 // Persistent CTAs take contiguous ranges of tiles of a group of heads small enough for
 // L2, so all rounds of those heads share cached rows.  Every wait is bounded
 // (sm100::wait); on a timeout the kernel records where in the workspace status block and
@@ -57,11 +63,10 @@ using namespace sm100;
 constexpr int kC = 64;            // chunk length
 constexpr int kRows = 128;        // rows per tile
 constexpr int kWin = 192;         // S columns per tile (window rows)
-constexpr int kSlots = 6;         // V ring
+constexpr int kSlots = 6;         // chunk ring (even: chunk parity = slot parity)
 constexpr int kSmWarps = 8;       // softmax / epilogue warps
-constexpr int kVLoaders = 1;      // V loader warps (12 warps in all: 3 per scheduler keeps 168 registers per thread)
-constexpr int kQkWarp = kSmWarps + kVLoaders;
-constexpr int kSWarp = kQkWarp + 1;
+constexpr int kLoaders = 2;       // loader warps (12 warps in all: 3 per scheduler keeps 168 registers per thread)
+constexpr int kSWarp = kSmWarps + kLoaders;
 constexpr int kPvWarp = kSWarp + 1;
 constexpr int kThreads = (kPvWarp + 1) * 32;
 constexpr int kTmemO = 2 * kWin;  // O accumulator column (384)
@@ -72,22 +77,23 @@ constexpr float kExactMaxLog2 = 64.f;
 constexpr size_t kL2Budget = 48ull << 20;
 
 struct AttnPlan {
-    int L, d, nb, n_rounds, causal;
+    int L, d, nb, n_rounds, causal, token_order;
     float scale;
     int nchunks, tps;            // chunks and 128-row tiles per segment
     int n_heads, heads_per_group, n_groups;
 };
 
-struct SlotMeta {
+struct __align__(16) SlotMeta {
     float cs[kC];    // key column scale: scale * log2(e) / |k_j|
     float m2[kC];    // query bound in log2 units: |scale| * log2(e) * |q_i|
-    int blo[kC];     // sorted index where the row's bucket starts
-    int bhi[kC];     // sorted index where the row's bucket ends
+    unsigned long long starts;   // bit r: a bucket run starts at row r (bit 0 also when
+                                 // the chunk opens its segment)
+    unsigned long long ends;     // bit r: a run ends at row r (row 63 never marked)
+    int jrow[kC];                // original position of each row
 };
 
 struct __align__(8) AttnBarriers {
-    uint64_t qk_full[2], qk_empty[2];             // Q/K window buffers (free after S)
-    uint64_t v_full[kSlots], v_empty[kSlots];     // V rows + metadata (free after P V)
+    uint64_t full[kSlots], empty[kSlots];         // chunk slots (free after the last P V)
     uint64_t s_full[2], p_full[2], pv_done[2];
     uint64_t o_full, o_empty, mma_done;
     uint32_t tmem_base;
@@ -125,6 +131,8 @@ __device__ __forceinline__ bool for_items(const AttnPlan &P, F &&f) {
     return true;
 }
 
+// Four rows (r0..r3) of 64 columns from column x, by the tensor-map gather, into 512
+// contiguous bytes (the map's 128-byte swizzle applied); completes `bytes` on bar.
 __device__ __forceinline__ void gather4(uint32_t dst, const CUtensorMap *map, int x, int r0, int r1,
                                         int r2, int r3, uint32_t bar) {
     asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
@@ -142,6 +150,38 @@ __device__ __forceinline__ void gather4(uint32_t dst, const CUtensorMap *map, in
 #else
 #define LSH_IDX(idx, bound, code) ((void)(bound), (idx))
 #endif
+
+// A permuted row index as a safe row: out of [0, L) (a corrupt permutation) it is
+// reported in a self-checking build and replaced by 0 in every build, so no copy ever
+// leaves the tensor.
+#ifdef LSH_CHECKED
+#define LSH_ROW(j, L, code) LSH_IDX(j, L, code)
+#else
+#define LSH_ROW(j, L, code) ((unsigned)(j) < (unsigned)(L) ? (j) : 0)
+#endif
+
+// Gather the 64 rows of a chunk into a K-major, 128-byte-swizzled tile: row r (global
+// row row_base + j_r, where lane k holds j of rows k and k + 32) lands at byte r * 128 of
+// each 64-column block (blocks kb_stride bytes apart), its 16-byte pieces permuted by
+// the swizzle (piece c of row r at ((c ^ (r & 7)) * 16)); rows r0..63 only.  16-byte
+// cp.async pieces, d / 8 lanes per row (whole rows per instruction).  Completion is
+// tracked by the caller (cp.async mbarrier arrive).
+__device__ __forceinline__ void gather_chunk(uint32_t dst, uint32_t kb_stride,
+                                             const __nv_bfloat16 *__restrict__ src,
+                                             long long row_base, int j0, int j1, int d, int lane,
+                                             int r0 = 0) {
+    const int lpr = d >> 3;                       // lanes per row
+    const int c = lane & (lpr - 1), kb = c >> 3, c16 = c & 7;
+    const int rstep = 32 / lpr;
+    const uint32_t dcol = dst + kb * kb_stride;
+    const __nv_bfloat16 *scol = src + row_base * d + c * 8;
+#pragma unroll 4
+    for (int r = r0 + lane / lpr; r < 64; r += rstep) {
+        const int a = __shfl_sync(0xffffffffu, j0, r & 31);
+        const int b = __shfl_sync(0xffffffffu, j1, r & 31);
+        cp_async16(dcol + r * 128 + ((c16 ^ (r & 7)) << 4), scol + (long long)(r < 32 ? a : b) * d);
+    }
+}
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -163,37 +203,45 @@ __device__ __forceinline__ void st_global_v8(void *p, const uint32_t *r) {
 // TMEM column of the packed P values of keys 16m .. 16m+15 (relative to the S buffer).
 __host__ __device__ __forceinline__ int p_col(int m) { return 32 * (m >> 1) + 8 * (m & 1); }
 
-// Softmax of one 32-key batch: key jj is a candidate iff jj + off lies in [0, len) (and,
-// not causal, jj != skip); candidates get p = 2^(s cs - m2), the rest 0 -- except column
-// one_at, which gets weight 1 (the self fallback).  Returns the sum of the p.
-template <bool kSelfCol>
-__device__ __forceinline__ float softmax_batch(const uint32_t (&s32)[32], const float *cs, int off,
-                                               unsigned len, int skip, int one_at, float m2,
-                                               uint32_t (&pk)[16]) {
-    float l = 0.f;
+// Bits lo..hi-1 of a 32-bit mask (the batch columns inside a row's key interval).
+__device__ __forceinline__ uint32_t range_mask(int lo, int hi) {
+    lo = max(lo, 0);
+    hi = min(hi, 32);
+    if (lo >= hi) return 0u;
+    const uint32_t below_hi = hi == 32 ? 0xffffffffu : (1u << hi) - 1u;
+    return below_hi & (0xffffffffu << lo);
+}
+
+// One 32-column batch of a row: p_j = 2^(s_j * cs_j - m2) for the columns whose bit is
+// set in `vm`, 0 elsewhere (ex2 of -inf), packed to bf16 pairs.  Returns sum_j p_j.
+// `cs` is 16-byte aligned shared memory.
+__device__ __forceinline__ float softmax_batch(const uint32_t (&s32)[32], const float *cs,
+                                               uint32_t vm, float m2, uint32_t (&pk)[16]) {
+    float la = 0.f, lb = 0.f;
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-        float p2[2];
+    for (int q = 0; q < 8; ++q) {
+        const float4 c4 = reinterpret_cast<const float4 *>(cs)[q];
+        const float c[4] = {c4.x, c4.y, c4.z, c4.w};
+        float p[4];
 #pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) {
-            const int jj = 2 * k + e2;
-            bool ok = (unsigned)(jj + off) < len;
-            if (kSelfCol) ok = ok && jj != skip;
-            const float x = fmaf(__uint_as_float(s32[jj]), cs[jj], -m2);
-            float p = ok ? ex2(x) : 0.f;
-            if (kSelfCol) p = jj == one_at ? 1.f : p;
-            p2[e2] = p;
+        for (int e = 0; e < 4; ++e) {
+            const int jj = 4 * q + e;
+            const float x = fmaf(__uint_as_float(s32[jj]), c[e], -m2);
+            p[e] = ex2((vm >> jj) & 1u ? x : -INFINITY);
         }
-        pk[k] = pack_bf16(p2[0], p2[1]);
-        l += p2[0] + p2[1];
+        pk[2 * q] = pack_bf16(p[0], p[1]);
+        pk[2 * q + 1] = pack_bf16(p[2], p[3]);
+        la += p[0] + p[1];
+        lb += p[2] + p[3];
     }
-    return l;
+    return la + lb;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-lsh_attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap vmap,
+lsh_attn_tc_kernel(const __grid_constant__ CUtensorMap vmap,
+                   const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *__restrict__ vv,
                    const AttnPlan P, const int32_t *__restrict__ buckets,
-                   const int32_t *__restrict__ perm, const int32_t *__restrict__ bstart,
+                   const int32_t *__restrict__ perm,
                    const float *__restrict__ inv_norm, __nv_bfloat16 *__restrict__ o_r,
                    float *__restrict__ lse_r, StatusBlock *status)
 {
@@ -204,25 +252,22 @@ lsh_attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
     // compiler keeps the shared state space (shared loads, not generic ones)
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int nkb = P.d / 64;                      // 64-column blocks of a row
-    const int wkb = kWin * 128;                    // Q/K window: [w][kb][192 rows][128 B]
-    const int wstride = nkb * wkb;
-    const int vslot = nkb * kC * 128;              // V ring: [slot][kb][64 rows][128 B]
-    uint8_t *QKW = smem;
-    uint8_t *V = QKW + 2 * wstride;
+    // Q/K rows: [kb][slot][64 rows][128 B] (for one kb the slots are consecutive, so the
+    // rows of chunks in consecutive slots form one operand); V rows: [slot][kb][64][128 B]
+    const int qk_plane = kSlots * kC * 128;
+    const int vslot = nkb * kC * 128;
+    uint8_t *QK = smem;
+    uint8_t *V = QK + nkb * qk_plane;
     SlotMeta *meta = (SlotMeta *)(V + kSlots * vslot);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int *abort_flag = &sb.abort_flag;
     const uint32_t FULL = 0xffffffffu;
-    uint32_t armed = 0, armed_par = 0;   // loaders: last fill per slot / window (wind-down)
 
     if (threadIdx.x == 0) {
-        for (int w = 0; w < 2; ++w) {
-            mbar_init(&sb.qk_full[w], 1);           // expect_tx arrive
-            mbar_init(&sb.qk_empty[w], 1);
-        }
         for (int s = 0; s < kSlots; ++s) {
-            mbar_init(&sb.v_full[s], 1 + 32);       // expect_tx arrive + 32 metadata lanes
-            mbar_init(&sb.v_empty[s], 1);
+            mbar_init(&sb.full[s], 32 + 32 + 1);    // loader lanes: cp.async + metadata;
+                                                    // expect_tx of the tensor-map rows
+            mbar_init(&sb.empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&sb.s_full[b], 1);
@@ -243,133 +288,159 @@ lsh_attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
     const size_t n_rows = (size_t)P.n_heads * P.n_rounds * P.L;
     const long long n_tok = (long long)P.n_heads * P.L;
 
-    if (warp >= kSmWarps && warp < kSmWarps + kVLoaders) {
-        // ------------------------------------------------------------- V loaders
-        const int lw = warp - kSmWarps;
+    if (warp >= kSmWarps && warp < kSmWarps + kLoaders) {
+        // ------------------------------------------------------------- loaders
+        const int lw = warp - kSmWarps;              // fills the chunks c with c & 1 == lw
+        uint32_t e_bits = (1u << kSlots) - 1;        // parity to wait per slot
+        uint32_t armed = 0;                          // slots with a fill issued (wind-down)
         if (lane == 0) prefetch_tmap(&vmap);
-        uint32_t v_bits = (1u << kSlots) - 1;        // parity to wait per slot
         const float ascale = fabsf(P.scale) * kLog2e, cscale = P.scale * kLog2e;
         for_items(P, [&](long long seg, int tb, int te) -> bool {
             const long long bh = seg / P.n_rounds;
-            const int c_begin = tb > 0 ? 2 * tb - 1 : 0;
+            int c = tb > 0 ? 2 * tb - 1 : 0;
             const int c_end = min(2 * te, P.nchunks);
-            for (int c = c_begin; c < c_end; ++c) {
+            if ((c & 1) != lw) ++c;
+            if (c >= c_end) return true;
+            const size_t seg_row0 = (size_t)seg * P.L;
+            // Row metadata is software-pipelined over this warp's chunks (c, c + 2, ...):
+            // the permutation two chunks ahead, buckets and norms one chunk ahead.  Lane k
+            // holds rows k and k + 32; every lane also holds the row before the chunk.
+            int ja0 = 0, ja1 = 0, jap = 0, jb0 = 0, jb1 = 0, jbp = 0;
+            auto ld_perm = [&](int cc, int &j0, int &j1, int &jp) {
+                const size_t row0 = seg_row0 + (size_t)cc * kC;
+                j0 = LSH_ROW(perm[LSH_IDX(row0 + lane, n_rows, 0x511)], P.L, 0x517);
+                j1 = LSH_ROW(perm[LSH_IDX(row0 + 32 + lane, n_rows, 0x512)], P.L, 0x518);
+                jp = cc > 0 ? LSH_ROW(perm[LSH_IDX(row0 - 1, n_rows, 0x519)], P.L, 0x51a) : 0;
+            };
+            int bk0, bk1, bkp;                           // buckets of the rows
+            float nm0, nm1;                              // 1 / |k| of the rows
+            auto ld_rows = [&](int j0, int j1, int jp) {
+                bk0 = buckets[LSH_IDX(seg_row0 + j0, n_rows, 0x513)];
+                bk1 = buckets[LSH_IDX(seg_row0 + j1, n_rows, 0x514)];
+                bkp = buckets[LSH_IDX(seg_row0 + jp, n_rows, 0x51b)];
+                nm0 = inv_norm[LSH_IDX(bh * P.L + j0, n_tok, 0x515)];
+                nm1 = inv_norm[LSH_IDX(bh * P.L + j1, n_tok, 0x516)];
+            };
+            ld_perm(c, ja0, ja1, jap);
+            if (c + 2 < c_end) ld_perm(c + 2, jb0, jb1, jbp);
+            ld_rows(ja0, ja1, jap);
+            for (; c < c_end; c += 2) {
                 const int s = c % kSlots;
-                if (s % kVLoaders != lw) continue;
-                const uint32_t pv = (v_bits >> s) & 1u;
-                v_bits ^= 1u << s;
-                // metadata first (it does not need the slot): rows lane and lane + 32
-                const size_t row0 = (size_t)seg * P.L + (size_t)c * kC;
-                const int j0 = perm[LSH_IDX(row0 + lane, n_rows, 0x511)];
-                const int j1 = perm[LSH_IDX(row0 + 32 + lane, n_rows, 0x512)];
-                int g[4];   // rows 4*lane .. 4*lane+3 of the chunk (lanes 0-15 gather)
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int row = (4 * lane + k) & 63;
-                    const int a = __shfl_sync(FULL, j0, row & 31);
-                    const int b = __shfl_sync(FULL, j1, row & 31);
-                    g[k] = (int)(bh * P.L) + (row < 32 ? a : b);
-                }
-                const int b0 = buckets[LSH_IDX((size_t)seg * P.L + j0, n_rows, 0x513)];
-                const int b1 = buckets[LSH_IDX((size_t)seg * P.L + j1, n_rows, 0x514)];
-                const float n0 = inv_norm[LSH_IDX(bh * P.L + j0, n_tok, 0x515)];
-                const float n1 = inv_norm[LSH_IDX(bh * P.L + j1, n_tok, 0x516)];
-                const size_t bs0 = (size_t)seg * (P.nb + 1);
-                const size_t n_bs = (size_t)P.n_heads * P.n_rounds * (P.nb + 1);
-                const int lo0 = bstart[LSH_IDX(bs0 + b0, n_bs, 0x517)];
-                const int hi0 = bstart[LSH_IDX(bs0 + b0 + 1, n_bs, 0x518)];
-                const int lo1 = bstart[LSH_IDX(bs0 + b1, n_bs, 0x519)];
-                const int hi1 = bstart[LSH_IDX(bs0 + b1 + 1, n_bs, 0x51a)];
-                bool ok = wait(&sb.v_empty[s], pv, abort_flag, status, 0x503);
+                const uint32_t pe = (e_bits >> s) & 1u;
+                const int j0 = ja0, j1 = ja1, b0 = bk0, b1 = bk1, bp = bkp;
+                const float n0 = nm0, n1 = nm1;
+                ja0 = jb0;
+                ja1 = jb1;
+                jap = jbp;
+                if (c + 4 < c_end) ld_perm(c + 4, jb0, jb1, jbp);
+                if (c + 2 < c_end) ld_rows(ja0, ja1, jap);
+                // where bucket runs start and end inside the chunk
+                const int up0 = __shfl_up_sync(FULL, b0, 1), up1 = __shfl_up_sync(FULL, b1, 1);
+                const int last0 = __shfl_sync(FULL, b0, 31);
+                const int dn0 = __shfl_down_sync(FULL, b0, 1), dn1 = __shfl_down_sync(FULL, b1, 1);
+                const int first1 = __shfl_sync(FULL, b1, 0);
+                const bool st0 = lane > 0 ? b0 != up0 : (c == 0 || b0 != bp);
+                const bool st1 = b1 != (lane > 0 ? up1 : last0);
+                const bool en0 = b0 != (lane < 31 ? dn0 : first1);
+                const bool en1 = lane < 31 && b1 != dn1;
+                const unsigned long long starts = (unsigned long long)__ballot_sync(FULL, st0) |
+                                                  ((unsigned long long)__ballot_sync(FULL, st1) << 32);
+                const unsigned long long ends = (unsigned long long)__ballot_sync(FULL, en0) |
+                                                ((unsigned long long)__ballot_sync(FULL, en1) << 32);
+                bool ok = wait(&sb.empty[s], pe, abort_flag, status, 0x503);
                 if (!__all_sync(FULL, ok)) return false;
-                if (lane == 0) mbar_expect_tx(&sb.v_full[s], (uint32_t)(kC * P.d * 2));
+                e_bits ^= 1u << s;   // now the parity of this fill's full phase
+                LSH_SPAN_BEGIN(t_g);
+                // Two copy engines in parallel: the tensor-map gather takes V rows 0-31
+                // (4 rows per operation, lanes 0-7), cp.async the Q/K rows and V rows 32-63.
+                if (lane == 0) mbar_expect_tx(&sb.full[s], (uint32_t)(32 * P.d * 2));
                 __syncwarp();
-                if (lane < 16)
-                    for (int kb = 0; kb < nkb; ++kb)
-                        gather4(smem_u32(V + s * vslot + kb * kC * 128 + 4 * lane * 128), &vmap,
-                                kb * 64, g[0], g[1], g[2], g[3], smem_u32(&sb.v_full[s]));
+                {
+                    int g[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        g[k] = (int)(bh * P.L) + __shfl_sync(FULL, j0, (4 * lane + k) & 31);
+                    if (lane < 8)
+                        for (int kb = 0; kb < nkb; ++kb)
+                            gather4(smem_u32(V + s * vslot + kb * kC * 128 + 4 * lane * 128), &vmap,
+                                    kb * 64, g[0], g[1], g[2], g[3], smem_u32(&sb.full[s]));
+                }
+                gather_chunk(smem_u32(QK + s * kC * 128), qk_plane, qk, bh * P.L, j0, j1, P.d, lane);
+                gather_chunk(smem_u32(V + s * vslot), kC * 128, vv, bh * P.L, j0, j1, P.d, lane, 32);
+                cp_async_mbar_arrive(&sb.full[s]);
+                armed |= 1u << s;
+                LSH_SPAN_END(t_g, 0x5a0);
                 SlotMeta &m = meta[s];
                 m.cs[lane] = cscale * n0;
                 m.cs[lane + 32] = cscale * n1;
                 m.m2[lane] = n0 > 0.f ? ascale / n0 : 0.f;
                 m.m2[lane + 32] = n1 > 0.f ? ascale / n1 : 0.f;
-                m.blo[lane] = lo0;
-                m.blo[lane + 32] = lo1;
-                m.bhi[lane] = hi0;
-                m.bhi[lane + 32] = hi1;
-                mbar_arrive(&sb.v_full[s]);
-                armed |= 1u << s;
-                armed_par = (armed_par & ~(1u << s)) | (pv << s);
+                m.jrow[lane] = j0;
+                m.jrow[lane + 32] = j1;
+                if (lane == 0) {
+                    m.starts = starts;
+                    m.ends = ends;
+                }
+                mbar_arrive(&sb.full[s]);
             }
             return true;
         });
-    } else if (warp == kQkWarp) {
-        // ------------------------------------------------------------- Q/K window loader
-        if (lane == 0) prefetch_tmap(&qmap);
-        int ctr = 0;
-        for_items(P, [&](long long seg, int tb, int te) -> bool {
-            const long long bh = seg / P.n_rounds;
-            for (int t = tb; t < te; ++t, ++ctr) {
-                const int w = ctr & 1;
-                const bool has_lb = t > 0, has_hi = 2 * t + 1 < P.nchunks;
-                int j[3][2];
-#pragma unroll
-                for (int ci = 0; ci < 3; ++ci) {
-                    const int c = 2 * t - 1 + ci;
-                    const bool present = ci == 1 || (ci == 0 ? has_lb : has_hi);
-                    const size_t row0 = (size_t)seg * P.L + (size_t)(present ? c : 0) * kC;
-                    j[ci][0] = present ? perm[LSH_IDX(row0 + lane, n_rows, 0x521)] : 0;
-                    j[ci][1] = present ? perm[LSH_IDX(row0 + 32 + lane, n_rows, 0x522)] : 0;
-                }
-                const uint32_t par = ((ctr >> 1) & 1) ^ 1;
-                bool ok = wait(&sb.qk_empty[w], par, abort_flag, status, 0x501);
-                if (!__all_sync(FULL, ok)) return false;
-                const int n_present = 1 + (has_lb ? 1 : 0) + (has_hi ? 1 : 0);
-                if (lane == 0) mbar_expect_tx(&sb.qk_full[w], (uint32_t)(n_present * kC * P.d * 2));
-                __syncwarp();
-#pragma unroll
-                for (int ci = 0; ci < 3; ++ci) {
-                    const bool present = ci == 1 || (ci == 0 ? has_lb : has_hi);
-                    if (!present) continue;
-                    int g[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int row = (4 * lane + k) & 63;
-                        const int a = __shfl_sync(FULL, j[ci][0], row & 31);
-                        const int b = __shfl_sync(FULL, j[ci][1], row & 31);
-                        g[k] = (int)(bh * P.L) + (row < 32 ? a : b);
-                    }
-                    if (lane < 16)
-                        for (int kb = 0; kb < nkb; ++kb)
-                            gather4(smem_u32(QKW + w * wstride + kb * wkb + (ci * kC + 4 * lane) * 128),
-                                    &qmap, kb * 64, g[0], g[1], g[2], g[3], smem_u32(&sb.qk_full[w]));
-                }
-                armed |= 1u << w;
-                armed_par = (armed_par & ~(1u << w)) | (par << w);
+        if (*abort_flag) {
+            // wind-down after a timeout: the last fill of each slot may still be in
+            // flight (no consumer waited for it); its full phase completes once its
+            // copies land, every arrival of the fill having been made
+            cp_async_wait_all();
+            for (int s = 0; s < kSlots; ++s) {
+                if (!(armed & (1u << s))) continue;
+                int dummy = 0;
+                wait(&sb.full[s], (e_bits >> s) & 1u, &dummy, nullptr, 0x502);
             }
-            return true;
-        });
+        }
     } else if (warp == kSWarp) {
         // ------------------------------------------------------------- S issuer
         {
-            const uint32_t qk_base = smem_u32(QKW);
-            const uint32_t idesc = idesc_bf16(kRows, kWin, 0, 0);
+            const uint32_t qk_base = smem_u32(QK);
+            uint32_t f_bits = 0;
             int ctr = 0;
+            auto need = [&](int c) -> bool {
+                const int s = c % kSlots;
+                const bool ok = wait_w(&sb.full[s], (f_bits >> s) & 1u, abort_flag, status, 0x601);
+                f_bits ^= 1u << s;
+                return ok;
+            };
             for_items(P, [&](long long, int tb, int te) -> bool {
                 for (int t = tb; t < te; ++t, ++ctr) {
-                    const int w = ctr & 1, b = ctr & 1;
-                    if (!wait_w(&sb.qk_full[w], (ctr >> 1) & 1, abort_flag, status, 0x601)) return false;
+                    const int b = ctr & 1;
+                    if (t == tb && tb > 0 && !need(2 * t - 1)) return false;
+                    if (!need(2 * t)) return false;
+                    if (2 * t + 1 < P.nchunks && !need(2 * t + 1)) return false;
                     if (ctr >= 2 && !wait_w(&sb.pv_done[b], ((ctr - 2) >> 1) & 1, abort_flag, status, 0x604))
                         return false;
                     fence_after_sync();
+                    // the rows were written by cp.async (generic proxy); the MMA reads them
+                    // through the async proxy
+                    fence_proxy_async();
+                    const int s0 = (2 * t) % kSlots;      // even: chunks 2t, 2t+1 in s0, s0+1
+                    // one N=192 chain when the look-back chunk sits in slot s0 - 1; else the
+                    // look-back (if any) as an N=64 chain into columns 0-63
+                    const bool joined = s0 > 0 && t > 0;
                     for (int ks = 0; ks < P.d / 16; ++ks) {
                         const int kb = ks >> 2, ko = (ks & 3) * 32;
-                        const uint32_t wb = qk_base + w * wstride + kb * wkb + ko;
-                        mma_ss(tmem + b * kWin, smem_desc(wb + kC * 128, 16, 1024),
-                               smem_desc(wb, 16, 1024), idesc, ks > 0);
+                        const uint32_t pb = qk_base + kb * qk_plane + ko;
+                        const uint64_t a = smem_desc(pb + s0 * kC * 128, 16, 1024);
+                        if (joined) {
+                            mma_ss(tmem + b * kWin, a, smem_desc(pb + (s0 - 1) * kC * 128, 16, 1024),
+                                   idesc_bf16(kRows, kWin, 0, 0), ks > 0);
+                        } else {
+                            if (t > 0)
+                                mma_ss(tmem + b * kWin, a,
+                                       smem_desc(pb + (kSlots - 1) * kC * 128, 16, 1024),
+                                       idesc_bf16(kRows, kC, 0, 0), ks > 0);
+                            mma_ss(tmem + b * kWin + kC, a, smem_desc(pb + s0 * kC * 128, 16, 1024),
+                                   idesc_bf16(kRows, 2 * kC, 0, 0), ks > 0);
+                        }
                     }
                     mma_commit(smem_u32(&sb.s_full[b]));
-                    mma_commit(smem_u32(&sb.qk_empty[w]));
                 }
                 return true;
             });
@@ -386,7 +457,7 @@ lsh_attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
             int ctr = 0;
             auto needv = [&](int c) -> bool {
                 const int s = c % kSlots;
-                const bool ok = wait_w(&sb.v_full[s], (v_bits >> s) & 1u, abort_flag, status, 0x606);
+                const bool ok = wait_w(&sb.full[s], (v_bits >> s) & 1u, abort_flag, status, 0x606);
                 v_bits ^= 1u << s;
                 return ok;
             };
@@ -399,6 +470,7 @@ lsh_attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                     if (!wait_w(&sb.p_full[b], (q >> 1) & 1, abort_flag, status, 0x602)) return false;
                     if (!wait_w(&sb.o_empty, (q & 1) ^ 1, abort_flag, status, 0x603)) return false;
                     fence_after_sync();
+                    fence_proxy_async();   // V rows were written by cp.async
                     uint32_t acc = 0;
                     for (int wc = 0; wc < 3; ++wc) {
                         const int kc = 2 * t - 1 + wc;
@@ -412,11 +484,12 @@ lsh_attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                     }
                     mma_commit(smem_u32(&sb.o_full));
                     mma_commit(smem_u32(&sb.pv_done[b]));
-                    // release the V rows whose last use was this tile
-                    if (t > 0) mma_commit(smem_u32(&sb.v_empty[(2 * t - 1) % kSlots]));
-                    mma_commit(smem_u32(&sb.v_empty[(2 * t) % kSlots]));
+                    // release the chunks whose last use was this tile (their S MMAs
+                    // completed before this tile's P was written)
+                    if (t > 0) mma_commit(smem_u32(&sb.empty[(2 * t - 1) % kSlots]));
+                    mma_commit(smem_u32(&sb.empty[(2 * t) % kSlots]));
                     if (t == te - 1 && 2 * t + 1 < P.nchunks)
-                        mma_commit(smem_u32(&sb.v_empty[(2 * t + 1) % kSlots]));
+                        mma_commit(smem_u32(&sb.empty[(2 * t + 1) % kSlots]));
                 }
                 return true;
             });
@@ -443,7 +516,6 @@ lsh_attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         float e_m2 = 0.f;
         bool e_live = false, e_self = false;
         bool ok = true;
-        const uint32_t zero16[16] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
 
         auto epilogue = [&](int q) -> bool {
             bool w = wait(&sb.o_full, q & 1, abort_flag, status, 0x702);
@@ -480,9 +552,10 @@ lsh_attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
 
         ok = for_items(P, [&](long long seg, int tb, int te) -> bool {
             for (int t = tb; t < te; ++t) {
+                LSH_SPAN_BEGIN(t_tile);
                 auto need = [&](int c) -> bool {
                     const int s = c % kSlots;
-                    bool w = wait(&sb.v_full[s], (full_bits >> s) & 1u, abort_flag, status, 0x701);
+                    bool w = wait(&sb.full[s], (full_bits >> s) & 1u, abort_flag, status, 0x701);
                     full_bits ^= 1u << s;
                     return __all_sync(FULL, w);
                 };
@@ -493,6 +566,7 @@ lsh_attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                 bool w = wait(&sb.s_full[b], (ctr >> 1) & 1, abort_flag, status, 0x703);
                 if (!__all_sync(FULL, w)) return false;
                 fence_after_sync();
+                LSH_SPAN_BEGIN(t_setup);
 
                 // this row: its keys are the sorted indices [klo, khi) (minus itself when
                 // not causal); the window of a row of chunk cq is chunks cq-1 and cq
@@ -503,10 +577,17 @@ lsh_attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                 const int r = i & (kC - 1);
                 int klo = 0, khi = 0;
                 float m2 = 0.f;
+                // where the row's outputs go: its sorted index, or its original position
+                const int orow = P.token_order ? mq.jrow[r] : srow;
                 if (live) {
-                    const int wlo = cq > 0 ? (cq - 1) * kC : 0;
-                    klo = max(wlo, mq.blo[r]);
-                    khi = P.causal ? srow : min((cq + 1) * kC, mq.bhi[r]);
+                    // the row's bucket run clipped to its window, from the run marks of its
+                    // chunk (and of the previous chunk when the run reaches back into it)
+                    const unsigned long long sm = mq.starts & (~0ull >> (63 - r));
+                    const unsigned long long sp = meta[(cq - 1 + kSlots) % kSlots].starts | 1ull;
+                    klo = sm ? cq * kC + 63 - __clzll((long long)sm)
+                             : (cq - 1) * kC + 63 - __clzll((long long)sp);
+                    const unsigned long long em = mq.ends & (~0ull << r);
+                    khi = P.causal ? srow : (em ? cq * kC + __ffsll((long long)em) : (cq + 1) * kC);
                     m2 = mq.m2[r];
                 }
                 // keys other than the row itself?
@@ -547,51 +628,57 @@ lsh_attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
                     named_bar_sync(1 + q4, 64);
                 }
 
+                LSH_SPAN_END(t_setup, 0x791);
                 LSH_SPAN_BEGIN(t_sm);
                 float l = 0.f;
-                const unsigned len = live ? (unsigned)(khi - klo) : 0u;
                 // both 32-column batches in flight before one wait
                 const bool nb0 = batch_needed(colA), nb1 = batch_needed(colA + 32);
                 uint32_t s32[2][32];
                 if (nb0) tmem_ld32(sbase + colA, s32[0]);
                 if (nb1) tmem_ld32(sbase + colA + 32, s32[1]);
                 if (nb0 || nb1) tmem_wait_ld(s32[0], s32[1]);
-                LSH_SPAN_END(t_sm, 0x784);
-                LSH_SPAN_BEGIN(t_c);
-                uint32_t pkk[2][16];
-                bool wr[2] = {false, false};
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int cc = colA + 32 * h;
-                    if (!(h ? nb1 : nb0)) continue;
-                    const SlotMeta &mk = meta[(2 * t - 1 + cc / kC + kSlots) % kSlots];
-                    const float *cs = mk.cs + (cc & (kC - 1));
-                    const int off = tk0 + cc - klo;        // key jj is valid iff jj + off in [0, len)
-                    if (cc == self_c0)   // the rows' own columns are in this batch: self rules
-                        l += softmax_batch<true>(s32[h], cs, off, len, P.causal ? -1 : lane,
-                                                 self_only ? lane : -1, m2, pkk[h]);
-                    else
-                        l += softmax_batch<false>(s32[h], cs, off, len, -1, -1, m2, pkk[h]);
-                    wr[h] = true;
+                    if (!(h ? nb1 : nb0)) {
+                        tmem_st16_zero(sbase + cc);
+                        continue;
+                    }
+                    const int t0 = tk0 + cc;               // sorted index of batch column 0
+                    uint32_t vm = live ? range_mask(klo - t0, khi - t0) : 0u;
+                    const bool self_batch = cc == self_c0; // the rows' own columns
+                    if (self_batch && !P.causal) vm &= ~(1u << lane);
+                    const float *cs = meta[(2 * t - 1 + cc / kC + kSlots) % kSlots].cs + (cc & (kC - 1));
+                    uint32_t pk[16];
+                    l += softmax_batch(s32[h], cs, vm, m2, pk);
+                    // a row with no key but itself: weight 1 on its own column (all its
+                    // other columns are masked, so its sum was 0)
+                    if (self_batch) {   // (selects, not a conditional store into pk,
+                                        // which would move pk to local memory)
+                        const uint32_t one = (lane & 1) ? 0x3F800000u : 0x00003F80u;
+                        const int kself = self_only ? (lane >> 1) : -1;
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) pk[k] = k == kself ? one : pk[k];
+                        l = self_only ? 1.f : l;
+                    }
+                    tmem_st16(sbase + cc, pk);
                 }
-                LSH_SPAN_END(t_c, 0x785);
-                LSH_SPAN_BEGIN(t_st2);
-                if (wr[0]) tmem_st16(sbase + colA, pkk[0]); else tmem_st16(sbase + colA, zero16);
-                if (wr[1]) tmem_st16(sbase + colA + 32, pkk[1]); else tmem_st16(sbase + colA + 32, zero16);
-                LSH_SPAN_END(t_st2, 0x786);
                 LSH_SPAN_END(t_sm, 0x781);
-                tmem_st16(sbase + colZ, zero16);
+                LSH_SPAN_BEGIN(t_tail);
+                tmem_st16_zero(sbase + colZ);
                 l_part[ctr % kLBufs][half][i] = l;
                 tmem_wait_st();
                 fence_before_sync();
                 mbar_arrive(&sb.p_full[b]);
 
+                LSH_SPAN_END(t_tail, 0x792);
                 if (ctr >= 1 && !epilogue(ctr - 1)) return false;
                 e_live = live;
-                e_row = seg * P.L + srow;
+                e_row = seg * P.L + orow;
                 e_m2 = m2;
                 e_self = self_only;
                 ++ctr;
+                LSH_SPAN_END(t_tile, 0x790);
             }
             return true;
         });
@@ -605,25 +692,15 @@ lsh_attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_consta
         fence_after_sync();
         tmem_dealloc(tmem, 512);
     }
-    if (*abort_flag && warp >= kSmWarps && warp <= kQkWarp) {
-        // Wind-down after a timeout: the gathers a loader issued last into each of its
-        // slots (or windows) may still be in flight (no consumer waited for them); let
-        // them land before the CTA exits.  A fill that was consumed and refilled has
-        // landed already; its stale phase is skipped by the bounded wait.
-        const bool qk = warp == kQkWarp;
-        for (int s = 0; s < (qk ? 2 : kSlots); ++s) {
-            if (!(armed & (1u << s))) continue;
-            int dummy = 0;
-            // a fill waited on parity p of the empty barrier; its full phase has parity p ^ 1
-            const uint32_t fp = ((armed_par >> s) & 1u) ^ 1u;
-            wait(qk ? &sb.qk_full[s] : &sb.v_full[s], fp, &dummy, nullptr, 0x502);
-        }
-    }
+    // Loaders: every copy they issued lands before the CTA exits (after a timeout no
+    // consumer may have waited for the last ones).
+    if (warp >= kSmWarps && warp < kSmWarps + kLoaders) cp_async_wait_all();
 }
 
 bool make_plan(const Problem &p, AttnPlan &P)
 {
     P.L = p.L; P.d = p.d; P.nb = p.nb; P.n_rounds = p.n_rounds; P.causal = p.causal;
+    P.token_order = p.token_order;
     P.scale = p.scale;
     P.nchunks = p.L / kC;
     P.tps = (P.nchunks + 1) / 2;
@@ -640,8 +717,7 @@ bool make_plan(const Problem &p, AttnPlan &P)
 size_t smem_bytes(const AttnPlan &P)
 {
     const int nkb = P.d / 64;
-    return 1024 + (size_t)2 * nkb * kWin * 128 + (size_t)kSlots * nkb * kC * 128 +
-           (size_t)kSlots * sizeof(SlotMeta);
+    return 1024 + (size_t)2 * kSlots * nkb * kC * 128 + (size_t)kSlots * sizeof(SlotMeta);
 }
 
 }  // namespace
@@ -655,11 +731,11 @@ cudaError_t attn_tc(const Problem &p, const void *qk, const void *v, const int32
                     const int32_t *perm, const int32_t *bstart, const float *inv_norm, void *o_r,
                     float *lse_r, StatusBlock *status, cudaStream_t st)
 {
+    (void)bstart;   // bucket runs come from the sorted rows' buckets (see the V loader)
     AttnPlan P;
     make_plan(p, P);
-    CUtensorMap qmap, vmap;
-    if (!make_tmap_2d_bf16(&qmap, qk, (uint64_t)p.n_tok(), (uint64_t)p.d, 64, 1) ||
-        !make_tmap_2d_bf16(&vmap, v, (uint64_t)p.n_tok(), (uint64_t)p.d, 64, 1))
+    CUtensorMap vmap;
+    if (!make_tmap_2d_bf16(&vmap, v, (uint64_t)p.n_tok(), (uint64_t)p.d, 64, 1))
         return cudaErrorNotSupported;
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -667,7 +743,7 @@ cudaError_t attn_tc(const Problem &p, const void *qk, const void *v, const int32
     cudaError_t e = cudaFuncSetAttribute(lsh_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    lsh_attn_tc_kernel<<<sms, kThreads, smem, st>>>(qmap, vmap, P, buckets, perm, bstart, inv_norm,
+    lsh_attn_tc_kernel<<<sms, kThreads, smem, st>>>(vmap, (const __nv_bfloat16 *)qk, (const __nv_bfloat16 *)v, P, buckets, perm, inv_norm,
                                                     (__nv_bfloat16 *)o_r, lse_r, status);
     return cudaGetLastError();
 }

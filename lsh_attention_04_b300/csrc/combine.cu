@@ -1,8 +1,9 @@
 // combine.cu -- un-sort the per-round outputs and combine the rounds.
 //
-// Each round r produced, in sorted order, an output row o_r and its log-normaliser
-// lse_r.  For token i the row of round r sits at sorted index inv_r[i].  The rounds are
-// weighted by their share of the total softmax mass:
+// Each round r produced an output row o_r and its log-normaliser lse_r per token, in
+// sorted order (token i's row of round r at sorted index inv_r[i]) or, inside the fused
+// forward, already in token order (at i; no index lookups).  The rounds are weighted by
+// their share of the total softmax mass:
 //   lse_i = logsumexp_r lse_r(i),   out_i = sum_r exp(lse_r(i) - lse_i) * o_r(i).
 // (Rounds run in parallel per the "Reformer" glossary, section "Atencion LSH"; the
 // logsumexp weighting is the standard way to merge softmax results computed over
@@ -51,7 +52,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kWarps * 32)
 combine_kernel(const T *__restrict__ o_r, const float *__restrict__ lse_r,
                const int32_t *__restrict__ inv, long n_tok, int L, int n_rounds,
-               float *__restrict__ out, float *__restrict__ lse)
+               int token_order, float *__restrict__ out, float *__restrict__ lse)
 {
     constexpr int EPL = D / 32;  // elements per lane, contiguous
     const int lane = threadIdx.x & 31;
@@ -67,7 +68,7 @@ combine_kernel(const T *__restrict__ o_r, const float *__restrict__ lse_r,
         const int r = r0 + lane;
         if (r < n_rounds) {
             const size_t base = (seg0 + r) * L;
-            mx = fmaxf(mx, __ldg(lse_r + base + __ldg(inv + base + i)));
+            mx = fmaxf(mx, __ldg(lse_r + base + (token_order ? i : __ldg(inv + base + i))));
         }
     }
     mx = warp_max(mx);
@@ -81,7 +82,7 @@ combine_kernel(const T *__restrict__ o_r, const float *__restrict__ lse_r,
         float w = 0.f;
         if (r < n_rounds) {
             const size_t base = (seg0 + r) * L;
-            s = __ldg(inv + base + i);
+            s = token_order ? i : __ldg(inv + base + i);
             w = expf(__ldg(lse_r + base + s) - mx);
         }
         sum += warp_sum(w);
@@ -119,14 +120,83 @@ combine_kernel(const T *__restrict__ o_r, const float *__restrict__ lse_r,
     if (lane == 0) lse[tok] = mx + logf(sum);
 }
 
+// Token-order rows (the fused forward), up to kTokRounds rounds: nothing depends on the
+// weights until the sum, so every round's row and log-normaliser is requested at once
+// (one memory round trip per token), then the warp reduces.  Two tokens per warp keep
+// more bytes in flight.
+constexpr int kTokRounds = 8;
+constexpr int kTokPerWarp = 2;
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kWarps * 32)
+combine_tok_kernel(const T *__restrict__ o_r, const float *__restrict__ lse_r, long n_tok, int L,
+                   int n_rounds, float *__restrict__ out, float *__restrict__ lse)
+{
+    constexpr int EPL = D / 32;
+    const int lane = threadIdx.x & 31;
+    const long tok0 = ((long)blockIdx.x * kWarps + (threadIdx.x >> 5)) * kTokPerWarp;
+    float x[kTokPerWarp][kTokRounds][EPL];
+    float lr[kTokPerWarp];
+#pragma unroll
+    for (int u = 0; u < kTokPerWarp; ++u) {
+        const long tok = tok0 + u;
+        const bool ok = tok < n_tok;
+        const long bh = ok ? tok / L : 0;
+        const int i = ok ? (int)(tok % L) : 0;
+        const size_t seg0 = (size_t)bh * n_rounds;
+        lr[u] = ok && lane < n_rounds ? __ldg(lse_r + (seg0 + lane) * L + i) : -INFINITY;
+#pragma unroll
+        for (int r = 0; r < kTokRounds; ++r) {
+            if (ok && r < n_rounds) {
+                load_row<EPL>(o_r + ((seg0 + r) * L + i) * D + lane * EPL, x[u][r]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) x[u][r][e] = 0.f;
+            }
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < kTokPerWarp; ++u) {
+        const long tok = tok0 + u;
+        if (tok >= n_tok) break;
+        const float mx = warp_max(lr[u]);
+        const float w = lane < n_rounds ? expf(lr[u] - mx) : 0.f;
+        const float sum = warp_sum(w);
+        float acc[EPL];
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+#pragma unroll
+        for (int r = 0; r < kTokRounds; ++r) {
+            const float wr = __shfl_sync(0xffffffffu, w, r);
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) acc[e] = fmaf(wr, x[u][r][e], acc[e]);
+        }
+        const float rs = 1.0f / sum;
+        float *dst = out + (size_t)tok * D + lane * EPL;
+        if constexpr (EPL == 4) {
+            __stcs(reinterpret_cast<float4 *>(dst), make_float4(acc[0] * rs, acc[1] * rs, acc[2] * rs, acc[3] * rs));
+        } else {
+            __stcs(reinterpret_cast<float2 *>(dst), make_float2(acc[0] * rs, acc[1] * rs));
+        }
+        if (lane == 0) lse[tok] = mx + logf(sum);
+    }
+}
+
 template <typename T, int D>
 cudaError_t launch(const Problem &p, const void *o_r, const float *lse_r, const int32_t *inv,
                    float *out, float *lse, cudaStream_t st)
 {
     const long n = p.n_tok();
+    if (p.token_order && p.n_rounds <= kTokRounds) {
+        const long per_block = (long)kWarps * kTokPerWarp;
+        const unsigned grid = (unsigned)((n + per_block - 1) / per_block);
+        combine_tok_kernel<T, D><<<grid, kWarps * 32, 0, st>>>((const T *)o_r, lse_r, n, p.L,
+                                                               p.n_rounds, out, lse);
+        return cudaGetLastError();
+    }
     const unsigned grid = (unsigned)((n + kWarps - 1) / kWarps);
     combine_kernel<T, D><<<grid, kWarps * 32, 0, st>>>((const T *)o_r, lse_r, inv, n, p.L,
-                                                       p.n_rounds, out, lse);
+                                                       p.n_rounds, p.token_order, out, lse);
     return cudaGetLastError();
 }
 

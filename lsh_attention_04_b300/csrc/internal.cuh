@@ -56,6 +56,10 @@ struct Problem {
     int B, H, L, d, nb, n_rounds, chunk, causal;
     float scale;
     lsh_dtype_t dtype;
+    // Attention output rows (o_r, lse_r) at the token's original position instead of its
+    // sorted index; the round combination then reads them without the inverse
+    // permutation.  Internal to the fused forward.
+    int token_order = 0;
     long n_tok() const { return (long)B * H * L; }
     long n_seg() const { return (long)B * H * n_rounds; }
 };

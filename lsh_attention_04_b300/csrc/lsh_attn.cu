@@ -151,10 +151,13 @@ lsh_status_t forward(const void *qk, const void *v, const void *R, lsh_dtype_t d
                      float scale, float *out, float *lse, void *workspace,
                      size_t workspace_bytes, void *stream, void *const *events)
 {
-    const Problem p = make_problem(B, H, L, d, n_buckets, n_rounds, chunk, causal, scale, dtype);
+    Problem p = make_problem(B, H, L, d, n_buckets, n_rounds, chunk, causal, scale, dtype);
     lsh_status_t s = validate(p);
     if (s != LSH_OK) return s;
     if (!qk || !v || !R || !out || !lse || !workspace) return LSH_ERR_INVALID_ARGUMENT;
+    // attention writes each round's rows at the tokens' own positions, so the round
+    // combination streams them (no inverse-permutation gather)
+    p.token_order = 1;
     if (((uintptr_t)workspace) % 256 != 0) return LSH_ERR_INVALID_ARGUMENT;
     const Layout w = layout(p);
     if (workspace_bytes < w.total) return LSH_ERR_WORKSPACE_TOO_SMALL;

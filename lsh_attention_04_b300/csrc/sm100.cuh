@@ -131,6 +131,11 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
                     "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]),
                     "r"(r[13]), "r"(r[14]), "r"(r[15]) : "memory");
 }
+// 16 zero columns into this thread's lane.
+__device__ __forceinline__ void tmem_st16_zero(uint32_t taddr) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,"
+                 "%1,%1,%1,%1,%1,%1};" :: "r"(taddr), "r"(0u) : "memory");
+}
 __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -213,7 +218,6 @@ extern __device__ unsigned long long g_wait_count[4096];
 
 static __device__ __noinline__ bool wait_impl(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
                                        StatusBlock *st, int where) {
-    if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait_sleep(bar, parity, 20000)) return true;
@@ -231,13 +235,16 @@ static __device__ __forceinline__ bool wait(uint64_t *bar, uint32_t parity, vola
                                             StatusBlock *st, int where) {
 #ifdef LSH_WAIT_PROF
     const long long c0 = clock64();
-    const bool ok = wait_impl(bar, parity, abort_flag, st, where);
+    const bool ok = mbar_try_wait(bar, parity) || wait_impl(bar, parity, abort_flag, st, where);
     if ((threadIdx.x & 31) == 0) {
         atomicAdd(&g_wait_cycles[where & 4095], (unsigned long long)(clock64() - c0));
         atomicAdd(&g_wait_count[where & 4095], 1ull);
     }
     return ok;
 #else
+    // Fast path inline: a phase that is already complete costs no call (a call would
+    // also make the caller's loads in flight land before it).
+    if (mbar_try_wait(bar, parity)) return true;
     return wait_impl(bar, parity, abort_flag, st, where);
 #endif
 }
@@ -269,6 +276,9 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
 // 16-byte asynchronous copy global -> shared (L2 only, bypassing L1).
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
 }
 __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
