@@ -34,13 +34,19 @@ L2_BYTES = 126 * 2 ** 20
 FP32_ALU_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
 
 
-# What bounds each kernel of the forward pass, per input dtype: the bf16 contractions
-# run on the tensor cores, the fp32 ones on the CUDA cores' FFMA lanes; sort and
-# combine move data.
-KERNEL_BOUND = {
-    "bf16": {"hash": "alu", "sort": "hbm", "attn": "alu", "combine": "hbm"},
-    "f32": {"hash": "alu", "sort": "hbm", "attn": "alu", "combine": "hbm"},
+# Where each kernel's arithmetic runs: the bf16 contractions (hash projection, QK^T and
+# P V) on the tensor cores, the fp32 ones on the CUDA cores' FFMA lanes.  A kernel's
+# bound is the slower of its FLOPs at that peak and its bytes at HBM bandwidth.
+COMPUTE_UNIT = {"bf16": "tensor", "f32": "alu"}
+# Kernel sources per stage: a DRAM-traffic figure recorded from ncu counts only while
+# these files are unchanged.
+KERNEL_SOURCES = {
+    "hash": ["hash_tc.cu", "sm100.cuh", "tmap.cu"],
+    "sort": ["sort.cu"],
+    "attn": ["attn_tc.cu", "sm100.cuh", "tmap.cu"],
+    "combine": ["combine.cu"],
 }
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
 
 def load_peaks():
@@ -50,6 +56,27 @@ def load_peaks():
         return p, "measured"
     except (OSError, ValueError):
         return FALLBACK, "fallback"
+
+
+def source_digest(stage):
+    import hashlib
+    h = hashlib.sha1()
+    for f in KERNEL_SOURCES[stage]:
+        with open(os.path.join(ROOT, "lsh_attention_04_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload, stage):
+    """DRAM bytes per launch of `stage` on `workload` from the ncu summary, or None when
+    there is none or the kernel's sources changed since it was taken."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+        k = rec[workload][stage]
+    except (OSError, ValueError, KeyError):
+        return None
+    return k["bytes_per_launch"] if k.get("source_sha1") == source_digest(stage) else None
 
 
 # ------------------------------------------------------------------ algorithmic work
@@ -67,7 +94,8 @@ def work(w):
     k["sort"] = dict(flops=0, bytes=N * R * 4 + N * R * 8 + S * (nb + 1) * 4)
     k["attn"] = dict(flops=8 * N * R * c * d,  # QK^T and PV over the c x 2c window
                      bytes=2 * N * d * e + N * R * (d * wr + 4) + N * R * 8 + N * 4)
-    k["combine"] = dict(flops=0, bytes=N * R * (d * wr + 8) + N * (4 * d + 4))
+    # token-order rows (fused forward): o_r and lse_r read once, no inverse permutation
+    k["combine"] = dict(flops=0, bytes=N * R * (d * wr + 4) + N * (4 * d + 4))
     return k
 
 
@@ -183,6 +211,11 @@ def allmax(dist, x):
     t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_value(tokens_per_rank, world, ms_max):
+    """Whole-job throughput: the units every rank processed over the slowest rank's time."""
+    return tokens_per_rank * world / (ms_max / 1e3)
 
 
 def run_reference(args, w):
@@ -317,32 +350,32 @@ def run_ours(args, w):
         return 0
 
     tokens = w.tokens * world
-    value = tokens / (ms_max / 1e3)
+    value = job_value(w.tokens, world, ms_max)
     peaks, peak_src = load_peaks()
     wk = work(w)
     # dominant kernel and its roofline
     dom = max(stage_ms, key=stage_ms.get)
-    kern_bound = dict(KERNEL_BOUND[w.dtype])
+    unit_c = COMPUTE_UNIT[w.dtype]
+    peak_c = peaks["bf16_tflops"] if unit_c == "tensor" else FP32_ALU_TFLOPS
 
     def roof(name):
         t = stage_ms[name] / 1e3
-        b = kern_bound[name]
-        if b == "hbm":
-            ach = wk[name]["bytes"] / t / 1e9
-            peak = peaks["hbm_gbs"]
-            unit = "GB/s"
-        elif b == "tensor":
-            ach = wk[name]["flops"] / t / 1e12
-            peak = peaks["bf16_tflops"]
-            unit = "TFLOP/s"
+        f, by = wk[name]["flops"], wk[name]["bytes"]
+        t_c = f / (peak_c * 1e12)
+        t_b = by / (peaks["hbm_gbs"] * 1e9)
+        if t_c > t_b:
+            b, ach, peak, unit = unit_c, f / t / 1e12, peak_c, "TFLOP/s"
+            src = (f"{peak_src} bf16 burst" if unit_c == "tensor" else "fp32 lanes x clock")
         else:
-            ach = wk[name]["flops"] / t / 1e12
-            peak = FP32_ALU_TFLOPS
-            unit = "TFLOP/s"
-        return {"bound": b, "achieved": ach, "peak": peak, "unit": unit, "frac": ach / peak,
-                "traffic": None, "kernel": name, "ms": stage_ms[name],
-                "algorithmic_flops": wk[name]["flops"], "algorithmic_bytes": wk[name]["bytes"],
-                "peak_source": peak_src if b != "alu" else "fp32 lanes x clock"}
+            b, ach, peak, unit = "hbm", by / t / 1e9, peaks["hbm_gbs"], "GB/s"
+            src = f"{peak_src} copy bandwidth"
+        r = {"bound": b, "achieved": ach, "peak": peak, "unit": unit, "frac": ach / peak,
+             "traffic": recorded_traffic(w.name, name), "kernel": name, "ms": stage_ms[name],
+             "roof_ms": 1e3 * max(t_c, t_b), "algorithmic_flops": f, "algorithmic_bytes": by,
+             "peak_source": src}
+        if f and unit_c == "tensor":
+            r["tensor_frac"] = f / t / 1e12 / peak_c   # of the measured dense bf16 peak
+        return r
 
     F = sum(k["flops"] for k in wk.values())
     Bts = sum(k["bytes"] for k in wk.values())

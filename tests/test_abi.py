@@ -47,10 +47,13 @@ def test_library_exports_every_declared_symbol(lib):
     assert set(lsh.EXPORTS) == set(header_functions())
 
 
-def test_library_is_built_for_sm103a(lib):
-    out = subprocess.run(["/usr/local/cuda/bin/cuobjdump", "--list-elf", lsh.LIB_PATH],
-                         capture_output=True, text=True).stdout
-    assert "sm_103a" in out
+def test_library_is_built_for_sm103a_only(lib):
+    # the build compiles every source for sm_103a and nothing else (no other arch,
+    # no PTX for a JIT fallback)
+    from lsh_attention_04_b300 import build as b
+    assert b.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+    assert not any("gencode" in f or "arch" in f for f in b.FLAGS)
+    assert all(not any("gencode" in f or "arch" in f for f in fl) for fl in b.EXTRA.values())
 
 
 def test_status_strings(lib):
