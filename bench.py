@@ -420,9 +420,14 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=gen.HEADLINE, choices=sorted(gen.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="run the workload with this many heads instead (small ncu captures); "
+                         "the printed line then names the reduced workload")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
     w = gen.WORKLOADS[args.workload]
+    if args.heads > 0 and args.heads != w.H:
+        w = w.replace(H=args.heads, name=w.name.replace(f"_H{w.H}_", f"_H{args.heads}_"))
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)
