@@ -37,16 +37,15 @@
 // Data movement: a ring of 6 chunk slots (chunk c in slot c mod 6) holds each chunk's
 // Q/K rows, V rows and row metadata, loaded once and released after the last P V that
 // reads the chunk.  Rows are gathered through the sort permutation by 16-byte cp.async
-// pieces written straight into the 128-byte-swizzled operand layout, and (V rows
-// 0-31 of each chunk) by the tensor-map gather, 4 rows per operation.  Neither engine
-// alone keeps up: the tensor-map gather moves about 7 bytes per clock per SM at this
-// size (512 bytes per operation), one warp's cp.async stream about 10, so two loader
-// warps take alternate chunks and both engines run side by side.  The MMA warps fence the async proxy after each wait,
-// since the rows were written through the generic one.
-// Warp roles: 0-7 softmax + output epilogue (warps w and w+4 share TMEM lane quarter w
-// and split the row's columns and O's columns), 8-9 loaders (warp 8 + (c & 1) fills
-// chunk c: one owner per slot, so each slot's fills and the parity waits on its barrier
-// happen in order), 10 S issuer and TMEM owner, 11 P V issuer.
+// pieces written straight into the 128-byte-swizzled operand layout (row r's piece c at
+// r * 128 + ((c ^ (r & 7)) * 16)).  (A tensor-map gather moves only 512 bytes per
+// operation here, about 7 bytes per clock per SM, and its issue stalls the issuing warp;
+// one warp's cp.async stream manages about 5-10.)  So every chunk is filled by several
+// loader warps at once.  The MMA warps fence the async proxy after each wait, since the
+// rows were written through the generic one.
+// Warp roles (16 warps, 128 registers each): 0-7 softmax + output epilogue (warps w and
+// w+4 share TMEM lane quarter w and split the row's columns and O's columns), 8 the
+// metadata warp, 9-13 row copiers, 14 S issuer and TMEM owner, 15 P V issuer.
 // Persistent CTAs take contiguous ranges of tiles of a group of heads small enough for
 // L2, so all rounds of those heads share cached rows.  Every wait is bounded
 // (sm100::wait); on a timeout the kernel records where in the workspace status block and
@@ -65,7 +64,8 @@ constexpr int kRows = 128;        // rows per tile
 constexpr int kWin = 192;         // S columns per tile (window rows)
 constexpr int kSlots = 6;         // chunk ring (even: chunk parity = slot parity)
 constexpr int kSmWarps = 8;       // softmax / epilogue warps
-constexpr int kLoaders = 2;       // loader warps (12 warps in all: 3 per scheduler keeps 168 registers per thread)
+constexpr int kLoaders = 6;       // loader warps: 1 metadata warp + kCopyWarps row copiers
+constexpr int kCopyWarps = kLoaders - 1;
 constexpr int kSWarp = kSmWarps + kLoaders;
 constexpr int kPvWarp = kSWarp + 1;
 constexpr int kThreads = (kPvWarp + 1) * 32;
@@ -131,16 +131,6 @@ __device__ __forceinline__ bool for_items(const AttnPlan &P, F &&f) {
     return true;
 }
 
-// Four rows (r0..r3) of 64 columns from column x, by the tensor-map gather, into 512
-// contiguous bytes (the map's 128-byte swizzle applied); completes `bytes` on bar.
-__device__ __forceinline__ void gather4(uint32_t dst, const CUtensorMap *map, int x, int r0, int r1,
-                                        int r2, int r3, uint32_t bar) {
-    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-                 " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
-                 :: "r"(dst), "l"((uint64_t)map), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
-                 : "memory");
-}
-
 // Range checks of a self-checking build (-DLSH_CHECKED): a failed check records `code`
 // in the status block and the access is skipped (the index is replaced by 0).
 #ifdef LSH_CHECKED
@@ -159,29 +149,6 @@ __device__ __forceinline__ void gather4(uint32_t dst, const CUtensorMap *map, in
 #else
 #define LSH_ROW(j, L, code) ((unsigned)(j) < (unsigned)(L) ? (j) : 0)
 #endif
-
-// Gather the 64 rows of a chunk into a K-major, 128-byte-swizzled tile: row r (global
-// row row_base + j_r, where lane k holds j of rows k and k + 32) lands at byte r * 128 of
-// each 64-column block (blocks kb_stride bytes apart), its 16-byte pieces permuted by
-// the swizzle (piece c of row r at ((c ^ (r & 7)) * 16)); rows r0..63 only.  16-byte
-// cp.async pieces, d / 8 lanes per row (whole rows per instruction).  Completion is
-// tracked by the caller (cp.async mbarrier arrive).
-__device__ __forceinline__ void gather_chunk(uint32_t dst, uint32_t kb_stride,
-                                             const __nv_bfloat16 *__restrict__ src,
-                                             long long row_base, int j0, int j1, int d, int lane,
-                                             int r0 = 0) {
-    const int lpr = d >> 3;                       // lanes per row
-    const int c = lane & (lpr - 1), kb = c >> 3, c16 = c & 7;
-    const int rstep = 32 / lpr;
-    const uint32_t dcol = dst + kb * kb_stride;
-    const __nv_bfloat16 *scol = src + row_base * d + c * 8;
-#pragma unroll 4
-    for (int r = r0 + lane / lpr; r < 64; r += rstep) {
-        const int a = __shfl_sync(0xffffffffu, j0, r & 31);
-        const int b = __shfl_sync(0xffffffffu, j1, r & 31);
-        cp_async16(dcol + r * 128 + ((c16 ^ (r & 7)) << 4), scol + (long long)(r < 32 ? a : b) * d);
-    }
-}
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -212,21 +179,21 @@ __device__ __forceinline__ uint32_t range_mask(int lo, int hi) {
     return below_hi & (0xffffffffu << lo);
 }
 
-// One 32-column batch of a row: p_j = 2^(s_j * cs_j - m2) for the columns whose bit is
-// set in `vm`, 0 elsewhere (ex2 of -inf), packed to bf16 pairs.  Returns sum_j p_j.
-// `cs` is 16-byte aligned shared memory.
-__device__ __forceinline__ float softmax_batch(const uint32_t (&s32)[32], const float *cs,
-                                               uint32_t vm, float m2, uint32_t (&pk)[16]) {
+// One 16-column quarter of a row: p_j = 2^(s_j * cs_j - m2) for the columns whose bit
+// is set in the low 16 bits of `vm`, 0 elsewhere (ex2 of -inf), packed to bf16 pairs.
+// Returns sum_j p_j.  `cs` is 16-byte aligned shared memory.
+__device__ __forceinline__ float softmax_quarter(const uint32_t (&s16)[16], const float *cs,
+                                                 uint32_t vm, float m2, uint32_t (&pk)[8]) {
     float la = 0.f, lb = 0.f;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
+    for (int q = 0; q < 4; ++q) {
         const float4 c4 = reinterpret_cast<const float4 *>(cs)[q];
         const float c[4] = {c4.x, c4.y, c4.z, c4.w};
         float p[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int jj = 4 * q + e;
-            const float x = fmaf(__uint_as_float(s32[jj]), c[e], -m2);
+            const float x = fmaf(__uint_as_float(s16[jj]), c[e], -m2);
             p[e] = ex2((vm >> jj) & 1u ? x : -INFINITY);
         }
         pk[2 * q] = pack_bf16(p[0], p[1]);
@@ -238,8 +205,7 @@ __device__ __forceinline__ float softmax_batch(const uint32_t (&s32)[32], const 
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-lsh_attn_tc_kernel(const __grid_constant__ CUtensorMap vmap,
-                   const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *__restrict__ vv,
+lsh_attn_tc_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *__restrict__ vv,
                    const AttnPlan P, const int32_t *__restrict__ buckets,
                    const int32_t *__restrict__ perm,
                    const float *__restrict__ inv_norm, __nv_bfloat16 *__restrict__ o_r,
@@ -247,6 +213,9 @@ lsh_attn_tc_kernel(const __grid_constant__ CUtensorMap vmap,
 {
     extern __shared__ uint8_t smem_raw[];
     __shared__ AttnBarriers sb;
+#ifdef LSH_WAIT_PROF
+    __shared__ volatile long long slot_clk[kSlots];   // when a slot's fill was released
+#endif
     __shared__ float l_part[kLBufs][2][kRows];   // partial row sums of the two column halves
     // 1024-byte aligned base, derived from the shared array by pointer arithmetic so the
     // compiler keeps the shared state space (shared loads, not generic ones)
@@ -265,8 +234,9 @@ lsh_attn_tc_kernel(const __grid_constant__ CUtensorMap vmap,
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kSlots; ++s) {
-            mbar_init(&sb.full[s], 32 + 32 + 1);    // loader lanes: cp.async + metadata;
-                                                    // expect_tx of the tensor-map rows
+            // metadata lanes + copy warps' cp.async lanes
+            mbar_init(&sb.full[s], 32 + 32 * kCopyWarps);
+
             mbar_init(&sb.empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -290,21 +260,71 @@ lsh_attn_tc_kernel(const __grid_constant__ CUtensorMap vmap,
 
     if (warp >= kSmWarps && warp < kSmWarps + kLoaders) {
         // ------------------------------------------------------------- loaders
-        const int lw = warp - kSmWarps;              // fills the chunks c with c & 1 == lw
-        uint32_t e_bits = (1u << kSlots) - 1;        // parity to wait per slot
-        uint32_t armed = 0;                          // slots with a fill issued (wind-down)
-        if (lane == 0) prefetch_tmap(&vmap);
+        // Every chunk is filled by all loader warps together, so a chunk lands in about a
+        // fifth of the time one warp's cp.async stream needs (the ring cannot hold more
+        // chunks in flight).  Warp kSmWarps is the metadata warp (row metadata); the copy
+        // warps copy the Q/K and V rows.  Every loader waits for the slot itself and
+        // takes part in every fill of every slot, in order, so no warp can fall a phase
+        // behind on a slot's barriers (a fill completes only with every warp's arrival).
+        const int lw = warp - kSmWarps;
+        uint32_t e_bits = (1u << kSlots) - 1;        // parity of the next empty wait, per slot
         const float ascale = fabsf(P.scale) * kLog2e, cscale = P.scale * kLog2e;
         for_items(P, [&](long long seg, int tb, int te) -> bool {
             const long long bh = seg / P.n_rounds;
-            int c = tb > 0 ? 2 * tb - 1 : 0;
+            const int c_begin = tb > 0 ? 2 * tb - 1 : 0;
             const int c_end = min(2 * te, P.nchunks);
-            if ((c & 1) != lw) ++c;
-            if (c >= c_end) return true;
             const size_t seg_row0 = (size_t)seg * P.L;
-            // Row metadata is software-pipelined over this warp's chunks (c, c + 2, ...):
-            // the permutation two chunks ahead, buckets and norms one chunk ahead.  Lane k
-            // holds rows k and k + 32; every lane also holds the row before the chunk.
+            if (lw > 0) {
+                // ---- copy warp k = lw - 1: row groups g = k, k + kCopyWarps, ... of
+                // rpi = 32 / (d / 8) rows, from both Q/K and V.  Each lane loads the
+                // permutation entry of its own row, one chunk ahead.
+                const int k = lw - 1;
+                const int lpr = P.d >> 3, rpi = 32 / lpr;
+                const int cpiece = lane & (lpr - 1), c16 = cpiece & 7, kb = cpiece >> 3;
+                const int rsub = lane / lpr;
+                const int n_grp = kC / rpi;
+                constexpr int kMine = (kC / 2 + kCopyWarps - 1) / kCopyWarps;  // groups per warp (d = 128)
+                int jn[kMine];
+                auto ld_j = [&](int cc) {
+#pragma unroll
+                    for (int q = 0; q < kMine; ++q) {
+                        const int g = k + q * kCopyWarps;
+                        jn[q] = g < n_grp ? LSH_ROW(perm[LSH_IDX(seg_row0 + (size_t)cc * kC + g * rpi + rsub,
+                                                                   n_rows, 0x51c)], P.L, 0x51d)
+                                          : 0;
+                    }
+                };
+                if (c_begin < c_end) ld_j(c_begin);
+                for (int c = c_begin; c < c_end; ++c) {
+                    const int s = c % kSlots;
+                    int jc[kMine];
+#pragma unroll
+                    for (int q = 0; q < kMine; ++q) jc[q] = jn[q];
+                    if (c + 1 < c_end) ld_j(c + 1);
+                    const bool ok = wait(&sb.empty[s], (e_bits >> s) & 1u, abort_flag, status, 0x504);
+                    if (!__all_sync(FULL, ok)) return false;
+                    e_bits ^= 1u << s;
+                    const uint32_t qdst = smem_u32(QK + s * kC * 128) + kb * qk_plane;
+                    const uint32_t vdst = smem_u32(V + s * vslot) + kb * kC * 128;
+#pragma unroll
+                    for (int q = 0; q < kMine; ++q) {
+                        const int g = k + q * kCopyWarps;
+                        if (g >= n_grp) break;
+                        const int r = g * rpi + rsub;
+                        const long long off = (bh * P.L + jc[q]) * P.d + cpiece * 8;
+                        const uint32_t sw = r * 128 + ((c16 ^ (r & 7)) << 4);
+                        cp_async16(qdst + sw, qk + off);
+                        cp_async16(vdst + sw, vv + off);
+                    }
+                    cp_async_mbar_arrive(&sb.full[s]);
+                }
+                return true;
+            }
+            // ---- metadata warp.  Loads are software-pipelined over the chunks: the
+            // permutation two chunks ahead, buckets and norms one chunk ahead.  Lane k holds
+            // rows k and k + 32; every lane also holds the row before the chunk.
+            int c = c_begin;
+            if (c >= c_end) return true;
             int ja0 = 0, ja1 = 0, jap = 0, jb0 = 0, jb1 = 0, jbp = 0;
             auto ld_perm = [&](int cc, int &j0, int &j1, int &jp) {
                 const size_t row0 = seg_row0 + (size_t)cc * kC;
@@ -322,9 +342,10 @@ lsh_attn_tc_kernel(const __grid_constant__ CUtensorMap vmap,
                 nm1 = inv_norm[LSH_IDX(bh * P.L + j1, n_tok, 0x516)];
             };
             ld_perm(c, ja0, ja1, jap);
-            if (c + 2 < c_end) ld_perm(c + 2, jb0, jb1, jbp);
+            if (c + 1 < c_end) ld_perm(c + 1, jb0, jb1, jbp);
             ld_rows(ja0, ja1, jap);
-            for (; c < c_end; c += 2) {
+            for (; c < c_end; ++c) {
+                LSH_SPAN_BEGIN(t_meta);
                 const int s = c % kSlots;
                 const uint32_t pe = (e_bits >> s) & 1u;
                 const int j0 = ja0, j1 = ja1, b0 = bk0, b1 = bk1, bp = bkp;
@@ -332,8 +353,8 @@ lsh_attn_tc_kernel(const __grid_constant__ CUtensorMap vmap,
                 ja0 = jb0;
                 ja1 = jb1;
                 jap = jbp;
-                if (c + 4 < c_end) ld_perm(c + 4, jb0, jb1, jbp);
-                if (c + 2 < c_end) ld_rows(ja0, ja1, jap);
+                if (c + 2 < c_end) ld_perm(c + 2, jb0, jb1, jbp);
+                if (c + 1 < c_end) ld_rows(ja0, ja1, jap);
                 // where bucket runs start and end inside the chunk
                 const int up0 = __shfl_up_sync(FULL, b0, 1), up1 = __shfl_up_sync(FULL, b1, 1);
                 const int last0 = __shfl_sync(FULL, b0, 31);
@@ -350,52 +371,25 @@ lsh_attn_tc_kernel(const __grid_constant__ CUtensorMap vmap,
                 bool ok = wait(&sb.empty[s], pe, abort_flag, status, 0x503);
                 if (!__all_sync(FULL, ok)) return false;
                 e_bits ^= 1u << s;   // now the parity of this fill's full phase
-                LSH_SPAN_BEGIN(t_g);
-                // Two copy engines in parallel: the tensor-map gather takes V rows 0-31
-                // (4 rows per operation, lanes 0-7), cp.async the Q/K rows and V rows 32-63.
-                if (lane == 0) mbar_expect_tx(&sb.full[s], (uint32_t)(32 * P.d * 2));
-                __syncwarp();
-                {
-                    int g[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        g[k] = (int)(bh * P.L) + __shfl_sync(FULL, j0, (4 * lane + k) & 31);
-                    if (lane < 8)
-                        for (int kb = 0; kb < nkb; ++kb)
-                            gather4(smem_u32(V + s * vslot + kb * kC * 128 + 4 * lane * 128), &vmap,
-                                    kb * 64, g[0], g[1], g[2], g[3], smem_u32(&sb.full[s]));
-                }
-                gather_chunk(smem_u32(QK + s * kC * 128), qk_plane, qk, bh * P.L, j0, j1, P.d, lane);
-                gather_chunk(smem_u32(V + s * vslot), kC * 128, vv, bh * P.L, j0, j1, P.d, lane, 32);
-                cp_async_mbar_arrive(&sb.full[s]);
-                armed |= 1u << s;
-                LSH_SPAN_END(t_g, 0x5a0);
                 SlotMeta &m = meta[s];
+                m.jrow[lane] = j0;
+                m.jrow[lane + 32] = j1;
+#ifdef LSH_WAIT_PROF
+                if (lane == 0) slot_clk[s] = clock64();
+#endif
                 m.cs[lane] = cscale * n0;
                 m.cs[lane + 32] = cscale * n1;
                 m.m2[lane] = n0 > 0.f ? ascale / n0 : 0.f;
                 m.m2[lane + 32] = n1 > 0.f ? ascale / n1 : 0.f;
-                m.jrow[lane] = j0;
-                m.jrow[lane + 32] = j1;
                 if (lane == 0) {
                     m.starts = starts;
                     m.ends = ends;
                 }
                 mbar_arrive(&sb.full[s]);
+                LSH_SPAN_END(t_meta, 0x5b0);
             }
             return true;
         });
-        if (*abort_flag) {
-            // wind-down after a timeout: the last fill of each slot may still be in
-            // flight (no consumer waited for it); its full phase completes once its
-            // copies land, every arrival of the fill having been made
-            cp_async_wait_all();
-            for (int s = 0; s < kSlots; ++s) {
-                if (!(armed & (1u << s))) continue;
-                int dummy = 0;
-                wait(&sb.full[s], (e_bits >> s) & 1u, &dummy, nullptr, 0x502);
-            }
-        }
     } else if (warp == kSWarp) {
         // ------------------------------------------------------------- S issuer
         {
@@ -406,6 +400,12 @@ lsh_attn_tc_kernel(const __grid_constant__ CUtensorMap vmap,
                 const int s = c % kSlots;
                 const bool ok = wait_w(&sb.full[s], (f_bits >> s) & 1u, abort_flag, status, 0x601);
                 f_bits ^= 1u << s;
+#ifdef LSH_WAIT_PROF
+                if (lane == 0) {   // from the slot's release to the S issuer seeing it full
+                    atomicAdd(&g_wait_cycles[0x5b1], (unsigned long long)(clock64() - slot_clk[s]));
+                    atomicAdd(&g_wait_count[0x5b1], 1ull);
+                }
+#endif
                 return ok;
             };
             for_items(P, [&](long long, int tb, int te) -> bool {
@@ -631,38 +631,62 @@ lsh_attn_tc_kernel(const __grid_constant__ CUtensorMap vmap,
                 LSH_SPAN_END(t_setup, 0x791);
                 LSH_SPAN_BEGIN(t_sm);
                 float l = 0.f;
-                // both 32-column batches in flight before one wait
+                // This warp's 64 columns are two 32-key batches (a mask and key scales
+                // each), processed as four 16-column quarters through two register
+                // buffers: quarter q+1 loads while q becomes P, so a tcgen05.ld is always
+                // in flight and the warp needs 32 registers of S, not 64.  P of quarter q
+                // (8 words at cc + 8 (q & 1)) only covers S columns already read.
                 const bool nb0 = batch_needed(colA), nb1 = batch_needed(colA + 32);
-                uint32_t s32[2][32];
-                if (nb0) tmem_ld32(sbase + colA, s32[0]);
-                if (nb1) tmem_ld32(sbase + colA + 32, s32[1]);
-                if (nb0 || nb1) tmem_wait_ld(s32[0], s32[1]);
+                uint32_t vmb[2];
+                const float *csb[2];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int cc = colA + 32 * h;
-                    if (!(h ? nb1 : nb0)) {
-                        tmem_st16_zero(sbase + cc);
-                        continue;
-                    }
                     const int t0 = tk0 + cc;               // sorted index of batch column 0
                     uint32_t vm = live ? range_mask(klo - t0, khi - t0) : 0u;
-                    const bool self_batch = cc == self_c0; // the rows' own columns
-                    if (self_batch && !P.causal) vm &= ~(1u << lane);
-                    const float *cs = meta[(2 * t - 1 + cc / kC + kSlots) % kSlots].cs + (cc & (kC - 1));
-                    uint32_t pk[16];
-                    l += softmax_batch(s32[h], cs, vm, m2, pk);
-                    // a row with no key but itself: weight 1 on its own column (all its
-                    // other columns are masked, so its sum was 0)
-                    if (self_batch) {   // (selects, not a conditional store into pk,
-                                        // which would move pk to local memory)
-                        const uint32_t one = (lane & 1) ? 0x3F800000u : 0x00003F80u;
-                        const int kself = self_only ? (lane >> 1) : -1;
-#pragma unroll
-                        for (int k = 0; k < 16; ++k) pk[k] = k == kself ? one : pk[k];
-                        l = self_only ? 1.f : l;
-                    }
-                    tmem_st16(sbase + cc, pk);
+                    if (cc == self_c0 && !P.causal) vm &= ~(1u << lane);
+                    vmb[h] = vm;
+                    csb[h] = meta[(2 * t - 1 + cc / kC + kSlots) % kSlots].cs + (cc & (kC - 1));
                 }
+                const bool self_here = colA == self_c0 || colA + 32 == self_c0;
+                auto quarter = [&](const uint32_t (&sq)[16], int q) {
+                    const int h = q >> 1, hq = q & 1;
+                    const int cc = colA + 32 * h;
+                    uint32_t pk[8];
+                    l += softmax_quarter(sq, csb[h] + 16 * hq, vmb[h] >> (16 * hq), m2, pk);
+                    if (cc == self_c0) {
+                        // a row with no key but itself: weight 1 on its own column (all
+                        // its other columns are masked).  Selects, not a conditional store
+                        // into pk, which would move pk to local memory.
+                        const uint32_t one = (lane & 1) ? 0x3F800000u : 0x00003F80u;
+                        const int kself = self_only && (lane >> 4) == hq ? (lane & 15) >> 1 : -1;
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) pk[k] = k == kself ? one : pk[k];
+                    }
+                    tmem_st8(sbase + cc + 8 * hq, pk);
+                };
+                uint32_t qa[16], qb[16];
+                if (nb0) {
+                    tmem_ld16(sbase + colA, qa);
+                    tmem_wait_ld16(qa);
+                    tmem_ld16(sbase + colA + 16, qb);
+                    quarter(qa, 0);
+                    tmem_wait_ld16(qb);
+                } else {
+                    tmem_st16_zero(sbase + colA);
+                }
+                if (nb1) tmem_ld16(sbase + colA + 32, qa);
+                if (nb0) quarter(qb, 1);
+                if (nb1) {
+                    tmem_wait_ld16(qa);
+                    tmem_ld16(sbase + colA + 48, qb);
+                    quarter(qa, 2);
+                    tmem_wait_ld16(qb);
+                    quarter(qb, 3);
+                } else {
+                    tmem_st16_zero(sbase + colA + 32);
+                }
+                if (self_here && self_only) l = 1.f;
                 LSH_SPAN_END(t_sm, 0x781);
                 LSH_SPAN_BEGIN(t_tail);
                 tmem_st16_zero(sbase + colZ);
@@ -734,16 +758,13 @@ cudaError_t attn_tc(const Problem &p, const void *qk, const void *v, const int32
     (void)bstart;   // bucket runs come from the sorted rows' buckets (see the V loader)
     AttnPlan P;
     make_plan(p, P);
-    CUtensorMap vmap;
-    if (!make_tmap_2d_bf16(&vmap, v, (uint64_t)p.n_tok(), (uint64_t)p.d, 64, 1))
-        return cudaErrorNotSupported;
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const size_t smem = smem_bytes(P);
     cudaError_t e = cudaFuncSetAttribute(lsh_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    lsh_attn_tc_kernel<<<sms, kThreads, smem, st>>>(vmap, (const __nv_bfloat16 *)qk, (const __nv_bfloat16 *)v, P, buckets, perm, inv_norm,
+    lsh_attn_tc_kernel<<<sms, kThreads, smem, st>>>((const __nv_bfloat16 *)qk, (const __nv_bfloat16 *)v, P, buckets, perm, inv_norm,
                                                     (__nv_bfloat16 *)o_r, lse_r, status);
     return cudaGetLastError();
 }
