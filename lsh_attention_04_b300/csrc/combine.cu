@@ -203,8 +203,10 @@ cudaError_t launch(const Problem &p, const void *o_r, const float *lse_r, const 
 }  // namespace
 
 cudaError_t combine_launch(const Problem &p, const void *o_r, const float *lse_r,
-                           const int32_t *inv, float *out, float *lse, cudaStream_t st)
+                           const int32_t *inv, float *out, float *lse, cudaStream_t st,
+                           StatusBlock *status)
 {
+    if (combine_tma_supported(p)) return combine_tma(p, o_r, lse_r, out, lse, status, st);
     if (p.dtype == LSH_F32)
         return p.d == 64 ? launch<float, 64>(p, o_r, lse_r, inv, out, lse, st)
                          : launch<float, 128>(p, o_r, lse_r, inv, out, lse, st);

@@ -86,6 +86,11 @@ cudaError_t attn_tc(const Problem &p, const void *qk, const void *v, const int32
                     float *lse_r, StatusBlock *status, cudaStream_t st);
 
 cudaError_t combine_launch(const Problem &p, const void *o_r, const float *lse_r,
-                           const int32_t *inv, float *out, float *lse, cudaStream_t st);
+                           const int32_t *inv, float *out, float *lse, cudaStream_t st,
+                           StatusBlock *status = nullptr);
+// token-order rows, bf16, <= 8 rounds: the TMA-fed combination (status may be null)
+bool combine_tma_supported(const Problem &p);
+cudaError_t combine_tma(const Problem &p, const void *o_r, const float *lse_r, float *out,
+                        float *lse, StatusBlock *status, cudaStream_t st);
 
 }  // namespace lsh

@@ -181,7 +181,8 @@ lsh_status_t forward(const void *qk, const void *v, const void *R, lsh_dtype_t d
     if ((s = run_attn(p, qk, v, buckets, perm, bstart, inv_norm, o_r, lse_r, workspace, st)) != LSH_OK)
         return s;
     if ((s = record(events, 3, st)) != LSH_OK) return s;
-    if ((s = cuda_status(combine_launch(p, o_r, lse_r, inv, out, lse, st))) != LSH_OK) return s;
+    if ((s = cuda_status(combine_launch(p, o_r, lse_r, inv, out, lse, st, (StatusBlock *)workspace))) != LSH_OK)
+        return s;
     return record(events, 4, st);
 }
 
