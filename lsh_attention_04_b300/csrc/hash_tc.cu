@@ -348,21 +348,33 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
                 int rr, jj;
                 if (P.split) { rr = k / P.cpr; jj = kChunkMax * (k % P.cpr); }
                 else { const int col = chunk_col0(P, k); rr = col / P.hp; jj = col - rr * P.hp; }
+                // 32-column batches through two register buffers: batch q+1 is loading
+                // while q is scanned (one tcgen05.ld in flight at each wait), and the
+                // accumulator goes back to its MMA warp as soon as its last batch is in
+                // registers.
                 uint32_t va[32], vb[32];
-                for (int c = 0; c < width; c += 64) {
-                    const bool two = c + 32 < width;
-                    LSH_SPAN_BEGIN(t_ld);
-                    tmem_ld32(tlane + c, va);
-                    if (two) tmem_ld32(tlane + c + 32, vb);
-                    tmem_wait_ld(va, vb);
-                    LSH_SPAN_END(t_ld, 0x480);
-                    LSH_SPAN_BEGIN(t_sc);
+                const int nbat = width / 32;
+                tmem_ld32(tlane, va);
+                tmem_wait_ld(va);
+                for (int q = 0; q < nbat; q += 2) {
+                    const bool has_b = q + 1 < nbat, has_a2 = q + 2 < nbat;
+                    if (has_b) tmem_ld32(tlane + 32 * (q + 1), vb);
+                    else {
+                        fence_before_sync();
+                        mbar_arrive(&sb.tm_empty[buf]);
+                    }
                     scan_batch(va, P, rr, jj, cur, best, bidx, live, buckets, tok, r0);
-                    if (two) scan_batch(vb, P, rr, jj, cur, best, bidx, live, buckets, tok, r0);
-                    LSH_SPAN_END(t_sc, 0x481);
+                    if (has_b) {
+                        tmem_wait_ld(vb);
+                        if (has_a2) tmem_ld32(tlane + 32 * (q + 2), va);
+                        else {
+                            fence_before_sync();
+                            mbar_arrive(&sb.tm_empty[buf]);
+                        }
+                        scan_batch(vb, P, rr, jj, cur, best, bidx, live, buckets, tok, r0);
+                        if (has_a2) tmem_wait_ld(va);
+                    }
                 }
-                fence_before_sync();
-                mbar_arrive(&sb.tm_empty[buf]);
             }
         }
     }
