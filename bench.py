@@ -43,8 +43,8 @@ COMPUTE_UNIT = {"bf16": "tensor", "f32": "alu"}
 KERNEL_SOURCES = {
     "hash": ["hash_tc.cu", "sm100.cuh", "tmap.cu"],
     "sort": ["sort.cu"],
-    "attn": ["attn_tc.cu", "sm100.cuh", "tmap.cu"],
-    "combine": ["combine.cu"],
+    "attn": ["attn_tc.cu", "sm100.cuh"],
+    "combine": ["combine.cu", "combine_tma.cu", "sm100.cuh"],
 }
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
