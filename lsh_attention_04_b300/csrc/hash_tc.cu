@@ -50,7 +50,14 @@ constexpr int kRCapBytes = 128 * 1024;
 constexpr int kMaxXStages = 4;         // qk tile stages (as many as shared memory holds)
 constexpr size_t kSmemCap = 227 * 1024;
 constexpr int kMmaWarps = kTmemBufs; // one MMA-issuing warp per accumulator
-constexpr int kThreads = (10 + kMmaWarps) * 32;  // 8 epilogue warps, producer, norm, MMA
+constexpr int kEpiGroups = kTmemBufs; // epilogue warpgroups, one accumulator each
+constexpr int kEpiWarps = 4 * kEpiGroups;
+constexpr int kProdWarp = kEpiWarps;      // producer (also the TMEM owner)
+constexpr int kNormWarp = kEpiWarps + 1;  // 1 / |x|
+constexpr int kMma0 = kEpiWarps + 2;      // MMA issuers kMma0 .. kMma0 + 3
+// 22 working warps, padded to 24: with a multiple of 4 warps every scheduler holds the
+// same number of warps, so the per-thread register cap is 65536 / 768 rounded down.
+constexpr int kThreads = 24 * 32;
 
 struct HashPlan {
     long long n_tok;
@@ -198,13 +205,13 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
         sb.abort_flag = 0;
         mbar_fence_init();
     }
-    if (warp == 8) tmem_alloc(&sb.tmem_base, 512);
+    if (warp == kProdWarp) tmem_alloc(&sb.tmem_base, 512);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = sb.tmem_base;
 
-    if (warp == 8) {
+    if (warp == kProdWarp) {
         // ---------------- producer: R group once, then qk tiles ----------------
         if (lane == 0) {
             prefetch_tmap(&xmap);
@@ -238,16 +245,13 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
             int dummy = 0;
             wait(&sb.r_full, 0, &dummy, status, 0x103);
         }
-    } else if (warp >= 10) {
-        // ---------------- MMA issuers: warp 10+b owns accumulator b ----------------
-        // Each issuer is a whole converged warp (the MMA wrappers elect one lane).  Chains
-        // on separate accumulators issued from separate warps overlap.  Tile `it` belongs
-        // to epilogue warpgroup it & 1, whose chunks alternate between its accumulators
-        // 2(it & 1) and 2(it & 1) + 1.
+    } else if (warp >= kMma0 && warp < kMma0 + kMmaWarps) {
+        // ---------------- MMA issuers: warp kMma0 + b owns accumulator b ----------------
+        // Each issuer is a whole converged warp (the MMA wrappers elect one lane).  Tile
+        // `it` belongs to epilogue warpgroup it % 4 and accumulator it % 4, whose issuer
+        // runs all the tile's chunks through it in order; four tiles are in flight.
         {
-            const int mi = warp - 10;
-            const int me = mi >> 1, mp = mi & 1;
-            const int n_mine = (nch + 1 - mp) / 2;   // chunks of a tile that use this accumulator
+            const int mi = warp - kMma0;
             bool ok = wait_w(&sb.r_full, 0, abort_flag, status, 0x201);
             fence_after_sync();
             int it = 0;
@@ -257,9 +261,9 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
                 if (!(ok = wait_w(&sb.x_full[s], (it / P.x_stages) & 1, abort_flag, status, 0x202))) break;
                 fence_after_sync();
                 bool touched = false;
-                if ((it & 1) == me) {
-                    for (int k = mp; k < nch; k += 2) {
-                        const int use = (it >> 1) * n_mine + (k >> 1);
+                if (it % kEpiGroups == mi) {
+                    for (int k = 0; k < nch; ++k) {
+                        const int use = (it / kEpiGroups) * nch + k;
                         if (!(ok = wait_w(&sb.tm_empty[mi], (use & 1) ^ 1, abort_flag, status, 0x203))) break;
                         fence_after_sync();
                         const int width = chunk_width(P, nr, k);
@@ -286,7 +290,7 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
             int dummy = 0;
             wait_w(&sb.mma_done, 0, &dummy, status, 0x204);
         }
-    } else if (warp == 9) {
+    } else if (warp == kNormWarp) {
         // ---------------- 1/|x| of each token (first group only) ----------------
         if (g == 0) {
             int it = 0;
@@ -319,26 +323,26 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
                 if (lane == 0) mbar_arrive(&sb.x_empty[s]);
             }
         }
-    } else {
-        // ---------------- epilogue warpgroups: warpgroup e takes the tiles it & 1 == e ------
-        // It sees every chunk of its tile, hence every round whole: no merging between
-        // warpgroups.  Its chunks alternate between accumulators 2e and 2e + 1.
+    } else if (warp < kEpiWarps) {
+        // ---------------- epilogue warpgroups: warpgroup e takes the tiles it % 4 == e ------
+        // It sees every chunk of its tile (in its own accumulator e), hence every round
+        // whole: no merging between warpgroups.  Four warpgroups keep four epilogue warps
+        // on every scheduler to hide each other's latencies.
         const int e = warp >> 2, q = warp & 3;
         const int row = q * 32 + lane;
         const uint32_t tlane0 = tmem + ((uint32_t)(q * 32) << 16);
-        const int n0 = (nch + 1) / 2, n1 = nch / 2;   // chunks per tile on each accumulator
         int it = 0;
         bool ok = true;
         for (int t = cj; ok && t < P.n_tiles; t += P.ctas_per_group, ++it) {
-            if ((it & 1) != e) continue;
+            if (it % kEpiGroups != e) continue;
             const long long tok = (long long)t * kTileM + row;
             const bool live = tok < P.n_tok;
             int cur = -1;
             float best = 0.f;
             int bidx = 0;
             for (int k = 0; k < nch; ++k) {
-                const int buf = 2 * e + (k & 1);
-                const int use = (it >> 1) * ((k & 1) ? n1 : n0) + (k >> 1);
+                const int buf = e;
+                const int use = (it / kEpiGroups) * nch + k;
                 const uint32_t tlane = tlane0 + buf * kChunkMax;
                 bool w = wait(&sb.tm_full[buf], use & 1, abort_flag, status, 0x401);
                 if (!(ok = __all_sync(0xffffffffu, w))) break;
@@ -348,32 +352,19 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
                 int rr, jj;
                 if (P.split) { rr = k / P.cpr; jj = kChunkMax * (k % P.cpr); }
                 else { const int col = chunk_col0(P, k); rr = col / P.hp; jj = col - rr * P.hp; }
-                // 32-column batches through two register buffers: batch q+1 is loading
-                // while q is scanned (one tcgen05.ld in flight at each wait), and the
-                // accumulator goes back to its MMA warp as soon as its last batch is in
-                // registers.
-                uint32_t va[32], vb[32];
+                // 32-column batches, one at a time (four epilogue warps per scheduler hide
+                // each other's tcgen05.ld latency); the accumulator goes back to its MMA
+                // warp as soon as its last batch is in registers.
                 const int nbat = width / 32;
-                tmem_ld32(tlane, va);
-                tmem_wait_ld(va);
-                for (int q = 0; q < nbat; q += 2) {
-                    const bool has_b = q + 1 < nbat, has_a2 = q + 2 < nbat;
-                    if (has_b) tmem_ld32(tlane + 32 * (q + 1), vb);
-                    else {
+                for (int q2 = 0; q2 < nbat; ++q2) {
+                    uint32_t va[32];
+                    tmem_ld32(tlane + 32 * q2, va);
+                    tmem_wait_ld(va);
+                    if (q2 == nbat - 1) {
                         fence_before_sync();
                         mbar_arrive(&sb.tm_empty[buf]);
                     }
                     scan_batch(va, P, rr, jj, cur, best, bidx, live, buckets, tok, r0);
-                    if (has_b) {
-                        tmem_wait_ld(vb);
-                        if (has_a2) tmem_ld32(tlane + 32 * (q + 2), va);
-                        else {
-                            fence_before_sync();
-                            mbar_arrive(&sb.tm_empty[buf]);
-                        }
-                        scan_batch(vb, P, rr, jj, cur, best, bidx, live, buckets, tok, r0);
-                        if (has_a2) tmem_wait_ld(va);
-                    }
                 }
             }
         }
@@ -381,7 +372,7 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
 
     fence_before_sync();
     __syncthreads();
-    if (warp == 8) {
+    if (warp == kProdWarp) {
         __syncwarp();
         fence_after_sync();
         tmem_dealloc(tmem, 512);
