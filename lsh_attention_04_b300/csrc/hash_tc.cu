@@ -17,21 +17,21 @@
 //  * Persistent CTAs: ctas_per_group CTAs per group walk the 128-token tiles in the same
 //    order, so the CTAs of all groups read a tile of qk within a short time window and
 //    only the first one fetches it from HBM (the others hit L2).
-//  * Warp roles: warp 8 issues TMA loads of the qk tile (2-D tensor map, 128-byte
-//    swizzle, 2-4 stages); warps 10-13 (one thread each) issue tcgen05.mma M=128 x N=chunk
-//    x K=16 into four 128-column TMEM accumulators, warp 10+b owning accumulator b: one
-//    issuing thread manages about one MMA per few hundred cycles whatever N is, so the
-//    independent chains are issued from separate warps; warps 0-3 and 4-7 (two epilogue
-//    warpgroups, taking even and odd tiles) read the projections with tcgen05.ld and
-//    keep, per token and round, the entry of largest magnitude (first index on ties);
-//    warp 9 computes 1/|x| of each token from the staged tile (first group only).
+//  * Warp roles (24 warps, 64 registers): warp 16 issues TMA loads of the qk tile (2-D
+//    tensor map, 128-byte swizzle, 2-4 stages) and owns TMEM; warps 18-21 issue
+//    tcgen05.mma M=128 x N=chunk x K=16 into four 128-column TMEM accumulators, warp 18+b
+//    owning accumulator b (each a whole warp, one lane elected per instruction); warps
+//    0-15 are four epilogue warpgroups that read the projections with tcgen05.ld and keep,
+//    per token and round, the entry of largest magnitude (first index on ties); warp 17
+//    computes 1/|x| of each token from the staged tile (first group only); warps 22-23
+//    only pad the block to a multiple of 4 warps (equal register caps per scheduler).
 //  * Bucket rule: the largest entry of [p, -p] is the entry of p with the largest |p_j|,
 //    taken with its sign: bucket = j if p_j >= 0, n_buckets/2 + j otherwise.  Scanning j
 //    in order with a strict comparison keeps the first index.  Two entries of equal
 //    magnitude and opposite sign have a zero top-1/top-2 margin, i.e. they are a near-tie.
-//  * Each 128-token tile goes to one epilogue warpgroup (alternating), which reads every
-//    chunk of it and so sees each round whole; its chunks alternate between the
-//    warpgroup's two accumulators, so the MMAs of one run while the other is scanned.
+//  * Tile `it` of a CTA goes to epilogue warpgroup it % 4 and accumulator it % 4: the
+//    group reads every chunk of it (so it sees each round whole) and four tiles are in
+//    flight, their MMAs running while other groups scan.
 // Every wait is bounded (see sm100::wait); on a timeout the kernel records the place in
 // the workspace status block and winds down.
 #include <math.h>
