@@ -162,7 +162,9 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 __device__ __forceinline__ void st_global_v8(void *p, const uint32_t *r) {
-    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+    // streaming store (.cs): the per-round outputs are read back once by the round
+    // combination much later, so they should not evict the gathered Q/K/V rows from L2
+    asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
                  :: "l"(p), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
                     "r"(r[6]), "r"(r[7]) : "memory");
 }
@@ -542,8 +544,8 @@ lsh_attn_tc_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *__
                 }
             }
             if (e_live && half == 0)
-                lse_r[LSH_IDX(e_row, (long long)n_rows, 0x713)] =
-                    e_self ? kSelfLogit : (e_m2 + __log2f(l)) * kLn2;
+                __stcs(&lse_r[LSH_IDX(e_row, (long long)n_rows, 0x713)],
+                       e_self ? kSelfLogit : (e_m2 + __log2f(l)) * kLn2);
             LSH_SPAN_END(t_ep, 0x783);
             fence_before_sync();
             mbar_arrive(&sb.o_empty);
