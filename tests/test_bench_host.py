@@ -1,0 +1,70 @@
+"""Host-side logic of the benchmark and the binding, on CPU.
+
+* the algorithmic work model (FLOPs and bytes per stage) gives the path totals the
+  hot-path scope fixes for the long-text workload, and the roofline is the slower of
+  FLOPs at the bf16 peak and bytes at HBM bandwidth;
+* a DRAM-traffic figure recorded from ncu is used only while the kernel's sources are
+  unchanged;
+* the whole-job value counts every rank's tokens over the slowest rank's time;
+* the binding refuses to run without the native library (no fallback).
+"""
+import json
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from lsh_attention_04_b300 import inputs as gen  # noqa: E402
+
+
+def test_work_model_long_text_totals():
+    w = gen.WORKLOADS["long_B1_H8_L65536_d128_R8"]
+    k = bench.work(w)
+    N, R, d, nb, c = w.tokens, w.n_rounds, w.d, w.n_buckets, w.chunk
+    # hash: N*R*(nb/2) dot products of length d; attention: QK^T and PV over c x 2c
+    assert k["hash"]["flops"] == N * R * d * nb == 549_755_813_888
+    assert k["attn"]["flops"] == 8 * N * R * c * d == 274_877_906_944
+    total_f = sum(v["flops"] for v in k.values())
+    assert total_f == 824_633_720_832                      # 825 GFLOP at this size
+    total_b = sum(v["bytes"] for v in k.values())
+    assert 2.9e9 < total_b < 3.0e9                         # ~2.95 GB: the o_r round trip dominates
+    # roofline: slower of the two, with the measured peaks
+    peaks, _ = bench.load_peaks()
+    t_f = total_f / (peaks["bf16_tflops"] * 1e12)
+    t_b = total_b / (peaks["hbm_gbs"] * 1e9)
+    assert t_f > 0 and t_b > 0
+
+
+def test_recorded_traffic_needs_unchanged_sources(tmp_path, monkeypatch):
+    rec = {"wl": {"attn": {"bytes_per_launch": 123, "source_sha1": bench.source_digest("attn")}}}
+    f = tmp_path / "traffic.json"
+    f.write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    assert bench.recorded_traffic("wl", "attn") == 123
+    assert bench.recorded_traffic("wl", "hash") is None            # no record
+    assert bench.recorded_traffic("other", "attn") is None
+    monkeypatch.setattr(bench, "source_digest", lambda stage: "0" * 40)
+    assert bench.recorded_traffic("wl", "attn") is None            # sources changed
+
+
+def test_kernel_sources_exist():
+    for stage, files in bench.KERNEL_SOURCES.items():
+        for f in files:
+            assert os.path.exists(os.path.join(ROOT, "lsh_attention_04_b300", "csrc", f)), (stage, f)
+
+
+def test_job_value_counts_all_ranks():
+    assert bench.job_value(1000, 1, 2.0) == pytest.approx(500_000)
+    assert bench.job_value(1000, 4, 2.0) == pytest.approx(2_000_000)
+
+
+def test_binding_refuses_without_library(monkeypatch, tmp_path):
+    import lsh_attention_04_b300 as lsh
+    monkeypatch.setattr(lsh, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(lsh, "_lib", None, raising=False)
+    with pytest.raises(OSError):
+        lsh.load()
