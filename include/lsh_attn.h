@@ -185,6 +185,11 @@ lsh_status_t lsh_bucket_sort_noalloc(const int32_t *buckets, int B, int H, int L
  * same-bucket, self and causal masks).  Sorted row s sees the sorted rows
  * [(s/chunk - 1)*chunk, (s/chunk + 1)*chunk) clipped to [0, L); chunk 0 has no
  * previous chunk.  Writes o_r and lse_r in sorted order (layouts above).
+ * buckets, perm and bstart must come from one sort of the same buckets (as
+ * lsh_bucket_sort writes them).  The bf16 tensor-core path finds each row's bucket run
+ * from the sorted rows' buckets, and the other paths read bstart, so inconsistent
+ * arrays give path-dependent results.  Permutation entries outside [0, L) are
+ * replaced by 0 (no out-of-range reads) and then the results are meaningless.
  */
 size_t lsh_chunk_attn_workspace_bytes(void);
 lsh_status_t lsh_chunk_attn(const void *qk, const void *v, lsh_dtype_t dtype,
