@@ -158,11 +158,13 @@ class ClockSampler:
 # ------------------------------------------------------------------ CPU oracle
 
 
-def oracle_sample(w):
+def oracle_sample(w, max_tokens=32768):
     """A bounded sample of workload w for the fp64 oracle: head 0, the first
-    min(L, 32768) tokens, all rounds, the workload's bucket count and chunk."""
+    min(L, max_tokens) tokens (a multiple of two chunks), all rounds, the workload's
+    bucket count and chunk.  The oracle's work per token does not depend on L (fixed
+    chunk and bucket count), so its tokens/s carries over to the whole workload."""
     from lsh_attention_04_b300 import inputs as gen
-    Ls = min(w.L, 32768)
+    Ls = min(w.L, max(2 * w.chunk, (max_tokens // (2 * w.chunk)) * (2 * w.chunk)))
     sub = w.replace(B=1, H=1, L=Ls)
     qk, v, R = gen.make_inputs(sub, seed=w.seed)
     desc = (f"head 0 of {w.name}: first {Ls} tokens, {w.n_rounds} rounds, "
@@ -170,9 +172,9 @@ def oracle_sample(w):
     return sub, qk, v, R, desc
 
 
-def time_oracle(w, threads, steps=1):
+def time_oracle(w, threads, steps=1, max_tokens=32768):
     import oracle
-    sub, qk, v, R, desc = oracle_sample(w)
+    sub, qk, v, R, desc = oracle_sample(w, max_tokens)
     oracle.build()
     times = []
     for _ in range(steps):
@@ -223,7 +225,11 @@ def run_reference(args, w):
     if int(os.environ.get("RANK", "0")) != 0:
         return 0
     threads = os.cpu_count() or 1
-    tokens, times, used, desc = time_oracle(w, threads, steps=args.warmup + args.steps)
+    # Bound the whole run to a couple of minutes: one 32K-token sample takes a few
+    # seconds, so many requested steps get proportionally smaller samples.
+    n = args.warmup + args.steps
+    max_tokens = 32768 if n <= 40 else max(2 * w.chunk, 32768 * 40 // n)
+    tokens, times, used, desc = time_oracle(w, threads, steps=n, max_tokens=max_tokens)
     timed = times[args.warmup:]
     t = sum(timed) / len(timed)
     value = tokens / t
