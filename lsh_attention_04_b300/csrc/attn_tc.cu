@@ -24,10 +24,10 @@
 // The S chain and the P V chain are issued from two different warps and overlap.
 // Masks: sorted order keeps each bucket in one run, so the keys of sorted row s form one
 // interval of window columns: [max(window start, bucket start), causal ? s : min(window
-// end, bucket end)), minus s itself when not causal.  A loader marks where runs start
-// and end inside its chunk (warp ballots over neighbouring rows' buckets); a softmax
-// lane turns the marks of its chunk and the previous one into its interval, so neither
-// needs the bucket-start table or a per-key bucket test.  A row with no key but itself
+// end, bucket end)), minus s itself when not causal.  The metadata warp marks where runs
+// start and end inside each chunk (warp ballots over neighbouring rows' buckets); a
+// softmax lane turns the marks of its chunk and the previous one into its interval, so
+// neither needs the bucket-start table or a per-key bucket test.  A row with no key but itself
 // gives its own column weight 1, so P V returns v_i exactly; its lse is the self logit
 // -1e5.
 // Softmax without a running maximum: with unit keys every score of query i is bounded
