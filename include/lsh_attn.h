@@ -209,6 +209,18 @@ lsh_status_t lsh_unsort_combine(const void *o_r, const float *lse_r, const int32
                                 float *out, float *lse, void *stream);
 
 /*
+ * Self test of the bounded waits the tensor-core kernels use (the pages have no
+ * counterpart: it exists to test this library's failure reporting).  Clears the status
+ * block at the start of `workspace` (>= 256 bytes, 256-byte aligned, device memory) and
+ * launches one warp that waits on an mbarrier nothing ever arrives on.  After the wait
+ * limit (1 s) the wait gives up, records detail 0xF01 in the status block and the
+ * kernel returns: nothing traps or hangs, and the context stays usable.  A following
+ * lsh_workspace_status() on the same stream then returns LSH_ERR_DEVICE_CHECK with
+ * detail 0xF01.  Returns launch errors only, like every entry point.
+ */
+lsh_status_t lsh_selftest_wait_timeout(void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Waits for `stream`, then reads the status block at the start of `workspace`:
  * LSH_OK, or LSH_ERR_DEVICE_CHECK when a kernel gave up a bounded wait since the
  * block was last cleared (each entry point that takes a workspace clears it).

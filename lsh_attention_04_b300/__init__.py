@@ -32,7 +32,7 @@ EXPORTS = (
     "lsh_attn_workspace_layout", "lsh_hash_workspace_bytes", "lsh_hash",
     "lsh_bucket_sort_workspace_bytes", "lsh_bucket_sort", "lsh_chunk_attn_workspace_bytes",
     "lsh_chunk_attn", "lsh_unsort_combine", "lsh_workspace_status", "lsh_attn_forward_timed",
-    "lsh_attn_kernel_launches", "lsh_bucket_sort_noalloc",
+    "lsh_attn_kernel_launches", "lsh_bucket_sort_noalloc", "lsh_selftest_wait_timeout",
 )
 
 _lib = None
@@ -81,6 +81,8 @@ def load():
     lib.lsh_unsort_combine.restype = I
     lib.lsh_workspace_status.argtypes = [P, ctypes.POINTER(I), P]
     lib.lsh_workspace_status.restype = I
+    lib.lsh_selftest_wait_timeout.argtypes = [P, S, P]
+    lib.lsh_selftest_wait_timeout.restype = I
     _lib = lib
     return lib
 
@@ -270,6 +272,16 @@ def lsh_unsort_combine(o_r, lse_r, inv, out=None, lse=None, stream=None):
                                      n_rounds, _ptr(out), _ptr(lse), _stream(stream)),
            "lsh_unsort_combine")
     return out, lse
+
+
+SELFTEST_WAIT_CODE = 0xF01
+
+
+def lsh_selftest_wait_timeout(ws, stream=None):
+    """Launch the bounded-wait self test into the status block of `ws` (a CUDA uint8
+    tensor of >= 256 bytes); lsh_workspace_status(ws) then reports the timeout."""
+    _check(load().lsh_selftest_wait_timeout(_ptr(ws), ws.numel() * ws.element_size(),
+                                            _stream(stream)), "lsh_selftest_wait_timeout")
 
 
 def lsh_workspace_status(ws, stream=None):

@@ -23,6 +23,9 @@ struct StatusBlock {
 };
 static_assert(sizeof(StatusBlock) == 256, "status block is 256 bytes");
 
+// status-block detail written by the bounded-wait self test
+constexpr int kSelftestWaitCode = 0xF01;
+
 constexpr size_t kAlign = 1024;
 inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
 
@@ -84,6 +87,8 @@ bool attn_tc_supported(const Problem &p);
 cudaError_t attn_tc(const Problem &p, const void *qk, const void *v, const int32_t *buckets,
                     const int32_t *perm, const int32_t *bstart, const float *inv_norm, void *o_r,
                     float *lse_r, StatusBlock *status, cudaStream_t st);
+
+cudaError_t selftest_wait_launch(StatusBlock *status, cudaStream_t st);
 
 cudaError_t combine_launch(const Problem &p, const void *o_r, const float *lse_r,
                            const int32_t *inv, float *out, float *lse, cudaStream_t st,

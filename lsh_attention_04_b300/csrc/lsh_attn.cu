@@ -309,6 +309,16 @@ lsh_status_t lsh_unsort_combine(const void *o_r, const float *lse_r, const int32
     return cuda_status(combine_launch(p, o_r, lse_r, inv, out, lse, (cudaStream_t)stream));
 }
 
+lsh_status_t lsh_selftest_wait_timeout(void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (!workspace || workspace_bytes < sizeof(StatusBlock)) return LSH_ERR_INVALID_ARGUMENT;
+    if (((uintptr_t)workspace) % 256 != 0) return LSH_ERR_INVALID_ARGUMENT;
+    cudaStream_t st = (cudaStream_t)stream;
+    lsh_status_t s = clear_status(workspace, st);
+    if (s != LSH_OK) return s;
+    return cuda_status(selftest_wait_launch((StatusBlock *)workspace, st));
+}
+
 lsh_status_t lsh_workspace_status(const void *workspace, int *detail, void *stream)
 {
     if (!workspace) return LSH_ERR_INVALID_ARGUMENT;
