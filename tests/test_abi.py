@@ -155,3 +155,7 @@ def test_stage_validation(lib):
                               1, 32, 1, ctypes.c_float(1.0), P(1), P(1), P(256), 1 << 20,
                               None) == lsh.LSH_ERR_INVALID_ARGUMENT   # L % chunk
     assert lib.lsh_workspace_status(None, None, None) == lsh.LSH_ERR_INVALID_ARGUMENT
+    # bounded-wait self test: needs a 256-byte aligned status block
+    assert lib.lsh_selftest_wait_timeout(None, 256, None) == lsh.LSH_ERR_INVALID_ARGUMENT
+    assert lib.lsh_selftest_wait_timeout(P(256), 128, None) == lsh.LSH_ERR_INVALID_ARGUMENT
+    assert lib.lsh_selftest_wait_timeout(P(260), 256, None) == lsh.LSH_ERR_INVALID_ARGUMENT
