@@ -36,11 +36,13 @@
  *  - the sort key is (bucket, original position), ascending;
  *  - rounds are combined with weights exp(lse_r - logsumexp_r lse_r).
  *
- * Parity unpinned: the pages fix none of three choices the tests therefore cannot pin
- * to anything but this restatement.  These are the value of `scale` (the pages disagree
- * on the 1/sqrt(d) factor), the self logit -1e5, and the logsumexp weighting of the
- * rounds.  Everything else in this file is pinned by the tests (closed forms, the
- * pages' worked hashing statistic, brute force on tiny inputs, planted mistakes).
+ * Parity unpinned: the pages fix neither the value of `scale` (they disagree on the
+ * 1/sqrt(d) factor) nor the self logit -1e5, so the tests cannot pin those to anything
+ * but this restatement.  The logsumexp weighting of the rounds is a reading as well (the
+ * pages only say the hashing is repeated), but its arithmetic is pinned: it must equal
+ * one softmax over the multiset union of the rounds' candidate sets.  Everything else in
+ * this file is pinned by the tests (closed forms, the pages' worked hashing statistic,
+ * brute force on tiny inputs, library SDPA, planted mistakes).
  *
  * Layouts (row-major, all fp64 unless stated):
  *  x/qk, v      [L][d]          (one head)

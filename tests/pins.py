@@ -376,4 +376,38 @@ def pin_combine_self_only_round_has_no_weight(orc):
     assert np.allclose(both[0, lonely], first[0, lonely], rtol=0, atol=1e-12)
 
 
+def pin_combine_is_softmax_over_the_rounds_multiset(orc):
+    """Weighting each round by its share of the softmax mass, with no correction for keys
+    found in several rounds, is one softmax over the multiset union of the rounds'
+    candidate sets: key j carries weight count_ij * exp(s_ij), count_ij = the number of
+    rounds in which j is a candidate of i.  Checked against library SDPA with the additive
+    mask ln(count_ij), candidate sets enumerated by brute force from the oracle's buckets;
+    the rows must include keys counted once and keys counted several times."""
+    rng = _rng(16)
+    L, d, nb, c, n_rounds, scale = 48, 8, 6, 8, 3, 0.6
+    qk = rng.standard_normal((L, d))
+    v = rng.standard_normal((L, d))
+    R = rng.standard_normal((n_rounds, d, nb // 2))
+    for causal in (False, True):
+        out, lse, it = orc.forward(qk[None], v[None], R, nb, c, causal, scale,
+                                   intermediates=True)
+        count = np.zeros((L, L))
+        for r in range(n_rounds):
+            bucket = it["bucket"][0, r]
+            for i in range(L):
+                count[i, _brute_candidates(bucket, i, c, causal)] += 1
+        rows = count.sum(1) > 0
+        assert (count == 1).any() and (count >= 2).any() and rows.sum() >= L - 2
+        logc = np.where(count > 0, np.log(np.maximum(count, 1)), -np.inf)
+        logc[~rows, np.arange(L)[~rows]] = 0.0        # rows with no candidate: not compared
+        q = torch.from_numpy(qk)
+        k = q / q.norm(dim=-1, keepdim=True)
+        mask = torch.from_numpy(logc)
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            q[None], k[None], torch.from_numpy(v)[None], attn_mask=mask[None], scale=scale)[0]
+        ref_lse = torch.logsumexp((q @ k.T) * scale + mask, dim=-1)
+        assert np.allclose(out[0][rows], ref.numpy()[rows], rtol=1e-10, atol=1e-10)
+        assert np.allclose(lse[0][rows], ref_lse.numpy()[rows], rtol=1e-10, atol=1e-10)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

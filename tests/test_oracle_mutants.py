@@ -33,6 +33,10 @@ MUTANTS = [
     ("attend_lse_unshifted", "lse_sorted[s] = mx + log(sum);", "lse_sorted[s] = log(sum);"),
     ("attend_self_logit_zero", "#define ORACLE_SELF_LOGIT (-1.0e5)", "#define ORACLE_SELF_LOGIT (0.0)"),
     ("combine_uniform_weights", "double w = exp(l[r] - LSE);", "double w = 1.0 / n_rounds;"),
+    ("combine_lse_is_round_max", "double LSE = mx + log(sum);", "double LSE = mx;"),
+    ("combine_rows_of_round0",
+     "int s = inv[(size_t)r * L + i];\n            double w",
+     "int s = inv[i];\n            double w"),
     ("combine_not_unsorted",
      "int s = inv[(size_t)r * L + i];\n            double w",
      "int s = i;\n            double w"),
