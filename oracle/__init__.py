@@ -17,6 +17,9 @@ Each function follows the Reformer pages:
                 when nothing else is left (modulabs-hub notes, "LSH attention")
   * combine  -- un-sort and logsumexp-weighted sum of rounds
   * forward  -- all of the above for B*H heads
+  * backward -- gradients of the forward in qk and v by the chain rule, buckets
+                held fixed (the pages train by back-propagation but print no
+                gradient formula; modulabs-hub notes, "Introduction")
 """
 from __future__ import annotations
 
@@ -85,6 +88,16 @@ class Oracle:
         lib.oracle_forward.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, i32,
                                        f64, i32] + [P] * 9
         lib.oracle_forward.restype = ctypes.c_int
+        lib.oracle_combine_backward.argtypes = [P, P, P, i32, i32, i32, P, P, P, P, P, P]
+        lib.oracle_combine_backward.restype = None
+        lib.oracle_attend_backward.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64,
+                                               P, P, P, P, P, P, P]
+        lib.oracle_attend_backward.restype = None
+        lib.oracle_key_norm_backward.argtypes = [P, P, P, i32, i32, P]
+        lib.oracle_key_norm_backward.restype = None
+        lib.oracle_backward.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, i32, f64,
+                                        P, P, P, P]
+        lib.oracle_backward.restype = ctypes.c_int
         lib.oracle_self_logit.argtypes = []
         lib.oracle_self_logit.restype = f64
         self.lib = lib
@@ -222,6 +235,60 @@ class Oracle:
             return out, lse, inter
         return out, lse
 
+    def backward(self, qk, v, R, n_buckets, chunk, causal, scale, g_out, g_lse):
+        """Gradients of  sum(g_out * out) + sum(g_lse * lse)  in qk and v, with the
+        buckets held fixed.  Shapes as in ``forward``; returns (dqk, dv)."""
+        lib = self.lib
+        shape = qk.shape
+        L, d = shape[-2], shape[-1]
+        n_heads = int(np.prod(shape[:-2]))
+        qk = _f64(qk).reshape(n_heads, L, d)
+        v = _f64(v).reshape(n_heads, L, d)
+        g_out = _f64(g_out).reshape(n_heads, L, d)
+        g_lse = _f64(g_lse).reshape(n_heads, L)
+        R = _f64(R)
+        n_rounds = R.shape[0]
+        assert R.shape == (n_rounds, d, n_buckets // 2)
+        dqk = np.empty((n_heads, L, d), np.float64)
+        dv = np.empty((n_heads, L, d), np.float64)
+        rc = lib.oracle_backward(_p(qk), _p(v), _p(R), n_heads, L, d, n_buckets, n_rounds,
+                                 chunk, int(causal), float(scale), _p(g_out), _p(g_lse),
+                                 _p(dqk), _p(dv))
+        if rc != 0:
+            raise MemoryError("oracle_backward ran out of host memory")
+        return dqk.reshape(shape), dv.reshape(shape)
+
+    def combine_backward(self, o_r, lse_r, inv, out, lse, g_out, g_lse):
+        """Backward of the round combination of one head: (g_o [R, L, d], g_lse_r [R, L])
+        in sorted order, from the forward's sorted o_r/lse_r and token-order out/lse."""
+        o_r = _f64(o_r)
+        lse_r = _f64(lse_r)
+        inv = _i32(inv)
+        out, lse, g_out, g_lse = _f64(out), _f64(lse), _f64(g_out), _f64(g_lse)
+        R, L, d = o_r.shape
+        g_o = np.zeros((R, L, d), np.float64)
+        g_lse_r = np.zeros((R, L), np.float64)
+        self.lib.oracle_combine_backward(_p(o_r), _p(lse_r), _p(inv), R, L, d, _p(out), _p(lse),
+                                         _p(g_out), _p(g_lse), _p(g_o), _p(g_lse_r))
+        return g_o, g_lse_r
+
+    def attend_backward(self, qk, v, bucket, perm, chunk, causal, scale, o, lse, g_o, g_lse):
+        """Backward of one round's attention of one head (all arrays of the round in sorted
+        order).  Returns (dq, dkhat, dv): the gradients through qk as query, through the
+        normalised key, and in v."""
+        qk, v = _f64(qk), _f64(v)
+        bucket, perm = _i32(bucket), _i32(perm)
+        o, lse, g_o, g_lse = _f64(o), _f64(lse), _f64(g_o), _f64(g_lse)
+        L, d = qk.shape
+        inorm = self.inv_norm(qk)
+        dq = np.zeros((L, d), np.float64)
+        dkhat = np.zeros((L, d), np.float64)
+        dv = np.zeros((L, d), np.float64)
+        self.lib.oracle_attend_backward(_p(qk), _p(v), _p(inorm), _p(bucket), _p(perm), L, d,
+                                        chunk, int(causal), float(scale), _p(o), _p(lse),
+                                        _p(g_o), _p(g_lse), _p(dq), _p(dkhat), _p(dv))
+        return dq, dkhat, dv
+
 
 def default() -> Oracle:
     """The oracle compiled from lsh_oracle.c (built on first use)."""
@@ -258,3 +325,7 @@ def combine(o_r, lse_r, inv, tokens=None):
 
 def forward(qk, v, R, n_buckets, chunk, causal, scale, threads=None, intermediates=False):
     return default().forward(qk, v, R, n_buckets, chunk, causal, scale, threads, intermediates)
+
+
+def backward(qk, v, R, n_buckets, chunk, causal, scale, g_out, g_lse):
+    return default().backward(qk, v, R, n_buckets, chunk, causal, scale, g_out, g_lse)

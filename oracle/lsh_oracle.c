@@ -34,7 +34,10 @@
  *  - causal means strictly earlier original position;
  *  - argmax ties go to the first index of the concatenated [p, -p] vector;
  *  - the sort key is (bucket, original position), ascending;
- *  - rounds are combined with weights exp(lse_r - logsumexp_r lse_r).
+ *  - rounds are combined with weights exp(lse_r - logsumexp_r lse_r);
+ *  - backward: the gradient of the forward with the buckets held fixed (the
+ *    hash is piecewise constant); a self-only row's logit is a constant, and
+ *    a zero key (inverse norm 0) receives no gradient through its key role.
  *
  * Parity unpinned: the pages fix neither the value of `scale` (they disagree on the
  * 1/sqrt(d) factor) nor the self logit -1e5, so the tests cannot pin those to anything
@@ -52,6 +55,7 @@
  *  bstart       int32 [n_rounds][nb+1] first sorted index of each bucket
  *  o_r          [n_rounds][L][d] in SORTED order;  lse_r [n_rounds][L] sorted
  *  out          [L][d];  lse [L]       in original order
+ *  g_out, g_lse  like out, lse;  dqk, dv like qk, v  (backward)
  */
 #include <math.h>
 #include <pthread.h>
@@ -138,12 +142,36 @@ void oracle_inv_norm(const double *qk, int L, int d, double *inv_norm)
 }
 
 /* ------------------------------------------------------------------------ */
+/* The candidate set of sorted row s of one round, built straight from the   */
+/* definition: every sorted position t of the own chunk or the previous      */
+/* chunk ([U], [Z]), t != s, whose token has the query's bucket ([M]), and,  */
+/* if causal, an earlier original position ([M]).  Writes the candidates'    */
+/* original positions to cand (room for 2*chunk) and returns their number.   */
+/* ------------------------------------------------------------------------ */
+static int oracle_candidates(const int32_t *bucket, const int32_t *perm, int L,
+                             int chunk, int causal, int s, int32_t *cand)
+{
+    int i = perm[s];
+    int k = s / chunk;
+    int lo = (k - 1) * chunk;
+    if (lo < 0) lo = 0;
+    int hi = (k + 1) * chunk;
+    if (hi > L) hi = L;
+    int n = 0;
+    for (int t = lo; t < hi; ++t) {
+        int j = perm[t];
+        if (t == s) continue;
+        if (bucket[j] != bucket[i]) continue;
+        if (causal && !(j < i)) continue;
+        cand[n++] = j;
+    }
+    return n;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Steps 3-4: chunked attention of one round, for the sorted rows listed in  */
-/* `rows` (all rows when rows == NULL).  The candidate set of sorted row s   */
-/* is built straight from the definition: every sorted position t of the     */
-/* own chunk or the previous chunk ([U], [Z]), t != s, whose token has the   */
-/* query's bucket ([M]), and, if causal, an earlier original position ([M]). */
-/* The self row is used only when that set is empty.                        */
+/* `rows` (all rows when rows == NULL).  The self row is used only when the  */
+/* candidate set is empty.                                                  */
 /* ------------------------------------------------------------------------ */
 void oracle_attend(const double *qk, const double *v, const double *inv_norm,
                    const int32_t *bucket, const int32_t *perm, int L, int d,
@@ -156,19 +184,7 @@ void oracle_attend(const double *qk, const double *v, const double *inv_norm,
     for (int q = 0; q < count; ++q) {
         int s = rows ? rows[q] : q;
         int i = perm[s];
-        int k = s / chunk;
-        int lo = (k - 1) * chunk;
-        if (lo < 0) lo = 0;
-        int hi = (k + 1) * chunk;
-        if (hi > L) hi = L;
-        int n = 0;
-        for (int t = lo; t < hi; ++t) {
-            int j = perm[t];
-            if (t == s) continue;
-            if (bucket[j] != bucket[i]) continue;
-            if (causal && !(j < i)) continue;
-            cand[n++] = j;
-        }
+        int n = oracle_candidates(bucket, perm, L, chunk, causal, s, cand);
         double *o = o_sorted + (size_t)s * d;
         if (n == 0) {
             for (int c = 0; c < d; ++c) o[c] = v[(size_t)i * d + c];
@@ -229,6 +245,113 @@ void oracle_combine(const double *o_r, const double *lse_r, const int32_t *inv,
         lse[q] = LSE;
     }
     free(l);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Backward pass.  The pages train the model by back-propagation ([M]        */
+/* "Introduction": without reversible layers every layer's activations are   */
+/* kept for it; [U] on how reversible layers recompute them) but state no    */
+/* formula for the attention's gradient.  These functions take the           */
+/* derivative of steps 3-6 by the chain rule, in reverse step order, for the */
+/* loss  sum_i g_out_i . out_i + sum_i g_lse_i lse_i.  The buckets, and so   */
+/* perm and inv, are held fixed: the hash is piecewise constant and is not   */
+/* differentiated.  Every gradient is ADDED into the caller's arrays.        */
+/* ------------------------------------------------------------------------ */
+
+/* Backward of steps 5-6 for one head.  With w_r = exp(lse_r(i) - LSE_i):
+ *   d o_r(i)   = w_r g_out_i
+ *   d lse_r(i) = w_r (g_out_i . (o_r(i) - out_i) + g_lse_i)
+ * (out_i = sum_r w_r o_r(i) and LSE_i = log sum_r exp lse_r(i) differentiated
+ * in lse_r(i)).  Inputs o_r, lse_r in sorted order as the forward leaves them;
+ * out, lse, g_out, g_lse in original order; g_o, g_lse_r written in sorted
+ * order, [n_rounds][L][d] and [n_rounds][L]. */
+void oracle_combine_backward(const double *o_r, const double *lse_r, const int32_t *inv,
+                             int n_rounds, int L, int d, const double *out,
+                             const double *lse, const double *g_out, const double *g_lse,
+                             double *g_o, double *g_lse_r)
+{
+    for (int i = 0; i < L; ++i) {
+        const double *oi = out + (size_t)i * d;
+        const double *gi = g_out + (size_t)i * d;
+        for (int r = 0; r < n_rounds; ++r) {
+            int s = inv[(size_t)r * L + i];
+            const double *src = o_r + ((size_t)r * L + s) * d;
+            double w = exp(lse_r[(size_t)r * L + s] - lse[i]);
+            double *go = g_o + ((size_t)r * L + s) * d;
+            double dot = 0.0;
+            for (int c = 0; c < d; ++c) {
+                go[c] += w * gi[c];
+                dot += gi[c] * (src[c] - oi[c]);
+            }
+            g_lse_r[(size_t)r * L + s] += w * (dot + g_lse[i]);
+        }
+    }
+}
+
+/* Backward of steps 3-4 for one round of one head.  Sorted row s (token i)
+ * with candidates j and weights p_j = exp(s_ij - lse_s), s_ij =
+ * scale * (qk_i . khat_j), khat_j = qk_j * inv_norm_j:
+ *   d v_j      += p_j g_o_s
+ *   d s_ij      = p_j (g_o_s . (v_j - o_s) + g_lse_s)
+ *   d q_i      += d s_ij * scale * khat_j
+ *   d khat_j   += d s_ij * scale * qk_i
+ * A row with no candidate copies v_i (d v_i += g_o_s); its logit is a
+ * constant.  dq is the gradient through the query role of qk, dkhat through
+ * the normalised key; oracle_key_norm_backward folds dkhat into qk. */
+void oracle_attend_backward(const double *qk, const double *v, const double *inv_norm,
+                            const int32_t *bucket, const int32_t *perm, int L, int d,
+                            int chunk, int causal, double scale, const double *o_sorted,
+                            const double *lse_sorted, const double *g_o,
+                            const double *g_lse_sorted, double *dq, double *dkhat,
+                            double *dv)
+{
+    int32_t *cand = (int32_t *)malloc(sizeof(int32_t) * (size_t)(2 * chunk));
+    for (int s = 0; s < L; ++s) {
+        int i = perm[s];
+        int n = oracle_candidates(bucket, perm, L, chunk, causal, s, cand);
+        const double *gs = g_o + (size_t)s * d;
+        const double *os = o_sorted + (size_t)s * d;
+        if (n == 0) {
+            for (int c = 0; c < d; ++c) dv[(size_t)i * d + c] += gs[c];
+            continue;
+        }
+        const double *qi = qk + (size_t)i * d;
+        for (int a = 0; a < n; ++a) {
+            int j = cand[a];
+            const double *kj = qk + (size_t)j * d;
+            const double *vj = v + (size_t)j * d;
+            double dot = 0.0;
+            for (int c = 0; c < d; ++c) dot += qi[c] * kj[c];
+            double p = exp(scale * dot * inv_norm[j] - lse_sorted[s]);
+            double gv = 0.0;
+            for (int c = 0; c < d; ++c) {
+                dv[(size_t)j * d + c] += p * gs[c];
+                gv += gs[c] * (vj[c] - os[c]);
+            }
+            double ds = p * (gv + g_lse_sorted[s]);
+            for (int c = 0; c < d; ++c) {
+                dq[(size_t)i * d + c] += ds * scale * kj[c] * inv_norm[j];
+                dkhat[(size_t)j * d + c] += ds * scale * qi[c];
+            }
+        }
+    }
+    free(cand);
+}
+
+/* d qk_j += inv_norm_j (dkhat_j - khat_j (khat_j . dkhat_j)): the Jacobian of
+ * x -> x / |x| at qk_j.  A zero key has inverse norm 0 and a constant score 0
+ * (the reading the forward takes), so it receives nothing here. */
+void oracle_key_norm_backward(const double *qk, const double *inv_norm, const double *dkhat,
+                              int L, int d, double *dqk)
+{
+    for (int j = 0; j < L; ++j) {
+        const double *x = qk + (size_t)j * d;
+        const double *g = dkhat + (size_t)j * d;
+        double proj = 0.0;
+        for (int c = 0; c < d; ++c) proj += x[c] * inv_norm[j] * g[c];
+        for (int c = 0; c < d; ++c)
+            dqk[(size_t)j * d + c] += inv_norm[j] * (g[c] - x[c] * inv_norm[j] * proj);
+    }
 }
 
 /* ------------------------------------------------------------------------ */
@@ -362,5 +485,63 @@ done:
     if (!lse_r_o) free(lse_r);
     free(inv_norm);
     free(jobs);
+    return rc;
+}
+
+/*
+ * Backward pass over n_heads independent heads: recompute the forward of each
+ * head (buckets, perm, inv, per-round o_r/lse_r, out, lse), then run the
+ * backward steps above in reverse order: combination, every round's
+ * attention, key normalisation.  g_out [n_heads][L][d] and g_lse
+ * [n_heads][L] are the loss's gradients in out and lse; dqk and dv
+ * [n_heads][L][d] are overwritten.  Returns 0, or -1 when memory runs out.
+ */
+int oracle_backward(const double *qk, const double *v, const double *R, int n_heads,
+                    int L, int d, int nb, int n_rounds, int chunk, int causal,
+                    double scale, const double *g_out, const double *g_lse,
+                    double *dqk, double *dv)
+{
+    size_t Ld = (size_t)L * d, RL = (size_t)n_rounds * L;
+    int32_t *bucket = (int32_t *)malloc(sizeof(int32_t) * RL);
+    int32_t *perm = (int32_t *)malloc(sizeof(int32_t) * RL);
+    int32_t *inv = (int32_t *)malloc(sizeof(int32_t) * RL);
+    int32_t *bstart = (int32_t *)malloc(sizeof(int32_t) * (size_t)n_rounds * (nb + 1));
+    double *o_r = (double *)malloc(sizeof(double) * RL * d);
+    double *lse_r = (double *)malloc(sizeof(double) * RL);
+    double *g_o = (double *)malloc(sizeof(double) * RL * d);
+    double *g_lse_r = (double *)malloc(sizeof(double) * RL);
+    double *out = (double *)malloc(sizeof(double) * Ld);
+    double *lse = (double *)malloc(sizeof(double) * L);
+    double *inv_norm = (double *)malloc(sizeof(double) * L);
+    double *dkhat = (double *)malloc(sizeof(double) * Ld);
+    int rc = 0;
+    if (!bucket || !perm || !inv || !bstart || !o_r || !lse_r || !g_o || !g_lse_r || !out ||
+        !lse || !inv_norm || !dkhat) {
+        rc = -1;
+        goto done;
+    }
+    for (int h = 0; h < n_heads; ++h) {
+        const double *qh = qk + h * Ld, *vh = v + h * Ld;
+        double *dq = dqk + h * Ld, *dvh = dv + h * Ld;
+        rc = oracle_forward(qh, vh, R, 1, L, d, nb, n_rounds, chunk, causal, scale, 1, out,
+                            lse, bucket, perm, inv, bstart, NULL, o_r, lse_r);
+        if (rc != 0) goto done;
+        oracle_inv_norm(qh, L, d, inv_norm);
+        memset(g_o, 0, sizeof(double) * RL * d);
+        memset(g_lse_r, 0, sizeof(double) * RL);
+        memset(dkhat, 0, sizeof(double) * Ld);
+        memset(dq, 0, sizeof(double) * Ld);
+        memset(dvh, 0, sizeof(double) * Ld);
+        oracle_combine_backward(o_r, lse_r, inv, n_rounds, L, d, out, lse, g_out + h * Ld,
+                                g_lse + (size_t)h * L, g_o, g_lse_r);
+        for (int r = 0; r < n_rounds; ++r)
+            oracle_attend_backward(qh, vh, inv_norm, bucket + r * (size_t)L, perm + r * (size_t)L,
+                                   L, d, chunk, causal, scale, o_r + r * Ld, lse_r + r * (size_t)L,
+                                   g_o + r * Ld, g_lse_r + r * (size_t)L, dq, dkhat, dvh);
+        oracle_key_norm_backward(qh, inv_norm, dkhat, L, d, dq);
+    }
+done:
+    free(bucket); free(perm); free(inv); free(bstart); free(o_r); free(lse_r);
+    free(g_o); free(g_lse_r); free(out); free(lse); free(inv_norm); free(dkhat);
     return rc;
 }

@@ -410,4 +410,100 @@ def pin_combine_is_softmax_over_the_rounds_multiset(orc):
         assert np.allclose(lse[0][rows], ref_lse.numpy()[rows], rtol=1e-10, atol=1e-10)
 
 
+
+# --------------------------------------------------------------------------
+# Backward pass (gradients of the forward in qk and v, buckets held fixed)
+# --------------------------------------------------------------------------
+
+def _fixed_bucket_loss(orc, qk, v, it, c, causal, scale, g_out, g_lse, lse0):
+    """sum(g_out * out) + sum(g_lse * (lse - lse0)) of one head, recomputed through the
+    oracle's staged attention and combination with the given rounds' buckets and
+    permutations.  lse0 (the unperturbed lse) is a constant offset that keeps the
+    self-only tokens' lse (about -1e5) from swamping the differences in rounding."""
+    o_r, lse_r = [], []
+    for r in range(it["bucket"].shape[1]):
+        o, l = orc.attend(qk, v, it["bucket"][0, r], it["perm"][0, r], c, causal, scale)
+        o_r.append(o)
+        lse_r.append(l)
+    out, lse = orc.combine(np.stack(o_r), np.stack(lse_r), it["inv"][0])
+    return float((g_out * out).sum() + (g_lse * (lse - lse0)).sum())
+
+
+def pin_backward_matches_finite_differences(orc):
+    """Central differences of the (pinned) forward, buckets held fixed, agree with the
+    backward in every element of qk and v; the value gradients of each token sum to the
+    token's output gradient summed over tokens (each output row's weights sum to one)."""
+    rng = _rng(17)
+    h = 1e-5
+    for L, d, nb, c, n_rounds, causal in ((16, 4, 4, 4, 2, True), (16, 4, 2, 8, 3, False)):
+        qk = rng.standard_normal((L, d))
+        v = rng.standard_normal((L, d))
+        R = rng.standard_normal((n_rounds, d, nb // 2))
+        g_out = rng.standard_normal((L, d))
+        g_lse = rng.standard_normal(L)
+        scale = 0.8
+        _, lse0, it = orc.forward(qk[None], v[None], R, nb, c, causal, scale,
+                                  intermediates=True)
+        lse0 = lse0[0]
+        assert lse0[0] < -1e4 or not causal   # causal: token 0 is alone in every round
+        dqk, dv = orc.backward(qk[None], v[None], R, nb, c, causal, scale, g_out[None],
+                               g_lse[None])
+        for name, x, grad in (("qk", qk, dqk[0]), ("v", v, dv[0])):
+            fd = np.empty_like(x)
+            for idx in np.ndindex(*x.shape):
+                xp, xm = x.copy(), x.copy()
+                xp[idx] += h
+                xm[idx] -= h
+                args_p = (xp, v) if name == "qk" else (qk, xp)
+                args_m = (xm, v) if name == "qk" else (qk, xm)
+                fd[idx] = (_fixed_bucket_loss(orc, *args_p, it, c, causal, scale, g_out, g_lse, lse0)
+                           - _fixed_bucket_loss(orc, *args_m, it, c, causal, scale, g_out, g_lse,
+                                                lse0)) / (2 * h)
+            assert np.allclose(grad, fd, rtol=1e-7, atol=1e-8), (name, np.abs(grad - fd).max())
+        # (a round weight exp(lse_r - LSE) of a token alone in every round subtracts two
+        # numbers near -1e5, so it carries about 1e-11 of rounding)
+        assert np.allclose(dv[0].sum(0), g_out.sum(0), rtol=0, atol=1e-9)
+
+
+def pin_backward_matches_autograd_of_the_multiset_softmax(orc):
+    """torch autograd of an independent dense formulation: one softmax over the multiset
+    union of the rounds' brute-force candidate sets (additive mask ln count_ij), the rounds
+    in which a token has no candidate entering as a constant diagonal logit
+    self_logit + ln(their number) with value v_i.  Gradients in qk and v of
+    sum(g_out * out) + sum(g_lse * lse) must match the oracle's backward."""
+    rng = _rng(18)
+    L, d, nb, c, n_rounds, scale = 48, 8, 6, 8, 3, 0.6
+    qk = rng.standard_normal((L, d))
+    v = rng.standard_normal((L, d))
+    R = rng.standard_normal((n_rounds, d, nb // 2))
+    g_out = rng.standard_normal((L, d))
+    g_lse = rng.standard_normal(L)
+    for causal in (False, True):
+        _, _, it = orc.forward(qk[None], v[None], R, nb, c, causal, scale, intermediates=True)
+        count = np.zeros((L, L))
+        n_self = np.zeros(L)
+        for r in range(n_rounds):
+            bucket = it["bucket"][0, r]
+            for i in range(L):
+                cands = _brute_candidates(bucket, i, c, causal)
+                count[i, cands] += 1
+                n_self[i] += not cands
+        assert n_self.max() >= 1 and (count >= 2).any()
+        eye = torch.eye(L, dtype=torch.bool)
+        logc = torch.from_numpy(np.where(count > 0, np.log(np.maximum(count, 1)), -np.inf))
+        diag = torch.from_numpy(np.where(n_self > 0, orc.SELF_LOGIT + np.log(np.maximum(n_self, 1)),
+                                         -np.inf))
+        q = torch.tensor(qk, requires_grad=True)
+        vv = torch.tensor(v, requires_grad=True)
+        k = q / q.norm(dim=-1, keepdim=True)
+        logits = torch.where(eye, diag[:, None].expand(L, L), (q @ k.T) * scale + logc)
+        out = torch.softmax(logits, dim=-1) @ vv
+        lse = torch.logsumexp(logits, dim=-1)
+        ((torch.from_numpy(g_out) * out).sum() + (torch.from_numpy(g_lse) * lse).sum()).backward()
+        dqk, dv = orc.backward(qk[None], v[None], R, nb, c, causal, scale, g_out[None],
+                               g_lse[None])
+        assert np.allclose(dqk[0], q.grad.numpy(), rtol=1e-9, atol=1e-10)
+        assert np.allclose(dv[0], vv.grad.numpy(), rtol=1e-9, atol=1e-10)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -26,8 +26,8 @@ MUTANTS = [
     ("attend_causal_reversed", "if (causal && !(j < i)) continue;", "if (causal && !(j > i)) continue;"),
     ("attend_no_lookback", "int lo = (k - 1) * chunk;", "int lo = k * chunk;"),
     ("attend_next_chunk_instead",
-     "int lo = (k - 1) * chunk;\n        if (lo < 0) lo = 0;\n        int hi = (k + 1) * chunk;",
-     "int lo = k * chunk;\n        if (lo < 0) lo = 0;\n        int hi = (k + 2) * chunk;"),
+     "int lo = (k - 1) * chunk;\n    if (lo < 0) lo = 0;\n    int hi = (k + 1) * chunk;",
+     "int lo = k * chunk;\n    if (lo < 0) lo = 0;\n    int hi = (k + 2) * chunk;"),
     ("attend_keys_not_normalised", "score[a] = scale * dot * inv_norm[j];", "score[a] = scale * dot;"),
     ("attend_scale_dropped", "score[a] = scale * dot * inv_norm[j];", "score[a] = dot * inv_norm[j];"),
     ("attend_lse_unshifted", "lse_sorted[s] = mx + log(sum);", "lse_sorted[s] = log(sum);"),
@@ -40,6 +40,19 @@ MUTANTS = [
     ("combine_not_unsorted",
      "int s = inv[(size_t)r * L + i];\n            double w",
      "int s = i;\n            double w"),
+    ("bwd_combine_no_mean_term", "dot += gi[c] * (src[c] - oi[c]);", "dot += gi[c] * src[c];"),
+    ("bwd_combine_round_weight_dropped", "go[c] += w * gi[c];", "go[c] += gi[c];"),
+    ("bwd_combine_lse_grad_dropped", "g_lse_r[(size_t)r * L + s] += w * (dot + g_lse[i]);",
+     "g_lse_r[(size_t)r * L + s] += w * dot;"),
+    ("bwd_attend_no_mean_term", "gv += gs[c] * (vj[c] - os[c]);", "gv += gs[c] * vj[c];"),
+    ("bwd_attend_query_scale_dropped", "dq[(size_t)i * d + c] += ds * scale * kj[c] * inv_norm[j];",
+     "dq[(size_t)i * d + c] += ds * kj[c] * inv_norm[j];"),
+    ("bwd_attend_key_grad_transposed", "dkhat[(size_t)j * d + c] += ds * scale * qi[c];",
+     "dkhat[(size_t)i * d + c] += ds * scale * kj[c];"),
+    ("bwd_attend_dv_at_query", "dv[(size_t)j * d + c] += p * gs[c];", "dv[(size_t)i * d + c] += p * gs[c];"),
+    ("bwd_attend_self_row_dropped", "for (int c = 0; c < d; ++c) dv[(size_t)i * d + c] += gs[c];", ""),
+    ("bwd_key_norm_jacobian_dropped", "inv_norm[j] * (g[c] - x[c] * inv_norm[j] * proj)",
+     "inv_norm[j] * g[c]"),
 ]
 
 RUNNER = r"""
