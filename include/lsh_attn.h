@@ -1,5 +1,6 @@
 /*
- * lsh_attn.h -- C ABI of the B300 (sm_103a) multi-round LSH-attention forward pass.
+ * lsh_attn.h -- C ABI of the B300 (sm_103a) multi-round LSH attention: the forward pass
+ * and its backward pass.
  *
  * The method is Reformer's LSH attention over a shared query/key projection
  * (Kitaev, Kaiser & Levskaya, "Reformer: The Efficient Transformer", ICLR 2020), as
@@ -119,6 +120,42 @@ lsh_status_t lsh_attn_forward_timed(const void *qk, const void *v, const void *R
                                     float scale, float *out, float *lse, void *workspace,
                                     size_t workspace_bytes, void *stream,
                                     void *const *stage_events);
+
+/*
+ * Bytes of device workspace lsh_attn_backward needs (0 when the arguments are invalid
+ * or unsupported).  Smaller than the forward's: no per-round outputs.
+ */
+size_t lsh_attn_backward_workspace_bytes(int B, int H, int L, int d, int n_buckets,
+                                         int n_rounds, int chunk, lsh_dtype_t dtype);
+
+/*
+ * Backward pass: the gradients in qk and v of the loss
+ *     sum(g_out * out) + sum(g_lse * lse)
+ * of the lsh_attn_forward call with the same arguments.  The Reformer pages train the
+ * model by back-propagation (modulabs-hub notes, "Introduction") but give no gradient
+ * formula; this is the derivative of steps 4-6 above with the buckets held fixed.  The
+ * hash is piecewise constant, so neither the hash nor the sort is differentiated.
+ * Steps 1-2 are recomputed here with the forward's kernels, which are deterministic and
+ * so give the forward's buckets and order.  Every (round, candidate) pair of token i is
+ * one entry of a single softmax with weight exp(s_ij - lse_i), which is why `out` and
+ * `lse` from the forward are all that is kept of it.
+ *   qk, v, R  as given to lsh_attn_forward (same dtype, sizes, causal and scale)
+ *   out, lse  fp32 [B][H][L][d] and [B][H][L]: that call's outputs
+ *   g_out     fp32 [B][H][L][d]: the loss's gradient in out
+ *   g_lse     fp32 [B][H][L]: the loss's gradient in lse, or NULL for zero
+ *   dqk, dv   fp32 [B][H][L][d]: overwritten with the gradients in qk and v
+ * A zero row of qk has a constant score 0 as a key and gets no gradient through that
+ * role.  A token with no key left in any round gets 1/n_rounds of its output gradient
+ * in dv from each round (it copies v_i).  dqk and dv must not alias any input or the
+ * workspace.  The gradients are summed with fp32 atomics, so the order of additions,
+ * and with it the last bits, can change from call to call.
+ */
+lsh_status_t lsh_attn_backward(const void *qk, const void *v, const void *R, lsh_dtype_t dtype,
+                               int B, int H, int L, int d, int n_buckets, int n_rounds,
+                               int chunk, int causal, float scale, const float *out,
+                               const float *lse, const float *g_out, const float *g_lse,
+                               float *dqk, float *dv, void *workspace, size_t workspace_bytes,
+                               void *stream);
 
 /*
  * Number of kernels one lsh_attn_forward call launches for this problem (0 when the

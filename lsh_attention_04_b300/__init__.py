@@ -4,9 +4,9 @@ Argument marshalling only: every step of the forward pass runs in the CUDA kerne
 ``liblshattn.so``.  torch supplies device memory and the current stream.  When the
 library cannot be loaded, every call raises; there is no fallback.
 
-Functions carry the C names: lsh_attn_forward, lsh_hash, lsh_bucket_sort,
-lsh_chunk_attn, lsh_unsort_combine, lsh_attn_workspace_bytes, lsh_status_string,
-lsh_workspace_status.
+Functions carry the C names: lsh_attn_forward, lsh_attn_backward, lsh_hash,
+lsh_bucket_sort, lsh_chunk_attn, lsh_unsort_combine, lsh_attn_workspace_bytes,
+lsh_status_string, lsh_workspace_status.
 """
 from __future__ import annotations
 
@@ -33,6 +33,7 @@ EXPORTS = (
     "lsh_bucket_sort_workspace_bytes", "lsh_bucket_sort", "lsh_chunk_attn_workspace_bytes",
     "lsh_chunk_attn", "lsh_unsort_combine", "lsh_workspace_status", "lsh_attn_forward_timed",
     "lsh_attn_kernel_launches", "lsh_bucket_sort_noalloc", "lsh_selftest_wait_timeout",
+    "lsh_attn_backward_workspace_bytes", "lsh_attn_backward",
 )
 
 _lib = None
@@ -81,6 +82,10 @@ def load():
     lib.lsh_unsort_combine.restype = I
     lib.lsh_workspace_status.argtypes = [P, ctypes.POINTER(I), P]
     lib.lsh_workspace_status.restype = I
+    lib.lsh_attn_backward_workspace_bytes.argtypes = [I] * 8
+    lib.lsh_attn_backward_workspace_bytes.restype = S
+    lib.lsh_attn_backward.argtypes = [P, P, P, I] + [I] * 8 + [F, P, P, P, P, P, P, P, S, P]
+    lib.lsh_attn_backward.restype = I
     lib.lsh_selftest_wait_timeout.argtypes = [P, S, P]
     lib.lsh_selftest_wait_timeout.restype = I
     _lib = lib
@@ -192,6 +197,40 @@ def lsh_attn_forward_timed(qk, v, R, n_buckets, chunk, causal, scale, out, lse, 
                                          ws.numel(), s, handles),
            "lsh_attn_forward_timed")
     return out, lse
+
+
+def lsh_attn_backward(qk, v, R, n_buckets, chunk, causal, scale, out, lse, g_out, g_lse=None,
+                      dqk=None, dv=None, ws=None, stream=None):
+    """Backward pass: gradients in qk and v of sum(g_out * out) + sum(g_lse * lse), where
+    out and lse are lsh_attn_forward's outputs for the same arguments (buckets held fixed).
+
+    g_out fp32 [B, H, L, d]; g_lse fp32 [B, H, L] or None (zero).  Returns (dqk, dv),
+    fp32 [B, H, L, d]."""
+    torch = _torch()
+    B, H, L, d = qk.shape
+    n_rounds = R.shape[0]
+    dt = _dtype_code(qk)
+    if v.dtype != qk.dtype or R.dtype != qk.dtype:
+        raise TypeError("qk, v and R must share one dtype")
+    for name, t in (("out", out), ("lse", lse), ("g_out", g_out), ("g_lse", g_lse)):
+        if t is not None and t.dtype != torch.float32:
+            raise TypeError(f"{name} must be float32")
+    if dqk is None:
+        dqk = torch.empty((B, H, L, d), dtype=torch.float32, device=qk.device)
+    if dv is None:
+        dv = torch.empty((B, H, L, d), dtype=torch.float32, device=qk.device)
+    if ws is None:
+        n = int(load().lsh_attn_backward_workspace_bytes(B, H, L, d, n_buckets, n_rounds, chunk, dt))
+        if n == 0:
+            raise LshError(LSH_ERR_INVALID_ARGUMENT, "lsh_attn_backward_workspace_bytes")
+        ws = torch.empty(n, dtype=torch.uint8, device=qk.device)
+    _check(load().lsh_attn_backward(_ptr(qk), _ptr(v), _ptr(R), dt, B, H, L, d, n_buckets,
+                                    n_rounds, chunk, int(causal), float(scale), _ptr(out),
+                                    _ptr(lse), _ptr(g_out),
+                                    None if g_lse is None else _ptr(g_lse), _ptr(dqk), _ptr(dv),
+                                    _ptr(ws), ws.numel(), _stream(stream)),
+           "lsh_attn_backward")
+    return dqk, dv
 
 
 def lsh_attn_kernel_launches(B, H, L, d, n_buckets, n_rounds, chunk, dtype_code) -> int:

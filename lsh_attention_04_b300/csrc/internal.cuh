@@ -88,6 +88,11 @@ cudaError_t attn_tc(const Problem &p, const void *qk, const void *v, const int32
                     const int32_t *perm, const int32_t *bstart, const float *inv_norm, void *o_r,
                     float *lse_r, StatusBlock *status, cudaStream_t st);
 
+// backward of attention + combination; dqk and dv (fp32) are accumulated into
+cudaError_t attn_bwd(const Problem &p, const void *qk, const void *v, const int32_t *buckets,
+                     const int32_t *perm, const float *inv_norm, const float *out, const float *lse,
+                     const float *g_out, const float *g_lse, float *dqk, float *dv, cudaStream_t st);
+
 cudaError_t selftest_wait_launch(StatusBlock *status, cudaStream_t st);
 
 cudaError_t combine_launch(const Problem &p, const void *o_r, const float *lse_r,

@@ -42,12 +42,13 @@ size_t esize(lsh_dtype_t t) { return t == LSH_F32 ? 4 : 2; }
 size_t rpack_bytes(const Problem &p) { return hash_tc_supported(p) ? hash_tc_pack_bytes(p) : 0; }
 size_t counts_bytes(const Problem &p) { return sizeof(int32_t) * p.n_seg() * p.nb * sort_tiles(p.L); }
 
-// Workspace of the whole forward pass.
+// Workspace of the whole forward pass; the backward pass uses the same layout without
+// the per-round outputs (round_outputs = false).
 struct Layout {
     size_t rpack, counts, buckets, inv_norm, perm, inv, bstart, o_r, lse_r, total;
 };
 
-Layout layout(const Problem &p)
+Layout layout(const Problem &p, bool round_outputs = true)
 {
     Layout w;
     size_t o = align_up(sizeof(StatusBlock));
@@ -59,8 +60,8 @@ Layout layout(const Problem &p)
     w.perm = o;     o = align_up(o + sizeof(int32_t) * SL);
     w.inv = o;      o = align_up(o + sizeof(int32_t) * SL);
     w.bstart = o;   o = align_up(o + sizeof(int32_t) * p.n_seg() * (p.nb + 1));
-    w.o_r = o;      o = align_up(o + esize(p.dtype) * SL * p.d);
-    w.lse_r = o;    o = align_up(o + sizeof(float) * SL);
+    w.o_r = o;      o = align_up(o + (round_outputs ? esize(p.dtype) * SL * p.d : 0));
+    w.lse_r = o;    o = align_up(o + (round_outputs ? sizeof(float) * SL : 0));
     w.total = o;
     return w;
 }
@@ -211,6 +212,48 @@ lsh_status_t lsh_attn_forward_timed(const void *qk, const void *v, const void *R
         if (!stage_events[i]) return LSH_ERR_INVALID_ARGUMENT;
     return forward(qk, v, R, dtype, B, H, L, d, n_buckets, n_rounds, chunk, causal, scale, out,
                    lse, workspace, workspace_bytes, stream, stage_events);
+}
+
+size_t lsh_attn_backward_workspace_bytes(int B, int H, int L, int d, int n_buckets,
+                                         int n_rounds, int chunk, lsh_dtype_t dtype)
+{
+    const Problem p = make_problem(B, H, L, d, n_buckets, n_rounds, chunk, 0, 1.f, dtype);
+    if (validate(p) != LSH_OK) return 0;
+    return layout(p, false).total;
+}
+
+lsh_status_t lsh_attn_backward(const void *qk, const void *v, const void *R, lsh_dtype_t dtype,
+                               int B, int H, int L, int d, int n_buckets, int n_rounds,
+                               int chunk, int causal, float scale, const float *out,
+                               const float *lse, const float *g_out, const float *g_lse,
+                               float *dqk, float *dv, void *workspace, size_t workspace_bytes,
+                               void *stream)
+{
+    const Problem p = make_problem(B, H, L, d, n_buckets, n_rounds, chunk, causal, scale, dtype);
+    lsh_status_t s = validate(p);
+    if (s != LSH_OK) return s;
+    if (!qk || !v || !R || !out || !lse || !g_out || !dqk || !dv || !workspace)
+        return LSH_ERR_INVALID_ARGUMENT;
+    if (((uintptr_t)workspace) % 256 != 0) return LSH_ERR_INVALID_ARGUMENT;
+    const Layout w = layout(p, false);
+    if (workspace_bytes < w.total) return LSH_ERR_WORKSPACE_TOO_SMALL;
+    cudaStream_t st = (cudaStream_t)stream;
+    int32_t *buckets = at<int32_t>(workspace, w.buckets);
+    float *inv_norm = at<float>(workspace, w.inv_norm);
+    int32_t *perm = at<int32_t>(workspace, w.perm);
+    const size_t grad_bytes = sizeof(float) * (size_t)p.n_tok() * p.d;
+    if ((s = clear_status(workspace, st)) != LSH_OK) return s;
+    if ((s = cuda_status(cudaMemsetAsync(dqk, 0, grad_bytes, st))) != LSH_OK) return s;
+    if ((s = cuda_status(cudaMemsetAsync(dv, 0, grad_bytes, st))) != LSH_OK) return s;
+    // the same deterministic kernels as the forward pass: the same buckets and order
+    if ((s = run_hash(p, qk, R, buckets, inv_norm, workspace, at<void>(workspace, w.rpack), st)) != LSH_OK)
+        return s;
+    if ((s = cuda_status(sort_launch(p, buckets, perm, at<int32_t>(workspace, w.inv),
+                                     at<int32_t>(workspace, w.bstart),
+                                     at<int32_t>(workspace, w.counts), st))) != LSH_OK)
+        return s;
+    return cuda_status(attn_bwd(p, qk, v, buckets, perm, inv_norm, out, lse, g_out, g_lse, dqk,
+                                dv, st));
 }
 
 int lsh_attn_kernel_launches(int B, int H, int L, int d, int n_buckets, int n_rounds, int chunk,

@@ -289,6 +289,41 @@ class Oracle:
                                         _p(g_o), _p(g_lse), _p(dq), _p(dkhat), _p(dv))
         return dq, dkhat, dv
 
+    def key_norm_backward(self, qk, dkhat):
+        """Gradient in qk through the unit key qk / |qk|, for the gradient dkhat in it."""
+        qk, dkhat = _f64(qk), _f64(dkhat)
+        L, d = qk.shape
+        inorm = self.inv_norm(qk)
+        dqk = np.zeros((L, d), np.float64)
+        self.lib.oracle_key_norm_backward(_p(qk), _p(inorm), _p(dkhat), L, d, _p(dqk))
+        return dqk
+
+    def backward_given_buckets(self, qk, v, bucket, n_buckets, chunk, causal, scale, g_out,
+                               g_lse):
+        """Forward and backward of one head with the given buckets [n_rounds, L] instead of
+        the oracle's own hash (so that hash near-ties of another implementation do not
+        enter a comparison).  Returns (out, lse, dqk, dv)."""
+        qk, v = _f64(qk), _f64(v)
+        bucket = _i32(bucket)
+        n_rounds = bucket.shape[0]
+        perm, inv, o_r, lse_r = [], [], [], []
+        for r in range(n_rounds):
+            p, i, _ = self.sort(bucket[r], n_buckets)
+            o, l = self.attend(qk, v, bucket[r], p, chunk, causal, scale)
+            perm.append(p); inv.append(i); o_r.append(o); lse_r.append(l)
+        o_r, lse_r, inv = np.stack(o_r), np.stack(lse_r), np.stack(inv)
+        out, lse = self.combine(o_r, lse_r, inv)
+        g_lse = np.zeros(len(lse)) if g_lse is None else g_lse
+        g_o, g_lse_r = self.combine_backward(o_r, lse_r, inv, out, lse, g_out, g_lse)
+        dq = np.zeros_like(qk)
+        dkhat = np.zeros_like(qk)
+        dv = np.zeros_like(v)
+        for r in range(n_rounds):
+            a, b, c = self.attend_backward(qk, v, bucket[r], perm[r], chunk, causal, scale,
+                                           o_r[r], lse_r[r], g_o[r], g_lse_r[r])
+            dq += a; dkhat += b; dv += c
+        return out, lse, dq + self.key_norm_backward(qk, dkhat), dv
+
 
 def default() -> Oracle:
     """The oracle compiled from lsh_oracle.c (built on first use)."""

@@ -159,3 +159,47 @@ def test_stage_validation(lib):
     assert lib.lsh_selftest_wait_timeout(None, 256, None) == lsh.LSH_ERR_INVALID_ARGUMENT
     assert lib.lsh_selftest_wait_timeout(P(256), 128, None) == lsh.LSH_ERR_INVALID_ARGUMENT
     assert lib.lsh_selftest_wait_timeout(P(260), 256, None) == lsh.LSH_ERR_INVALID_ARGUMENT
+
+
+def test_backward_workspace_sizing(lib):
+    args = (1, 8, 65536, 128, 1024, 8, 64, lsh.LSH_BF16)
+    fwd = lib.lsh_attn_workspace_bytes(*args)
+    bwd = lib.lsh_attn_backward_workspace_bytes(*args)
+    # no per-round outputs (o_r alone is B*H*R*L*d*2 bytes), but buckets, perm, inv
+    assert 0 < bwd < fwd - 1 * 8 * 8 * 65536 * 128 * 2
+    assert bwd > 3 * 4 * 8 * 8 * 65536 and bwd % 256 == 0
+    assert lib.lsh_attn_backward_workspace_bytes(1, 1, 100, 64, 32, 1, 64, lsh.LSH_F32) == 0
+
+
+def _bwd(lib, **kw):
+    a = dict(qk=1, v=1, R=1, dtype=lsh.LSH_BF16, B=1, H=1, L=1024, d=64, nb=32, R_=1,
+             chunk=64, causal=1, scale=0.125, out=1, lse=1, g_out=1, g_lse=0, dqk=1, dv=1,
+             ws=256, wsb=1 << 30, st=None)
+    a.update(kw)
+    P = ctypes.c_void_p
+    return lib.lsh_attn_backward(P(a["qk"]), P(a["v"]), P(a["R"]), a["dtype"], a["B"], a["H"],
+                                 a["L"], a["d"], a["nb"], a["R_"], a["chunk"], a["causal"],
+                                 a["scale"], P(a["out"]), P(a["lse"]), P(a["g_out"]),
+                                 P(a["g_lse"]), P(a["dqk"]), P(a["dv"]), P(a["ws"]), a["wsb"],
+                                 a["st"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(qk=0), lsh.LSH_ERR_INVALID_ARGUMENT),
+    (dict(out=0), lsh.LSH_ERR_INVALID_ARGUMENT),
+    (dict(lse=0), lsh.LSH_ERR_INVALID_ARGUMENT),
+    (dict(g_out=0), lsh.LSH_ERR_INVALID_ARGUMENT),
+    (dict(dqk=0), lsh.LSH_ERR_INVALID_ARGUMENT),
+    (dict(dv=0), lsh.LSH_ERR_INVALID_ARGUMENT),
+    (dict(ws=0), lsh.LSH_ERR_INVALID_ARGUMENT),
+    (dict(ws=4), lsh.LSH_ERR_INVALID_ARGUMENT),          # misaligned workspace
+    (dict(L=1000), lsh.LSH_ERR_INVALID_ARGUMENT),        # not a multiple of chunk
+    (dict(causal=2), lsh.LSH_ERR_INVALID_ARGUMENT),
+    (dict(d=96), lsh.LSH_ERR_UNSUPPORTED),
+    (dict(chunk=128, L=1024), lsh.LSH_ERR_UNSUPPORTED),
+    (dict(nb=40), lsh.LSH_ERR_UNSUPPORTED),
+    (dict(wsb=1024), lsh.LSH_ERR_WORKSPACE_TOO_SMALL),
+])
+@no_device
+def test_backward_validation(lib, kw, expect):
+    assert _bwd(lib, **kw) == expect
