@@ -2,12 +2,15 @@
 """Forward throughput of multi-round LSH attention on B300 (tokens/s = B*H*L per second).
 
     python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference] [--workload NAME]
+                    [--pass forward|backward]
 
 Default workload: the long-text shape B=1, H=8, L=65536, d=128, bf16, 1024 buckets,
 8 rounds, chunk 64, causal (the headline L = 64K, 8-round configuration).  Each rank runs
 its own copy of the workload (independent heads: weak scaling, no data-path collective).
 Rank 0 prints one JSON line.  ``--impl reference`` times the fp64 CPU oracle on a bounded
-sample of the same workload instead.
+sample of the same workload instead.  ``--pass backward`` times lsh_attn_backward (the
+gradients in qk and v) on the same workload instead of the forward pass, with its own
+metric line.
 """
 from __future__ import annotations
 
@@ -27,6 +30,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "LSH-attention fwd tokens/s (B·H·L per sec) at L=64K, 8 rounds; % of roofline"
+METRIC_BWD = "LSH-attention bwd tokens/s (B·H·L per sec) at L=64K, 8 rounds: dqk, dv"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 L2_BYTES = 126 * 2 ** 20
@@ -45,6 +49,7 @@ KERNEL_SOURCES = {
     "sort": ["sort.cu"],
     "attn": ["attn_tc.cu", "sm100.cuh"],
     "combine": ["combine.cu", "combine_tma.cu", "sm100.cuh"],
+    "attn_bwd": ["attn_bwd.cu"],
 }
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
@@ -97,6 +102,46 @@ def work(w):
     # token-order rows (fused forward): o_r and lse_r read once, no inverse permutation
     k["combine"] = dict(flops=0, bytes=N * R * (d * wr + 4) + N * (4 * d + 4))
     return k
+
+
+def work_backward(w):
+    """Algorithmic FLOPs and bytes per kernel for one backward pass of workload w: the
+    hash and sort recomputed, then the attention backward.  Per token and round that
+    kernel does five contractions over the c x 2c window (Q K^T again, g_out V^T, and the
+    gradients in q, k and v), 4 c d flops each; it reads qk, v, out, g_out, lse, g_lse,
+    the inverse norms, buckets and perm once and writes dqk and dv once."""
+    N, R, d, c = w.tokens, w.n_rounds, w.d, w.chunk
+    e = 2 if w.dtype == "bf16" else 4
+    k = work(w)
+    return {
+        "hash": k["hash"],
+        "sort": k["sort"],
+        "attn_bwd": dict(flops=20 * N * R * c * d,
+                         bytes=2 * N * d * e + 2 * N * d * 4 + 3 * N * 4 + 2 * N * R * 4
+                         + 2 * N * d * 4),
+    }
+
+
+def kernel_roof(w, name, ms, wk, unit_c, peak_c, peaks, peak_src):
+    """Roofline entry of one kernel: the slower of its FLOPs at the compute peak and its
+    bytes at HBM bandwidth decides the bound; achieved = algorithmic work / measured time."""
+    t = ms / 1e3
+    f, by = wk["flops"], wk["bytes"]
+    t_c = f / (peak_c * 1e12)
+    t_b = by / (peaks["hbm_gbs"] * 1e9)
+    if t_c > t_b:
+        b, ach, peak, unit = unit_c, f / t / 1e12, peak_c, "TFLOP/s"
+        src = (f"{peak_src} bf16 burst" if unit_c == "tensor" else "fp32 lanes x clock")
+    else:
+        b, ach, peak, unit = "hbm", by / t / 1e9, peaks["hbm_gbs"], "GB/s"
+        src = f"{peak_src} copy bandwidth"
+    r = {"bound": b, "achieved": ach, "peak": peak, "unit": unit, "frac": ach / peak,
+         "traffic": recorded_traffic(w.name, name), "kernel": name, "ms": ms,
+         "roof_ms": 1e3 * max(t_c, t_b), "algorithmic_flops": f, "algorithmic_bytes": by,
+         "peak_source": src}
+    if f and unit_c == "tensor":
+        r["tensor_frac"] = f / t / 1e12 / peak_c   # of the measured dense bf16 peak
+    return r
 
 
 # ------------------------------------------------------------------ clocks
@@ -185,6 +230,23 @@ def time_oracle(w, threads, steps=1, max_tokens=32768):
     return sub.tokens, times, used, desc
 
 
+def time_oracle_backward(w, steps=1, max_tokens=4096):
+    """The oracle's backward pass (one thread per head: a single head here) on a bounded
+    sample of w, with seeded output gradients."""
+    import oracle
+    sub, qk, v, R, desc = oracle_sample(w, max_tokens)
+    rng = np.random.default_rng(w.seed + 5)
+    g_out = rng.standard_normal(qk.shape)
+    g_lse = rng.standard_normal(qk.shape[:-1])
+    oracle.build()
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        oracle.backward(qk, v, R, sub.n_buckets, sub.chunk, sub.causal, sub.scale, g_out, g_lse)
+        times.append(time.perf_counter() - t0)
+    return sub.tokens, times, 1, desc + "; backward (forward recomputed inside)"
+
+
 # ------------------------------------------------------------------ runs
 
 
@@ -228,13 +290,18 @@ def run_reference(args, w):
     # Bound the whole run to a couple of minutes: one 32K-token sample takes a few
     # seconds, so many requested steps get proportionally smaller samples.
     n = args.warmup + args.steps
-    max_tokens = 32768 if n <= 40 else max(2 * w.chunk, 32768 * 40 // n)
-    tokens, times, used, desc = time_oracle(w, threads, steps=n, max_tokens=max_tokens)
+    if args.pass_ == "backward":
+        max_tokens = 4096 if n <= 10 else max(2 * w.chunk, 4096 * 10 // n)
+        tokens, times, used, desc = time_oracle_backward(w, steps=n, max_tokens=max_tokens)
+    else:
+        max_tokens = 32768 if n <= 40 else max(2 * w.chunk, 32768 * 40 // n)
+        tokens, times, used, desc = time_oracle(w, threads, steps=n, max_tokens=max_tokens)
     timed = times[args.warmup:]
     t = sum(timed) / len(timed)
     value = tokens / t
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "impl": "reference", "metric": METRIC_BWD if args.pass_ == "backward" else METRIC,
+        "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * t, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -365,23 +432,7 @@ def run_ours(args, w):
     peak_c = peaks["bf16_tflops"] if unit_c == "tensor" else FP32_ALU_TFLOPS
 
     def roof(name):
-        t = stage_ms[name] / 1e3
-        f, by = wk[name]["flops"], wk[name]["bytes"]
-        t_c = f / (peak_c * 1e12)
-        t_b = by / (peaks["hbm_gbs"] * 1e9)
-        if t_c > t_b:
-            b, ach, peak, unit = unit_c, f / t / 1e12, peak_c, "TFLOP/s"
-            src = (f"{peak_src} bf16 burst" if unit_c == "tensor" else "fp32 lanes x clock")
-        else:
-            b, ach, peak, unit = "hbm", by / t / 1e9, peaks["hbm_gbs"], "GB/s"
-            src = f"{peak_src} copy bandwidth"
-        r = {"bound": b, "achieved": ach, "peak": peak, "unit": unit, "frac": ach / peak,
-             "traffic": recorded_traffic(w.name, name), "kernel": name, "ms": stage_ms[name],
-             "roof_ms": 1e3 * max(t_c, t_b), "algorithmic_flops": f, "algorithmic_bytes": by,
-             "peak_source": src}
-        if f and unit_c == "tensor":
-            r["tensor_frac"] = f / t / 1e12 / peak_c   # of the measured dense bf16 peak
-        return r
+        return kernel_roof(w, name, stage_ms[name], wk[name], unit_c, peak_c, peaks, peak_src)
 
     F = sum(k["flops"] for k in wk.values())
     Bts = sum(k["bytes"] for k in wk.values())
@@ -417,6 +468,163 @@ def run_ours(args, w):
     return 0
 
 
+def run_backward(args, w):
+    """The backward pass of workload w: K timed lsh_attn_backward calls on device-resident
+    inputs (qk, v, R, the forward's out and lse, seeded g_out and g_lse), stage events
+    inside each call, then the same calls end to end from pinned host buffers."""
+    import torch
+    import lsh_attention_04_b300 as lsh
+    from lsh_attention_04_b300 import inputs as gen
+
+    world, rank, local, dist = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lib = lsh.load()
+    dt_code = lsh.LSH_BF16 if w.dtype == "bf16" else lsh.LSH_F32
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+
+    qk, v, R = gen.make_inputs(w, seed=w.seed + 7919 * rank)
+    rng = np.random.default_rng(w.seed + 5 + 7919 * rank)
+    h_qk = torch.from_numpy(qk).to(tdt).pin_memory()
+    h_v = torch.from_numpy(v).to(tdt).pin_memory()
+    h_R = torch.from_numpy(R).to(tdt).pin_memory()
+    h_g = torch.from_numpy(rng.standard_normal(qk.shape).astype(np.float32)).pin_memory()
+    h_gl = torch.from_numpy(rng.standard_normal(qk.shape[:-1]).astype(np.float32)).pin_memory()
+    d_qk, d_v, d_R, d_g, d_gl = (t.to(dev) for t in (h_qk, h_v, h_R, h_g, h_gl))
+    out, lse = lsh.lsh_attn_forward(d_qk, d_v, d_R, w.n_buckets, w.chunk, w.causal, w.scale)
+    h_out = out.cpu().pin_memory()
+    h_lse = lse.cpu().pin_memory()
+    dqk = torch.empty((w.B, w.H, w.L, w.d), dtype=torch.float32, device=dev)
+    dv = torch.empty_like(dqk)
+    n_ws = int(lib.lsh_attn_backward_workspace_bytes(w.B, w.H, w.L, w.d, w.n_buckets,
+                                                     w.n_rounds, w.chunk, dt_code))
+    ws = torch.empty(n_ws, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    K, Wm = args.steps, args.warmup
+
+    def bwd(events=None):
+        if events is None:
+            lsh.lsh_attn_backward(d_qk, d_v, d_R, w.n_buckets, w.chunk, w.causal, w.scale, out,
+                                  lse, d_g, d_gl, dqk=dqk, dv=dv, ws=ws)
+        else:
+            lsh.lsh_attn_backward_timed(d_qk, d_v, d_R, w.n_buckets, w.chunk, w.causal,
+                                        w.scale, out, lse, d_g, d_gl, dqk, dv, ws, events)
+
+    for _ in range(Wm):
+        bwd()
+    torch.cuda.synchronize()
+    st, dd = lsh.lsh_workspace_status(ws)
+    if st != lsh.LSH_OK:
+        raise RuntimeError(f"device check failed after warm-up: {lsh.lsh_status_string(st)} {dd}")
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    for evs in events:
+        for e in evs:
+            e.record(stream)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    clocks = ClockSampler(uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
+    torch.cuda.synchronize()
+    barrier(dist)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t0.record(stream)
+    for k in range(K):
+        bwd(events[k])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms_max = allmax(dist, t0.elapsed_time(t1) / K)
+    stage_names = ("hash", "sort", "attn_bwd")
+    stage_ms = {n: statistics.mean(events[k][i].elapsed_time(events[k][i + 1]) for k in range(K))
+                for i, n in enumerate(stage_names)}
+    st, dd = lsh.lsh_workspace_status(ws)
+    if st != lsh.LSH_OK:
+        raise RuntimeError(f"device check failed: {lsh.lsh_status_string(st)} {dd}")
+    if not (torch.isfinite(dqk).all() and torch.isfinite(dv).all()):
+        raise RuntimeError("non-finite gradients")
+
+    # ---- end to end: H2D of every input, backward, D2H of both gradients
+    h_dqk = torch.empty(dqk.shape, dtype=torch.float32).pin_memory()
+    h_dv = torch.empty(dv.shape, dtype=torch.float32).pin_memory()
+    srcs = (h_qk, h_v, h_R, h_out, h_lse, h_g, h_gl)
+    dsts = (d_qk, d_v, d_R, out, lse, d_g, d_gl)
+
+    def e2e_step():
+        for d_, h_ in zip(dsts, srcs):
+            d_.copy_(h_, non_blocking=True)
+        bwd()
+        h_dqk.copy_(dqk, non_blocking=True)
+        h_dv.copy_(dv, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(dist)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = allmax(dist, e0.elapsed_time(e1) / K)
+    barrier(dist)
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    value = job_value(w.tokens, world, ms_max)
+    peaks, peak_src = load_peaks()
+    wk = work_backward(w)
+    unit_c = COMPUTE_UNIT[w.dtype]
+    peak_c = peaks["bf16_tflops"] if unit_c == "tensor" else FP32_ALU_TFLOPS
+    kernels = {n: kernel_roof(w, n, stage_ms[n], wk[n], unit_c, peak_c, peaks, peak_src)
+               for n in stage_names}
+    # the attention backward runs on the CUDA cores' fp32 lanes: its share of those too
+    kb = kernels["attn_bwd"]
+    kb["alu_frac"] = kb["algorithmic_flops"] / (kb["ms"] / 1e3) / 1e12 / FP32_ALU_TFLOPS
+    dom = max(stage_ms, key=stage_ms.get)
+    F = sum(k["flops"] for k in wk.values())
+    Bts = sum(k["bytes"] for k in wk.values())
+    t_roof = max(F / (peaks["bf16_tflops"] * 1e12), Bts / (peaks["hbm_gbs"] * 1e9))
+    # kernels per call: the forward's hash and sort launches plus the backward kernel
+    # (the forward's count less its attention and combination, plus one)
+    launches = int(lib.lsh_attn_kernel_launches(w.B, w.H, w.L, w.d, w.n_buckets, w.n_rounds,
+                                                w.chunk, dt_code)) - 1
+    line = {
+        "metric": METRIC_BWD, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": Wm, "ms_per_step": ms_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "pass": "backward",
+        "config": dict(config_of(w), parallelism=f"replicas{world}",
+                       l2="inputs larger than L2: qk, v, out, g_out, dqk, dv "
+                          f"{w.tokens * w.d * (2 * (2 if w.dtype == 'bf16' else 4) + 16) / 2**20:.0f} MiB "
+                          "> L2 126 MiB; no flush"),
+        "roofline": kernels[dom],
+        "kernels": kernels,
+        "path_roofline": {"flops": F, "bytes": Bts, "t_roof_ms": 1e3 * t_roof,
+                          "frac": 1e3 * t_roof / ms_max, "peaks": peak_src},
+        "e2e": {"value": w.tokens * world / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(sum(t.nbytes for t in srcs)),
+                "d2h_bytes_per_step": int(h_dqk.nbytes + h_dv.nbytes), "ms_per_step": e2e_ms},
+        "clocks": clk,
+        "gpu_launches": launches * K,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        tok, times, used, desc = time_oracle_backward(w, steps=1)
+        line["cpu_baseline"] = {"value": tok / times[0], "unit": "tokens/s", "cores": used,
+                                "kind": "oracle", "sample": desc}
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     from lsh_attention_04_b300 import inputs as gen
     ap = argparse.ArgumentParser(description=__doc__)
@@ -426,6 +634,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=gen.HEADLINE, choices=sorted(gen.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pass", dest="pass_", choices=("forward", "backward"), default="forward",
+                    help="time the forward pass (default) or the backward pass")
     ap.add_argument("--heads", type=int, default=0,
                     help="run the workload with this many heads instead (small ncu captures); "
                          "the printed line then names the reduced workload")
@@ -436,6 +646,8 @@ def main():
         w = w.replace(H=args.heads, name=w.name.replace(f"_H{w.H}_", f"_H{args.heads}_"))
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.pass_ == "backward":
+        return run_backward(args, w)
     return run_ours(args, w)
 
 

@@ -158,6 +158,20 @@ lsh_status_t lsh_attn_backward(const void *qk, const void *v, const void *R, lsh
                                void *stream);
 
 /*
+ * lsh_attn_backward that also records four caller-created CUDA events (cudaEvent_t) on
+ * `stream`: stage_events[0] before the hash, [1] before the sort, [2] before the backward
+ * kernel and [3] after it (the clearing of dqk and dv comes before [0]).  A NULL array or
+ * event is LSH_ERR_INVALID_ARGUMENT.
+ */
+lsh_status_t lsh_attn_backward_timed(const void *qk, const void *v, const void *R,
+                                     lsh_dtype_t dtype, int B, int H, int L, int d,
+                                     int n_buckets, int n_rounds, int chunk, int causal,
+                                     float scale, const float *out, const float *lse,
+                                     const float *g_out, const float *g_lse, float *dqk,
+                                     float *dv, void *workspace, size_t workspace_bytes,
+                                     void *stream, void *const *stage_events);
+
+/*
  * Number of kernels one lsh_attn_forward call launches for this problem (0 when the
  * arguments are invalid or unsupported).  The workspace status clear is a memset, not
  * a kernel, and is not counted.

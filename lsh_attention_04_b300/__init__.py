@@ -33,7 +33,7 @@ EXPORTS = (
     "lsh_bucket_sort_workspace_bytes", "lsh_bucket_sort", "lsh_chunk_attn_workspace_bytes",
     "lsh_chunk_attn", "lsh_unsort_combine", "lsh_workspace_status", "lsh_attn_forward_timed",
     "lsh_attn_kernel_launches", "lsh_bucket_sort_noalloc", "lsh_selftest_wait_timeout",
-    "lsh_attn_backward_workspace_bytes", "lsh_attn_backward",
+    "lsh_attn_backward_workspace_bytes", "lsh_attn_backward", "lsh_attn_backward_timed",
 )
 
 _lib = None
@@ -86,6 +86,8 @@ def load():
     lib.lsh_attn_backward_workspace_bytes.restype = S
     lib.lsh_attn_backward.argtypes = [P, P, P, I] + [I] * 8 + [F, P, P, P, P, P, P, P, S, P]
     lib.lsh_attn_backward.restype = I
+    lib.lsh_attn_backward_timed.argtypes = [P, P, P, I] + [I] * 8 + [F, P, P, P, P, P, P, P, S, P, P]
+    lib.lsh_attn_backward_timed.restype = I
     lib.lsh_selftest_wait_timeout.argtypes = [P, S, P]
     lib.lsh_selftest_wait_timeout.restype = I
     _lib = lib
@@ -230,6 +232,26 @@ def lsh_attn_backward(qk, v, R, n_buckets, chunk, causal, scale, out, lse, g_out
                                     None if g_lse is None else _ptr(g_lse), _ptr(dqk), _ptr(dv),
                                     _ptr(ws), ws.numel(), _stream(stream)),
            "lsh_attn_backward")
+    return dqk, dv
+
+
+def lsh_attn_backward_timed(qk, v, R, n_buckets, chunk, causal, scale, out, lse, g_out, g_lse,
+                            dqk, dv, ws, events, stream=None):
+    """lsh_attn_backward recording four torch.cuda.Event objects at the stage boundaries
+    (before hash, sort, backward kernel, and after it)."""
+    B, H, L, d = qk.shape
+    s = _stream(stream)
+    handles = (ctypes.c_void_p * 4)()
+    for k, ev in enumerate(events):
+        if ev.cuda_event == 0:  # torch creates the event on its first record
+            ev.record()
+        handles[k] = ev.cuda_event
+    _check(load().lsh_attn_backward_timed(_ptr(qk), _ptr(v), _ptr(R), _dtype_code(qk), B, H, L,
+                                          d, n_buckets, R.shape[0], chunk, int(causal),
+                                          float(scale), _ptr(out), _ptr(lse), _ptr(g_out),
+                                          None if g_lse is None else _ptr(g_lse), _ptr(dqk),
+                                          _ptr(dv), _ptr(ws), ws.numel(), s, handles),
+           "lsh_attn_backward_timed")
     return dqk, dv
 
 

@@ -187,6 +187,46 @@ lsh_status_t forward(const void *qk, const void *v, const void *R, lsh_dtype_t d
     return record(events, 4, st);
 }
 
+// The backward pass; `events`, when not null, are recorded before the hash, the sort and
+// the backward kernel, and after it.
+lsh_status_t backward(const void *qk, const void *v, const void *R, lsh_dtype_t dtype, int B,
+                      int H, int L, int d, int n_buckets, int n_rounds, int chunk, int causal,
+                      float scale, const float *out, const float *lse, const float *g_out,
+                      const float *g_lse, float *dqk, float *dv, void *workspace,
+                      size_t workspace_bytes, void *stream, void *const *events)
+{
+    const Problem p = make_problem(B, H, L, d, n_buckets, n_rounds, chunk, causal, scale, dtype);
+    lsh_status_t s = validate(p);
+    if (s != LSH_OK) return s;
+    if (!qk || !v || !R || !out || !lse || !g_out || !dqk || !dv || !workspace)
+        return LSH_ERR_INVALID_ARGUMENT;
+    if (((uintptr_t)workspace) % 256 != 0) return LSH_ERR_INVALID_ARGUMENT;
+    const Layout w = layout(p, false);
+    if (workspace_bytes < w.total) return LSH_ERR_WORKSPACE_TOO_SMALL;
+    cudaStream_t st = (cudaStream_t)stream;
+    int32_t *buckets = at<int32_t>(workspace, w.buckets);
+    float *inv_norm = at<float>(workspace, w.inv_norm);
+    int32_t *perm = at<int32_t>(workspace, w.perm);
+    const size_t grad_bytes = sizeof(float) * (size_t)p.n_tok() * p.d;
+    if ((s = clear_status(workspace, st)) != LSH_OK) return s;
+    if ((s = cuda_status(cudaMemsetAsync(dqk, 0, grad_bytes, st))) != LSH_OK) return s;
+    if ((s = cuda_status(cudaMemsetAsync(dv, 0, grad_bytes, st))) != LSH_OK) return s;
+    if ((s = record(events, 0, st)) != LSH_OK) return s;
+    // the same deterministic kernels as the forward pass: the same buckets and order
+    if ((s = run_hash(p, qk, R, buckets, inv_norm, workspace, at<void>(workspace, w.rpack), st)) != LSH_OK)
+        return s;
+    if ((s = record(events, 1, st)) != LSH_OK) return s;
+    if ((s = cuda_status(sort_launch(p, buckets, perm, at<int32_t>(workspace, w.inv),
+                                     at<int32_t>(workspace, w.bstart),
+                                     at<int32_t>(workspace, w.counts), st))) != LSH_OK)
+        return s;
+    if ((s = record(events, 2, st)) != LSH_OK) return s;
+    if ((s = cuda_status(attn_bwd(p, qk, v, buckets, perm, inv_norm, out, lse, g_out, g_lse, dqk,
+                                  dv, st))) != LSH_OK)
+        return s;
+    return record(events, 3, st);
+}
+
 }  // namespace
 
 extern "C" {
@@ -229,31 +269,23 @@ lsh_status_t lsh_attn_backward(const void *qk, const void *v, const void *R, lsh
                                float *dqk, float *dv, void *workspace, size_t workspace_bytes,
                                void *stream)
 {
-    const Problem p = make_problem(B, H, L, d, n_buckets, n_rounds, chunk, causal, scale, dtype);
-    lsh_status_t s = validate(p);
-    if (s != LSH_OK) return s;
-    if (!qk || !v || !R || !out || !lse || !g_out || !dqk || !dv || !workspace)
-        return LSH_ERR_INVALID_ARGUMENT;
-    if (((uintptr_t)workspace) % 256 != 0) return LSH_ERR_INVALID_ARGUMENT;
-    const Layout w = layout(p, false);
-    if (workspace_bytes < w.total) return LSH_ERR_WORKSPACE_TOO_SMALL;
-    cudaStream_t st = (cudaStream_t)stream;
-    int32_t *buckets = at<int32_t>(workspace, w.buckets);
-    float *inv_norm = at<float>(workspace, w.inv_norm);
-    int32_t *perm = at<int32_t>(workspace, w.perm);
-    const size_t grad_bytes = sizeof(float) * (size_t)p.n_tok() * p.d;
-    if ((s = clear_status(workspace, st)) != LSH_OK) return s;
-    if ((s = cuda_status(cudaMemsetAsync(dqk, 0, grad_bytes, st))) != LSH_OK) return s;
-    if ((s = cuda_status(cudaMemsetAsync(dv, 0, grad_bytes, st))) != LSH_OK) return s;
-    // the same deterministic kernels as the forward pass: the same buckets and order
-    if ((s = run_hash(p, qk, R, buckets, inv_norm, workspace, at<void>(workspace, w.rpack), st)) != LSH_OK)
-        return s;
-    if ((s = cuda_status(sort_launch(p, buckets, perm, at<int32_t>(workspace, w.inv),
-                                     at<int32_t>(workspace, w.bstart),
-                                     at<int32_t>(workspace, w.counts), st))) != LSH_OK)
-        return s;
-    return cuda_status(attn_bwd(p, qk, v, buckets, perm, inv_norm, out, lse, g_out, g_lse, dqk,
-                                dv, st));
+    return backward(qk, v, R, dtype, B, H, L, d, n_buckets, n_rounds, chunk, causal, scale, out,
+                    lse, g_out, g_lse, dqk, dv, workspace, workspace_bytes, stream, nullptr);
+}
+
+lsh_status_t lsh_attn_backward_timed(const void *qk, const void *v, const void *R,
+                                     lsh_dtype_t dtype, int B, int H, int L, int d,
+                                     int n_buckets, int n_rounds, int chunk, int causal,
+                                     float scale, const float *out, const float *lse,
+                                     const float *g_out, const float *g_lse, float *dqk,
+                                     float *dv, void *workspace, size_t workspace_bytes,
+                                     void *stream, void *const *stage_events)
+{
+    if (!stage_events) return LSH_ERR_INVALID_ARGUMENT;
+    for (int i = 0; i < 4; ++i)
+        if (!stage_events[i]) return LSH_ERR_INVALID_ARGUMENT;
+    return backward(qk, v, R, dtype, B, H, L, d, n_buckets, n_rounds, chunk, causal, scale, out,
+                    lse, g_out, g_lse, dqk, dv, workspace, workspace_bytes, stream, stage_events);
 }
 
 int lsh_attn_kernel_launches(int B, int H, int L, int d, int n_buckets, int n_rounds, int chunk,

@@ -203,3 +203,13 @@ def _bwd(lib, **kw):
 @no_device
 def test_backward_validation(lib, kw, expect):
     assert _bwd(lib, **kw) == expect
+
+
+@no_device
+def test_backward_timed_needs_four_events(lib):
+    P = ctypes.c_void_p
+    ev = (ctypes.c_void_p * 4)(1, 1, 0, 1)
+    args = [P(1), P(1), P(1), lsh.LSH_BF16, 1, 1, 1024, 64, 32, 1, 64, 1, ctypes.c_float(0.125),
+            P(1), P(1), P(1), None, P(1), P(1), P(256), 1 << 30, None]
+    assert lib.lsh_attn_backward_timed(*args, None) == lsh.LSH_ERR_INVALID_ARGUMENT
+    assert lib.lsh_attn_backward_timed(*args, ev) == lsh.LSH_ERR_INVALID_ARGUMENT

@@ -39,6 +39,20 @@ def test_work_model_long_text_totals():
     assert t_f > 0 and t_b > 0
 
 
+def test_work_model_backward_totals():
+    """Backward at the long-text shape: the hash and sort as in the forward pass, then five
+    window contractions per token and round (20 c d flops) in the attention backward."""
+    w = gen.WORKLOADS[gen.HEADLINE]
+    wk = bench.work_backward(w)
+    assert set(wk) == {"hash", "sort", "attn_bwd"}
+    fwd = bench.work(w)
+    assert wk["hash"] == fwd["hash"] and wk["sort"] == fwd["sort"]
+    N = 8 * 65536
+    assert wk["attn_bwd"]["flops"] == 20 * N * 8 * 64 * 128 == 687_194_767_360
+    # qk, v bf16; out, g_out, dqk, dv fp32; lse, g_lse, inverse norms; buckets, perm
+    assert wk["attn_bwd"]["bytes"] == N * (2 * 128 * 2 + 4 * 128 * 4 + 3 * 4 + 2 * 8 * 4)
+
+
 def test_recorded_traffic_needs_unchanged_sources(tmp_path, monkeypatch):
     rec = {"wl": {"attn": {"bytes_per_launch": 123, "source_sha1": bench.source_digest("attn")}}}
     f = tmp_path / "traffic.json"
