@@ -205,6 +205,9 @@ lsh_status_t lsh_hash(const void *qk, const void *R, lsh_dtype_t dtype, int B, i
  * Step 2, stable sort of each (b, h, r) segment by bucket (ai-scholar.tech article,
  * "LSH attention": sort each LSH bucket; modulabs-hub: "ordering" the bucketed
  * keys).  Ties keep position order.  Writes perm, inv and bstart (layouts above).
+ * Every bucket id must lie in [0, n_buckets).  An id outside that range is skipped:
+ * its token gets no sorted slot, so perm, inv and bstart are then undefined, but no
+ * memory outside them is written.
  */
 size_t lsh_bucket_sort_workspace_bytes(int B, int H, int L, int n_buckets, int n_rounds);
 lsh_status_t lsh_bucket_sort(const int32_t *buckets, int B, int H, int L, int n_buckets,

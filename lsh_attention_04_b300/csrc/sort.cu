@@ -34,7 +34,10 @@ sort_count_kernel(const int32_t *__restrict__ buckets, int L, int nb, int tiles,
     const int32_t *keys = buckets + seg * L;
     const int lo = tile * kSortTile;
     const int hi = min(L, lo + kSortTile);
-    for (int i = lo + threadIdx.x; i < hi; i += blockDim.x) atomicAdd(&hist[keys[i]], 1);
+    for (int i = lo + threadIdx.x; i < hi; i += blockDim.x) {
+        const int k = keys[i];
+        if ((unsigned)k < (unsigned)nb) atomicAdd(&hist[k], 1);   // ids outside [0, nb) skipped
+    }
     __syncthreads();
     int32_t *c = counts + (size_t)seg * nb * tiles;
     for (int b = threadIdx.x; b < nb; b += blockDim.x) c[(size_t)b * tiles + tile] = hist[b];
@@ -106,7 +109,8 @@ sort_scatter_kernel(const int32_t *__restrict__ buckets, const int32_t *__restri
     // pass 1: per-warp counts
     for (int it = 0; it < kKeysPerWarp / 32; ++it) {
         const int pos = wlo + it * 32 + lane;
-        const int key = pos < L ? keys[pos] : -1;
+        int key = pos < L ? keys[pos] : -1;
+        if (key >= nb) key = -1;
         const unsigned peers = __match_any_sync(0xffffffffu, key);
         if (key >= 0 && (peers & lt) == 0) hist[key] += __popc(peers);
     }
@@ -129,7 +133,8 @@ sort_scatter_kernel(const int32_t *__restrict__ buckets, const int32_t *__restri
     int32_t *I = inv + seg * L;
     for (int it = 0; it < kKeysPerWarp / 32; ++it) {
         const int pos = wlo + it * 32 + lane;
-        const int key = pos < L ? keys[pos] : -1;
+        int key = pos < L ? keys[pos] : -1;
+        if (key >= nb) key = -1;
         const unsigned peers = __match_any_sync(0xffffffffu, key);
         int base = 0;
         if (key >= 0) base = hist[key];

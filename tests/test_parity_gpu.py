@@ -105,9 +105,11 @@ def test_hash_parity(w):
     assert np.allclose(got, ref, rtol=2e-6, atol=0)
 
 
+# Tile counts from 1 to 18 per segment, 1 to 2048 buckets, heavy and light buckets.
 SORT_CASES = [
     (6, 1344, 64, 1.0), (2, 8256, 128, 1.0), (4, 65536, 1024, 1.0), (3, 4096, 1, 1.0),
     (2, 64, 2048, 1.0), (4, 12288, 192, 0.05), (5, 1000, 7, 0.3), (1, 4097, 2, 1.0),
+    (2, 65536, 16, 0.02), (1, 70000, 64, 1.0), (1, 65536, 2048, 1.0),
 ]
 
 
