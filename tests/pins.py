@@ -506,4 +506,48 @@ def pin_backward_matches_autograd_of_the_multiset_softmax(orc):
         assert np.allclose(dv[0], vv.grad.numpy(), rtol=1e-9, atol=1e-10)
 
 
+
+def pin_backward_zero_key_gets_no_key_gradient(orc):
+    """A zero row of qk has inverse norm 0 (reading R2): as a key it scores 0 whatever the
+    query, so it gets no gradient through its key role, while its query and value roles
+    still get theirs.  torch autograd of the dense multiset softmax, with the unit keys
+    built from a guarded inverse norm (0 for the zero row), must match the oracle."""
+    rng = _rng(19)
+    L, d, nb, c, n_rounds, scale = 32, 8, 2, 8, 2, 0.7
+    qk = rng.standard_normal((L, d))
+    qk[5] = 0.0
+    qk[20] = 0.0
+    v = rng.standard_normal((L, d))
+    R = rng.standard_normal((n_rounds, d, nb // 2))
+    g_out = rng.standard_normal((L, d))
+    g_lse = rng.standard_normal(L)
+    _, _, it = orc.forward(qk[None], v[None], R, nb, c, False, scale, intermediates=True)
+    count = np.zeros((L, L))
+    n_self = np.zeros(L)
+    for r in range(n_rounds):
+        for i in range(L):
+            cands = _brute_candidates(it["bucket"][0, r], i, c, False)
+            count[i, cands] += 1
+            n_self[i] += not cands
+    assert count[:, 5].sum() > 0 and count[5].sum() > 0   # the zero row plays both roles
+    eye = torch.eye(L, dtype=torch.bool)
+    logc = torch.from_numpy(np.where(count > 0, np.log(np.maximum(count, 1)), -np.inf))
+    diag = torch.from_numpy(np.where(n_self > 0, orc.SELF_LOGIT + np.log(np.maximum(n_self, 1)),
+                                     -np.inf))
+    q = torch.tensor(qk, requires_grad=True)
+    vv = torch.tensor(v, requires_grad=True)
+    norm = q.norm(dim=-1, keepdim=True)
+    inv = torch.where(norm > 0, 1.0 / torch.where(norm > 0, norm, torch.ones_like(norm)),
+                      torch.zeros_like(norm))
+    logits = torch.where(eye, diag[:, None].expand(L, L), (q @ (q * inv).T) * scale + logc)
+    out = torch.softmax(logits, dim=-1) @ vv
+    lse = torch.logsumexp(logits, dim=-1)
+    ((torch.from_numpy(g_out) * out).sum() + (torch.from_numpy(g_lse) * lse).sum()).backward()
+    dqk, dv = orc.backward(qk[None], v[None], R, nb, c, False, scale, g_out[None], g_lse[None])
+    assert np.all(np.isfinite(q.grad.numpy()))
+    assert np.allclose(dqk[0], q.grad.numpy(), rtol=1e-9, atol=1e-10)
+    assert np.allclose(dv[0], vv.grad.numpy(), rtol=1e-9, atol=1e-10)
+    assert np.abs(dqk[0, 5]).max() > 0          # its query role still has a gradient
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -51,6 +51,7 @@ MUTANTS = [
      "dkhat[(size_t)i * d + c] += ds * scale * kj[c];"),
     ("bwd_attend_dv_at_query", "dv[(size_t)j * d + c] += p * gs[c];", "dv[(size_t)i * d + c] += p * gs[c];"),
     ("bwd_attend_self_row_dropped", "for (int c = 0; c < d; ++c) dv[(size_t)i * d + c] += gs[c];", ""),
+    ("inv_norm_unguarded", "inv_norm[j] = s > 0.0 ? 1.0 / sqrt(s) : 0.0;", "inv_norm[j] = 1.0 / sqrt(s);"),
     ("bwd_key_norm_jacobian_dropped", "inv_norm[j] * (g[c] - x[c] * inv_norm[j] * proj)",
      "inv_norm[j] * g[c]"),
 ]
