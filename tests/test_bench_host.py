@@ -82,3 +82,21 @@ def test_binding_refuses_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(lsh, "_lib", None, raising=False)
     with pytest.raises(OSError):
         lsh.load()
+
+
+def test_reference_arm_times_the_oracle_backward(capsys, monkeypatch):
+    """--impl reference --pass backward on rank 0: the oracle's backward pass on a bounded
+    sample, printed as one JSON line with the backward metric and a one-core baseline."""
+    monkeypatch.setenv("RANK", "0")
+    w = gen.Workload("tiny_bf16_B1_H1_L256_d64_R2", 1, 1, 256, 64, "bf16", 8, 2, 64, True, 4, 3)
+
+    class A:
+        gpus, steps, warmup, pass_ = 1, 1, 0, "backward"
+
+    assert bench.run_reference(A, w) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC_BWD
+    assert line["value"] > 0 and line["cpu_baseline"]["cores"] == 1
+    assert line["cpu_baseline"]["value"] == line["value"]
+    assert "backward" in line["cpu_baseline"]["sample"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
