@@ -140,7 +140,11 @@ size_t lsh_attn_backward_workspace_bytes(int B, int H, int L, int d, int n_bucke
  * one entry of a single softmax with weight exp(s_ij - lse_i), which is why `out` and
  * `lse` from the forward are all that is kept of it.
  *   qk, v, R  as given to lsh_attn_forward (same dtype, sizes, causal and scale)
- *   out, lse  fp32 [B][H][L][d] and [B][H][L]: that call's outputs
+ *   out, lse  fp32 [B][H][L][d] and [B][H][L]: that call's outputs, unchanged.  lse
+ *             must be the forward's own combined lse: the kernel uses it as the softmax
+ *             normaliser of every (round, candidate) weight, and it reads a value below
+ *             -5e4 (half the self logit) as "no key in any round".  A recomputed or
+ *             shifted lse gives wrong gradients without an error.
  *   g_out     fp32 [B][H][L][d]: the loss's gradient in out
  *   g_lse     fp32 [B][H][L]: the loss's gradient in lse, or NULL for zero
  *   dqk, dv   fp32 [B][H][L][d]: overwritten with the gradients in qk and v
@@ -227,6 +231,9 @@ lsh_status_t lsh_bucket_sort(const int32_t *buckets, int B, int H, int L, int n_
  *    corrupt each other; order them on one stream.
  *  - The first call on a device looks the array's address up with that device
  *    current; make it before any stream capture, with the stream's device current.
+ *    The address is kept for the life of the process: after cudaDeviceReset (or any
+ *    teardown of the device's primary context) this entry point must not be called
+ *    again on that device.
  *  - Allocates nothing and takes no workspace.
  */
 lsh_status_t lsh_bucket_sort_noalloc(const int32_t *buckets, int B, int H, int L, int n_buckets,
@@ -257,6 +264,9 @@ lsh_status_t lsh_chunk_attn(const void *qk, const void *v, lsh_dtype_t dtype,
  * Steps 5-6, un-sort and combine rounds: for token i,
  * lse_i = logsumexp_r lse_r[inv_r[i]] and out_i = sum_r exp(lse_r[inv_r[i]] - lse_i)
  * o_r[inv_r[i]].  o_r is bf16 when dtype is LSH_BF16 and fp32 when LSH_F32.
+ * Every inv entry must lie in [0, L), as lsh_bucket_sort writes it.  An entry outside
+ * that range is replaced by 0 (no read leaves the round's rows); that token's results
+ * are then meaningless.
  */
 lsh_status_t lsh_unsort_combine(const void *o_r, const float *lse_r, const int32_t *inv,
                                 lsh_dtype_t dtype, int B, int H, int L, int d, int n_rounds,

@@ -24,6 +24,10 @@ namespace {
 constexpr int kWarps = 8;
 constexpr int kRowsInFlight = 8;
 
+// A caller's inverse-permutation entry as a row index: entries outside [0, L) (a
+// corrupt or foreign inv) are replaced by 0, so no read leaves the round's rows.
+__device__ __forceinline__ int safe_row(int s, int L) { return (unsigned)s < (unsigned)L ? s : 0; }
+
 template <int EPL>
 __device__ __forceinline__ void load_row(const float *p, float (&x)[EPL]) {
     if constexpr (EPL == 4) {
@@ -68,7 +72,7 @@ combine_kernel(const T *__restrict__ o_r, const float *__restrict__ lse_r,
         const int r = r0 + lane;
         if (r < n_rounds) {
             const size_t base = (seg0 + r) * L;
-            mx = fmaxf(mx, __ldg(lse_r + base + (token_order ? i : __ldg(inv + base + i))));
+            mx = fmaxf(mx, __ldg(lse_r + base + (token_order ? i : safe_row(__ldg(inv + base + i), L))));
         }
     }
     mx = warp_max(mx);
@@ -82,7 +86,7 @@ combine_kernel(const T *__restrict__ o_r, const float *__restrict__ lse_r,
         float w = 0.f;
         if (r < n_rounds) {
             const size_t base = (seg0 + r) * L;
-            s = token_order ? i : __ldg(inv + base + i);
+            s = token_order ? i : safe_row(__ldg(inv + base + i), L);
             w = expf(__ldg(lse_r + base + s) - mx);
         }
         sum += warp_sum(w);

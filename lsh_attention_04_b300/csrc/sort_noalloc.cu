@@ -21,7 +21,10 @@
 //    kernel writes every entry the later kernels read.
 //  - The first call on a device looks up the array's device address
 //    (cudaGetSymbolAddress) with that device current; make that first call before any
-//    stream capture, with the device that owns `stream` current.
+//    stream capture, with the device that owns `stream` current.  The address is
+//    cached for the life of the process, so after cudaDeviceReset (or any teardown of
+//    the device's primary context) this entry point must not be called again on that
+//    device: the cached address would no longer belong to a live allocation.
 //  - No cudaMalloc, cudaFree or other allocating routine is called.
 #include <mutex>
 
