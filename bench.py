@@ -217,17 +217,55 @@ def oracle_sample(w, max_tokens=32768):
     return sub, qk, v, R, desc
 
 
-def time_oracle(w, threads, steps=1, max_tokens=32768):
+def cpu_model():
+    """The host CPU's model name from /proc/cpuinfo (None where unavailable)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith("model name"):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
+
+
+def time_oracle(w, threads, steps=1, max_tokens=32768, keep=None):
+    """Time the oracle's forward pass on a bounded sample of w.  With ``keep`` (a dict),
+    the last run's inputs and per-round buckets and margins are stored in it."""
     import oracle
     sub, qk, v, R, desc = oracle_sample(w, max_tokens)
     oracle.build()
     times = []
     for _ in range(steps):
         t0 = time.perf_counter()
-        oracle.forward(qk, v, R, sub.n_buckets, sub.chunk, sub.causal, sub.scale, threads=threads)
+        res = oracle.forward(qk, v, R, sub.n_buckets, sub.chunk, sub.causal, sub.scale,
+                             threads=threads, intermediates=keep is not None)
         times.append(time.perf_counter() - t0)
+    if keep is not None:
+        keep.update(sub=sub, qk=qk, R=R, bucket=res[2]["bucket"], margin=res[2]["margin"])
     used = min(threads, sub.B * sub.H * sub.n_rounds)
     return sub.tokens, times, used, desc
+
+
+def near_tie_report(lsh, dev, keep, band=1e-5):
+    """Bucket mismatches between the GPU hash and the oracle's buckets of the CPU-baseline
+    sample (the same input values on both sides).  A mismatch is allowed only where the
+    oracle's top-1/top-2 margin is below band * |x| * |R| (|R| = largest column 2-norm of
+    R_r); the line reports both counts."""
+    import torch
+    sub = keep["sub"]
+    tdt = torch.bfloat16 if sub.dtype == "bf16" else torch.float32
+    d_qk = torch.from_numpy(keep["qk"]).to(dev).to(tdt).contiguous()
+    d_R = torch.from_numpy(keep["R"]).to(dev).to(tdt).contiguous()
+    b, _ = lsh.lsh_hash(d_qk, d_R, sub.n_buckets)
+    gb = b.cpu().numpy().reshape(keep["bucket"].shape)
+    bad = gb != keep["bucket"]
+    xn = np.linalg.norm(keep["qk"].reshape(-1, sub.d).astype(np.float64), axis=1)
+    rn = np.linalg.norm(keep["R"].astype(np.float64), axis=1).max(axis=1)
+    lim = band * xn.reshape(sub.B, sub.H, 1, sub.L) * rn.reshape(1, 1, -1, 1)
+    return {"buckets_compared": int(gb.size), "mismatches": int(bad.sum()),
+            "outside_band": int((bad & ~(keep["margin"] < lim)).sum()),
+            "band": f"{band:g}*|x|*|R|", "sample": "the cpu_baseline sample"}
 
 
 def time_oracle_backward(w, steps=1, max_tokens=4096):
@@ -307,7 +345,7 @@ def run_reference(args, w):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_of(w),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": used, "kind": "oracle",
-                         "sample": desc},
+                         "cpu_model": cpu_model(), "sample": desc},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -436,7 +474,8 @@ def run_ours(args, w):
 
     F = sum(k["flops"] for k in wk.values())
     Bts = sum(k["bytes"] for k in wk.values())
-    t_roof = max(F / (peaks["bf16_tflops"] * 1e12), Bts / (peaks["hbm_gbs"] * 1e9))
+    # the same compute peak as the per-kernel entries: tensor for bf16, fp32 lanes for f32
+    t_roof = max(F / (peak_c * 1e12), Bts / (peaks["hbm_gbs"] * 1e9))
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -459,9 +498,11 @@ def run_ours(args, w):
     }
     if not args.no_cpu_baseline and world == 1:
         threads = os.cpu_count() or 1
-        tok, times, used, desc = time_oracle(w, threads, steps=1)
+        keep = {}
+        tok, times, used, desc = time_oracle(w, threads, steps=1, keep=keep)
         line["cpu_baseline"] = {"value": tok / times[0], "unit": "tokens/s", "cores": used,
-                                "kind": "oracle", "sample": desc}
+                                "cpu_model": cpu_model(), "kind": "oracle", "sample": desc}
+        line["near_ties"] = near_tie_report(lsh, dev, keep)
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -591,7 +632,7 @@ def run_backward(args, w):
     dom = max(stage_ms, key=stage_ms.get)
     F = sum(k["flops"] for k in wk.values())
     Bts = sum(k["bytes"] for k in wk.values())
-    t_roof = max(F / (peaks["bf16_tflops"] * 1e12), Bts / (peaks["hbm_gbs"] * 1e9))
+    t_roof = max(F / (peak_c * 1e12), Bts / (peaks["hbm_gbs"] * 1e9))
     # kernels per call: the forward's hash and sort launches plus the backward kernel
     # (the forward's count less its attention and combination, plus one)
     launches = int(lib.lsh_attn_kernel_launches(w.B, w.H, w.L, w.d, w.n_buckets, w.n_rounds,
@@ -618,7 +659,7 @@ def run_backward(args, w):
     if not args.no_cpu_baseline and world == 1:
         tok, times, used, desc = time_oracle_backward(w, steps=1)
         line["cpu_baseline"] = {"value": tok / times[0], "unit": "tokens/s", "cores": used,
-                                "kind": "oracle", "sample": desc}
+                                "cpu_model": cpu_model(), "kind": "oracle", "sample": desc}
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

@@ -15,6 +15,17 @@ TOL_OUT = {"bf16": 2e-2, "f32": 1e-4}
 NEAR_TIE = 1e-5
 SELF_LOGIT = -1.0e5
 
+#: Near-tie bucket mismatches per test case: {case: (mismatches, buckets compared)}.
+#: Printed as a table at the end of the pytest run (tests/conftest.py).
+NEAR_TIES: dict = {}
+
+
+def record_near_ties(case, n_bad, n_total):
+    """Count a case's near-tie bucket mismatches (all already checked to lie inside the
+    near-tie band) for the end-of-run report."""
+    bad, tot = NEAR_TIES.get(case, (0, 0))
+    NEAR_TIES[case] = (bad + int(n_bad), tot + int(n_total))
+
 
 def torch_dtype(name):
     import torch
