@@ -362,7 +362,8 @@ def test_self_only_tokens():
 
 
 def _antiparallel_inputs(w, m2_lo, m2_hi):
-    """qk for the softmax-bound cases: one bucket (R = 0), and every row a signed copy
+    """qk for the softmax-bound cases: one bucket (R = 0: every projection is 0, so every
+    token takes bucket 0), and every row a signed copy
     of one direction u with a little noise, the sign alternating from chunk to chunk.
     The first row of each chunk then sees, causally, only the previous chunk: keys
     pointing the other way, all scoring about -|scale| |q|.  Row norms are spread so
@@ -388,10 +389,10 @@ def _antiparallel_inputs(w, m2_lo, m2_hi):
 BOUND_CASES = [
     # bound path with its smallest weights (2^-64 at m2 = 32) and the exact-maximum
     # path around the first threshold (64), where the bound would flush every weight
-    (W("bound_bf16_m2_20_32", 1, 2, 1024, 64, "bf16", 2, 2, 64, True, 0, 41), 20.0, 32.0),
-    (W("bound_bf16_m2_58_68", 1, 4, 1024, 64, "bf16", 2, 2, 64, True, 0, 42), 58.0, 68.0),
-    (W("bound_bf16_m2_58_68_d128", 1, 4, 1024, 128, "bf16", 2, 1, 64, True, 0, 45), 58.0, 68.0),
-    (W("bound_bf16_m2_55_70_d128_noncausal", 1, 1, 1024, 128, "bf16", 2, 1, 64, False, 0, 43),
+    (W("bound_bf16_m2_20_32", 1, 2, 1024, 64, "bf16", 16, 2, 64, True, 0, 41), 20.0, 32.0),
+    (W("bound_bf16_m2_58_68", 1, 4, 1024, 64, "bf16", 16, 2, 64, True, 0, 42), 58.0, 68.0),
+    (W("bound_bf16_m2_58_68_d128", 1, 4, 1024, 128, "bf16", 16, 1, 64, True, 0, 45), 58.0, 68.0),
+    (W("bound_bf16_m2_55_70_d128_noncausal", 1, 1, 1024, 128, "bf16", 16, 1, 64, False, 0, 43),
      55.0, 70.0),
     (W("bound_f32_m2_55_70", 1, 2, 1024, 64, "f32", 2, 2, 64, True, 0, 44), 55.0, 70.0),
 ]
