@@ -17,21 +17,21 @@
 //  * Persistent CTAs: ctas_per_group CTAs per group walk the 128-token tiles in the same
 //    order, so the CTAs of all groups read a tile of qk within a short time window and
 //    only the first one fetches it from HBM (the others hit L2).
-//  * Warp roles (24 warps, 64 registers): warp 16 issues TMA loads of the qk tile (2-D
-//    tensor map, 128-byte swizzle, 2-4 stages) and owns TMEM; warps 18-21 issue
-//    tcgen05.mma M=128 x N=chunk x K=16 into four 128-column TMEM accumulators, warp 18+b
-//    owning accumulator b (each a whole warp, one lane elected per instruction); warps
-//    0-15 are four epilogue warpgroups that read the projections with tcgen05.ld and keep,
-//    per token and round, the entry of largest magnitude (first index on ties); warp 17
-//    computes 1/|x| of each token from the staged tile (first group only); warps 22-23
-//    only pad the block to a multiple of 4 warps (equal register caps per scheduler).
+//  * Warp roles (12 warps): warp 8 issues TMA loads of the qk tile (2-D tensor map,
+//    128-byte swizzle, 2-4 stages) and owns TMEM; warps 10-11 issue tcgen05.mma
+//    M=128 x N=chunk x K=16 (each a whole warp, one lane elected per instruction); warps
+//    0-7 are two epilogue warpgroups that read the projections with tcgen05.ld and keep,
+//    per token and round, the entry of largest magnitude (first index on ties); warp 9
+//    computes 1/|x| of each token from the staged tile (first group only).
+//  * Four 128-column TMEM accumulators, two per epilogue warpgroup: warpgroup e and its
+//    MMA warp 10 + e take the tiles it % 2 == e and alternate the tile's chunks between
+//    accumulators 2e and 2e + 1, so the warpgroup scans one chunk while the next one is
+//    being computed (a single accumulator per warpgroup left it waiting for every
+//    refill), and it sees each round whole.
 //  * Bucket rule: the largest entry of [p, -p] is the entry of p with the largest |p_j|,
 //    taken with its sign: bucket = j if p_j >= 0, n_buckets/2 + j otherwise.  Scanning j
 //    in order with a strict comparison keeps the first index.  Two entries of equal
 //    magnitude and opposite sign have a zero top-1/top-2 margin, i.e. they are a near-tie.
-//  * Tile `it` of a CTA goes to epilogue warpgroup it % 4 and accumulator it % 4: the
-//    group reads every chunk of it (so it sees each round whole) and four tiles are in
-//    flight, their MMAs running while other groups scan.
 // Every wait is bounded (see sm100::wait); on a timeout the kernel records the place in
 // the workspace status block and winds down.
 #include <math.h>
@@ -49,15 +49,14 @@ constexpr int kTmemBufs = 4;         // accumulators: 4 x 128 TMEM columns
 constexpr int kRCapBytes = 128 * 1024;
 constexpr int kMaxXStages = 4;         // qk tile stages (as many as shared memory holds)
 constexpr size_t kSmemCap = 227 * 1024;
-constexpr int kMmaWarps = kTmemBufs; // one MMA-issuing warp per accumulator
-constexpr int kEpiGroups = kTmemBufs; // epilogue warpgroups, one accumulator each
+constexpr int kEpiGroups = 2;         // epilogue warpgroups, two accumulators each
+constexpr int kMmaWarps = kEpiGroups; // one MMA-issuing warp per epilogue warpgroup
 constexpr int kEpiWarps = 4 * kEpiGroups;
 constexpr int kProdWarp = kEpiWarps;      // producer (also the TMEM owner)
 constexpr int kNormWarp = kEpiWarps + 1;  // 1 / |x|
-constexpr int kMma0 = kEpiWarps + 2;      // MMA issuers kMma0 .. kMma0 + 3
-// 22 working warps, padded to 24: with a multiple of 4 warps every scheduler holds the
-// same number of warps, so the per-thread register cap is 65536 / 768 rounded down.
-constexpr int kThreads = 24 * 32;
+constexpr int kMma0 = kEpiWarps + 2;      // MMA issuers kMma0 .. kMma0 + 1
+// 12 warps: a multiple of 4, so every scheduler holds the same number of warps
+constexpr int kThreads = 12 * 32;
 
 struct HashPlan {
     long long n_tok;
@@ -246,10 +245,10 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
             wait(&sb.r_full, 0, &dummy, status, 0x103);
         }
     } else if (warp >= kMma0 && warp < kMma0 + kMmaWarps) {
-        // ---------------- MMA issuers: warp kMma0 + b owns accumulator b ----------------
+        // ---------------- MMA issuers: warp kMma0 + e feeds epilogue warpgroup e ----------
         // Each issuer is a whole converged warp (the MMA wrappers elect one lane).  Tile
-        // `it` belongs to epilogue warpgroup it % 4 and accumulator it % 4, whose issuer
-        // runs all the tile's chunks through it in order; four tiles are in flight.
+        // `it` belongs to warpgroup it % 2; its chunks alternate between the warpgroup's
+        // accumulators 2e and 2e + 1 (use u of the warpgroup goes to 2e + u % 2).
         {
             const int mi = warp - kMma0;
             bool ok = wait_w(&sb.r_full, 0, abort_flag, status, 0x201);
@@ -264,7 +263,8 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
                 if (it % kEpiGroups == mi) {
                     for (int k = 0; k < nch; ++k) {
                         const int use = (it / kEpiGroups) * nch + k;
-                        if (!(ok = wait_w(&sb.tm_empty[mi], (use & 1) ^ 1, abort_flag, status, 0x203))) break;
+                        const int b = 2 * mi + (use & 1);
+                        if (!(ok = wait_w(&sb.tm_empty[b], ((use >> 1) & 1) ^ 1, abort_flag, status, 0x203))) break;
                         fence_after_sync();
                         const int width = chunk_width(P, nr, k);
                         const uint32_t idesc = idesc_bf16(kTileM, width, 0, 0);
@@ -273,9 +273,9 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
                             const int kb = ks >> 2, ko = (ks & 3) * 32;
                             const uint64_t a = smem_desc(xs + s * x_bytes + kb * kTileM * 128 + ko, 16, 1024);
                             const uint64_t bd = smem_desc(rbase + kb * width * 128 + ko, 16, 1024);
-                            mma_ss(tmem + mi * kChunkMax, a, bd, idesc, ks > 0);
+                            mma_ss(tmem + b * kChunkMax, a, bd, idesc, ks > 0);
                         }
-                        mma_commit(smem_u32(&sb.tm_full[mi]));
+                        mma_commit(smem_u32(&sb.tm_full[b]));
                         touched = true;
                     }
                 }
@@ -324,10 +324,9 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
             }
         }
     } else if (warp < kEpiWarps) {
-        // ---------------- epilogue warpgroups: warpgroup e takes the tiles it % 4 == e ------
-        // It sees every chunk of its tile (in its own accumulator e), hence every round
-        // whole: no merging between warpgroups.  Four warpgroups keep four epilogue warps
-        // on every scheduler to hide each other's latencies.
+        // ---------------- epilogue warpgroups: warpgroup e takes the tiles it % 2 == e ------
+        // It sees every chunk of its tile (alternately in its accumulators 2e, 2e + 1),
+        // hence every round whole: no merging between warpgroups.
         const int e = warp >> 2, q = warp & 3;
         const int row = q * 32 + lane;
         const uint32_t tlane0 = tmem + ((uint32_t)(q * 32) << 16);
@@ -341,10 +340,10 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
             float best = 0.f;
             int bidx = 0;
             for (int k = 0; k < nch; ++k) {
-                const int buf = e;
                 const int use = (it / kEpiGroups) * nch + k;
+                const int buf = 2 * e + (use & 1);
                 const uint32_t tlane = tlane0 + buf * kChunkMax;
-                bool w = wait(&sb.tm_full[buf], use & 1, abort_flag, status, 0x401);
+                bool w = wait(&sb.tm_full[buf], (use >> 1) & 1, abort_flag, status, 0x401);
                 if (!(ok = __all_sync(0xffffffffu, w))) break;
                 fence_after_sync();
                 const int width = chunk_width(P, nr, k);
@@ -352,8 +351,7 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
                 int rr, jj;
                 if (P.split) { rr = k / P.cpr; jj = kChunkMax * (k % P.cpr); }
                 else { const int col = chunk_col0(P, k); rr = col / P.hp; jj = col - rr * P.hp; }
-                // 32-column batches, one at a time (four epilogue warps per scheduler hide
-                // each other's tcgen05.ld latency); the accumulator goes back to its MMA
+                // 32-column batches, one at a time; the accumulator goes back to its MMA
                 // warp as soon as its last batch is in registers.
                 const int nbat = width / 32;
                 for (int q2 = 0; q2 < nbat; ++q2) {
