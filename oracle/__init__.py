@@ -20,6 +20,11 @@ Each function follows the Reformer pages:
   * backward -- gradients of the forward in qk and v by the chain rule, buckets
                 held fixed (the pages train by back-propagation but print no
                 gradient formula; modulabs-hub notes, "Introduction")
+  * knn      -- LSH bucketing as approximate nearest-neighbour search: the k
+                most cosine-similar tokens among the union of the rounds'
+                candidate sets ("Reformer" glossary, "Atencion LSH", the
+                paragraph after the algorithm); exact_knn is the exhaustive
+                search it is measured against
 """
 from __future__ import annotations
 
@@ -98,6 +103,10 @@ class Oracle:
         lib.oracle_backward.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, i32, f64,
                                         P, P, P, P]
         lib.oracle_backward.restype = ctypes.c_int
+        lib.oracle_knn.argtypes = [P, i32, i32, P, P, P, i32, i32, i32, P, i32, P, P]
+        lib.oracle_knn.restype = None
+        lib.oracle_exact_knn.argtypes = [P, i32, i32, i32, P, i32, P, P]
+        lib.oracle_exact_knn.restype = None
         lib.oracle_self_logit.argtypes = []
         lib.oracle_self_logit.restype = f64
         self.lib = lib
@@ -189,6 +198,38 @@ class Oracle:
         lib.oracle_combine(_p(o_r), _p(lse_r), _p(inv), R, L, d, _p(tokens), len(tokens),
                            _p(out), _p(lse))
         return out, lse
+
+    def knn(self, x, bucket, perm, inv, chunk, k, tokens=None):
+        """Approximate k nearest neighbours of one head from its LSH buckets.
+
+        x [L, d]; bucket, perm, inv [n_rounds, L] of one head.  Returns (idx [n, k] int32,
+        sim [n, k]) for ``tokens`` (all when None): the k most cosine-similar tokens of the
+        union of the rounds' non-causal candidate sets, ties to the smaller index, padded
+        with -1 / -2.
+        """
+        x = _f64(x)
+        L, d = x.shape
+        bucket, perm, inv = _i32(bucket), _i32(perm), _i32(inv)
+        n_rounds = bucket.shape[0]
+        tok = None if tokens is None else _i32(tokens)
+        n = L if tok is None else len(tok)
+        idx = np.empty((n, k), np.int32)
+        sim = np.empty((n, k), np.float64)
+        self.lib.oracle_knn(_p(x), L, d, _p(bucket), _p(perm), _p(inv), n_rounds, chunk, k,
+                            _p(tok), 0 if tok is None else n, _p(idx), _p(sim))
+        return idx, sim
+
+    def exact_knn(self, x, k, tokens=None):
+        """Exact k nearest neighbours by cosine similarity over every other token of x."""
+        x = _f64(x)
+        L, d = x.shape
+        tok = None if tokens is None else _i32(tokens)
+        n = L if tok is None else len(tok)
+        idx = np.empty((n, k), np.int32)
+        sim = np.empty((n, k), np.float64)
+        self.lib.oracle_exact_knn(_p(x), L, d, k, _p(tok), 0 if tok is None else n, _p(idx),
+                                  _p(sim))
+        return idx, sim
 
     def forward(self, qk, v, R, n_buckets, chunk, causal, scale, threads=None, intermediates=False):
         """Full forward pass.  qk, v: [B, H, L, d] (or [n_heads, L, d]); R [n_rounds, d, nb/2].
@@ -364,3 +405,11 @@ def forward(qk, v, R, n_buckets, chunk, causal, scale, threads=None, intermediat
 
 def backward(qk, v, R, n_buckets, chunk, causal, scale, g_out, g_lse):
     return default().backward(qk, v, R, n_buckets, chunk, causal, scale, g_out, g_lse)
+
+
+def knn(x, bucket, perm, inv, chunk, k, tokens=None):
+    return default().knn(x, bucket, perm, inv, chunk, k, tokens)
+
+
+def exact_knn(x, k, tokens=None):
+    return default().exact_knn(x, k, tokens)

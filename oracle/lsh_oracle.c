@@ -214,6 +214,107 @@ void oracle_attend(const double *qk, const double *v, const double *inv_norm,
 }
 
 /* ------------------------------------------------------------------------ */
+/* LSH bucketing as approximate nearest-neighbour search ([U], the paragraph */
+/* after the algorithm: LSH finds most of a query's nearest neighbours at a  */
+/* small fraction of the cost of an exhaustive search).  The candidates of   */
+/* token i are the union over the rounds of its attention candidates without */
+/* causality (same bucket, own chunk or previous chunk, i itself left out).  */
+/* They are ranked by cosine similarity x_i.x_j / (|x_i| |x_j|) (0 when      */
+/* either vector is zero), ties to the smaller j, and the first k are        */
+/* written, a shorter list padded with index -1 and similarity -2.           */
+/* ------------------------------------------------------------------------ */
+static void oracle_top_k(const double *sim, const int32_t *idx, int n, int k,
+                         int32_t *out_idx, double *out_sim)
+{
+    char *taken = (char *)calloc((size_t)(n > 0 ? n : 1), 1);
+    for (int a = 0; a < k; ++a) {
+        int b = -1;
+        for (int t = 0; t < n; ++t) {
+            if (taken[t]) continue;
+            if (b < 0 || sim[t] > sim[b] || (sim[t] == sim[b] && idx[t] < idx[b])) b = t;
+        }
+        if (b < 0) {
+            out_idx[a] = -1;
+            out_sim[a] = -2.0;
+            continue;
+        }
+        taken[b] = 1;
+        out_idx[a] = idx[b];
+        out_sim[a] = sim[b];
+    }
+    free(taken);
+}
+
+static double oracle_cosine(const double *x, const double *inv_norm, int d, int i, int j)
+{
+    double dot = 0.0;
+    for (int c = 0; c < d; ++c) dot += x[(size_t)i * d + c] * x[(size_t)j * d + c];
+    return dot * inv_norm[i] * inv_norm[j];
+}
+
+/* bucket, perm, inv: [n_rounds][L] of one head; tokens: the queries (all when NULL);  */
+/* nn_idx, nn_sim: [count][k]                                                          */
+void oracle_knn(const double *x, int L, int d, const int32_t *bucket, const int32_t *perm,
+                const int32_t *inv, int n_rounds, int chunk, int k, const int32_t *tokens,
+                int n_tokens, int32_t *nn_idx, double *nn_sim)
+{
+    double *inv_norm = (double *)malloc(sizeof(double) * (size_t)L);
+    int32_t *cand = (int32_t *)malloc(sizeof(int32_t) * (size_t)(2 * chunk));
+    int32_t *all = (int32_t *)malloc(sizeof(int32_t) * (size_t)(2 * chunk) * (size_t)n_rounds);
+    double *sim = (double *)malloc(sizeof(double) * (size_t)(2 * chunk) * (size_t)n_rounds);
+    int32_t *seen = (int32_t *)malloc(sizeof(int32_t) * (size_t)L);
+    oracle_inv_norm(x, L, d, inv_norm);
+    for (int j = 0; j < L; ++j) seen[j] = -1;
+    int count = tokens ? n_tokens : L;
+    for (int q = 0; q < count; ++q) {
+        int i = tokens ? tokens[q] : q;
+        int n_all = 0;
+        for (int r = 0; r < n_rounds; ++r) {
+            int s = inv[(size_t)r * L + i];
+            int n = oracle_candidates(bucket + (size_t)r * L, perm + (size_t)r * L, L, chunk, 0,
+                                      s, cand);
+            for (int a = 0; a < n; ++a) {
+                int j = cand[a];
+                if (seen[j] != q) { seen[j] = q; all[n_all++] = j; }
+            }
+        }
+        for (int a = 0; a < n_all; ++a) sim[a] = oracle_cosine(x, inv_norm, d, i, all[a]);
+        oracle_top_k(sim, all, n_all, k, nn_idx + (size_t)q * k, nn_sim + (size_t)q * k);
+    }
+    free(inv_norm);
+    free(cand);
+    free(all);
+    free(sim);
+    free(seen);
+}
+
+/* The exact k nearest neighbours by the same similarity and tie rule, over every j != i */
+/* (the reference an approximate search is measured against).                           */
+void oracle_exact_knn(const double *x, int L, int d, int k, const int32_t *tokens, int n_tokens,
+                      int32_t *nn_idx, double *nn_sim)
+{
+    double *inv_norm = (double *)malloc(sizeof(double) * (size_t)L);
+    int32_t *all = (int32_t *)malloc(sizeof(int32_t) * (size_t)L);
+    double *sim = (double *)malloc(sizeof(double) * (size_t)L);
+    oracle_inv_norm(x, L, d, inv_norm);
+    int count = tokens ? n_tokens : L;
+    for (int q = 0; q < count; ++q) {
+        int i = tokens ? tokens[q] : q;
+        int n = 0;
+        for (int j = 0; j < L; ++j) {
+            if (j == i) continue;
+            all[n] = j;
+            sim[n] = oracle_cosine(x, inv_norm, d, i, j);
+            ++n;
+        }
+        oracle_top_k(sim, all, n, k, nn_idx + (size_t)q * k, nn_sim + (size_t)q * k);
+    }
+    free(inv_norm);
+    free(all);
+    free(sim);
+}
+
+/* ------------------------------------------------------------------------ */
 /* Steps 5-6: un-sort each round and combine rounds with logsumexp weights,  */
 /* for the tokens listed in `tokens` (all when NULL).                        */
 /* ------------------------------------------------------------------------ */

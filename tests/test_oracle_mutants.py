@@ -54,6 +54,15 @@ MUTANTS = [
     ("inv_norm_unguarded", "inv_norm[j] = s > 0.0 ? 1.0 / sqrt(s) : 0.0;", "inv_norm[j] = 1.0 / sqrt(s);"),
     ("bwd_key_norm_jacobian_dropped", "inv_norm[j] * (g[c] - x[c] * inv_norm[j] * proj)",
      "inv_norm[j] * g[c]"),
+    ("knn_duplicates_kept", "if (seen[j] != q) { seen[j] = q; all[n_all++] = j; }",
+     "all[n_all++] = j;"),
+    ("knn_causal_window", "L, chunk, 0,\n                                      s, cand);",
+     "L, chunk, 1,\n                                      s, cand);"),
+    ("knn_query_norm_dropped", "return dot * inv_norm[i] * inv_norm[j];", "return dot * inv_norm[j];"),
+    ("knn_ties_to_larger_index", "(sim[t] == sim[b] && idx[t] < idx[b])", "(sim[t] == sim[b] && idx[t] > idx[b])"),
+    ("knn_first_round_only", "for (int r = 0; r < n_rounds; ++r) {\n            int s = inv[(size_t)r * L + i];\n            int n = oracle_candidates(",
+     "for (int r = 0; r < 1; ++r) {\n            int s = inv[(size_t)r * L + i];\n            int n = oracle_candidates("),
+    ("exact_knn_keeps_self", "if (j == i) continue;\n            all[n] = j;", "all[n] = j;"),
 ]
 
 RUNNER = r"""
