@@ -272,6 +272,32 @@ lsh_status_t lsh_unsort_combine(const void *o_r, const float *lse_r, const int32
                                 lsh_dtype_t dtype, int B, int H, int L, int d, int n_rounds,
                                 float *out, float *lse, void *stream);
 
+/* ---------------------------------------------------------------- k-NN search */
+
+/*
+ * LSH bucketing as approximate k-nearest-neighbour search ("Reformer" glossary,
+ * ultralytics.com, section "Atencion LSH", the paragraph after the algorithm: LSH is the
+ * classic approximate nearest-neighbour method and finds most of a query's nearest
+ * neighbours at a fraction of the cost of an exhaustive search).  Steps 1-2 above, then:
+ * the candidates of token i are the union over the rounds of the tokens sharing its
+ * bucket in its chunk window (own chunk in both directions and the previous chunk, i
+ * itself left out); they are ranked by cosine similarity x_i.x_j / (|x_i| |x_j|) (0 when
+ * either vector is zero), ties to the smaller j, and the first k are written.
+ *   qk        [B][H][L][d] dtype;  R [n_rounds][d][n_buckets/2] dtype
+ *   k         1..32, with n_rounds * k <= 256
+ *   nn_idx    int32 [B][H][L][k]: token positions in [0, L), -1 where fewer than k exist
+ *   nn_sim    fp32  [B][H][L][k]: their similarities, descending; -2 beside a -1
+ * Sizes, dtype and chunk follow lsh_attn_forward's rules.  The workspace (device,
+ * 256-byte aligned, caller-owned, lsh_knn_workspace_bytes() bytes) holds the buckets,
+ * the sort and the per-round candidate lists.  Asynchronous on `stream`; returns
+ * argument and launch errors only.
+ */
+size_t lsh_knn_workspace_bytes(int B, int H, int L, int d, int n_buckets, int n_rounds,
+                               int chunk, int k, lsh_dtype_t dtype);
+lsh_status_t lsh_knn(const void *qk, const void *R, lsh_dtype_t dtype, int B, int H, int L,
+                     int d, int n_buckets, int n_rounds, int chunk, int k, int32_t *nn_idx,
+                     float *nn_sim, void *workspace, size_t workspace_bytes, void *stream);
+
 /*
  * Self test of the bounded waits the tensor-core kernels use (the pages have no
  * counterpart: it exists to test this library's failure reporting).  Clears the status

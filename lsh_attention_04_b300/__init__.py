@@ -34,6 +34,7 @@ EXPORTS = (
     "lsh_chunk_attn", "lsh_unsort_combine", "lsh_workspace_status", "lsh_attn_forward_timed",
     "lsh_attn_kernel_launches", "lsh_bucket_sort_noalloc", "lsh_selftest_wait_timeout",
     "lsh_attn_backward_workspace_bytes", "lsh_attn_backward", "lsh_attn_backward_timed",
+    "lsh_knn_workspace_bytes", "lsh_knn",
 )
 
 _lib = None
@@ -78,6 +79,10 @@ def load():
     lib.lsh_chunk_attn_workspace_bytes.restype = S
     lib.lsh_chunk_attn.argtypes = [P, P, I, P, P, P, P] + [I] * 8 + [F, P, P, P, S, P]
     lib.lsh_chunk_attn.restype = I
+    lib.lsh_knn_workspace_bytes.argtypes = [I] * 8 + [I]
+    lib.lsh_knn_workspace_bytes.restype = S
+    lib.lsh_knn.argtypes = [P, P, I] + [I] * 8 + [P, P, P, S, P]
+    lib.lsh_knn.restype = I
     lib.lsh_unsort_combine.argtypes = [P, P, P, I] + [I] * 5 + [P, P, P]
     lib.lsh_unsort_combine.restype = I
     lib.lsh_workspace_status.argtypes = [P, ctypes.POINTER(I), P]
@@ -253,6 +258,32 @@ def lsh_attn_backward_timed(qk, v, R, n_buckets, chunk, causal, scale, out, lse,
                                           _ptr(dv), _ptr(ws), ws.numel(), s, handles),
            "lsh_attn_backward_timed")
     return dqk, dv
+
+
+def lsh_knn(qk, R, n_buckets, chunk, k, nn_idx=None, nn_sim=None, ws=None, stream=None):
+    """LSH bucketing as approximate k-nearest-neighbour search over qk [B, H, L, d] with
+    R [n_rounds, d, n_buckets/2] (same dtype).  Returns (nn_idx int32 [B, H, L, k],
+    nn_sim fp32 [B, H, L, k]): per token the k most cosine-similar tokens of the union of
+    its rounds' bucket-and-chunk-window candidates, padded with (-1, -2)."""
+    torch = _torch()
+    B, H, L, d = qk.shape
+    n_rounds = R.shape[0]
+    dt = _dtype_code(qk)
+    if R.dtype != qk.dtype:
+        raise TypeError("qk and R must share one dtype")
+    if nn_idx is None:
+        nn_idx = torch.empty((B, H, L, k), dtype=torch.int32, device=qk.device)
+    if nn_sim is None:
+        nn_sim = torch.empty((B, H, L, k), dtype=torch.float32, device=qk.device)
+    if ws is None:
+        n = int(load().lsh_knn_workspace_bytes(B, H, L, d, n_buckets, n_rounds, chunk, k, dt))
+        if n == 0:
+            raise LshError(LSH_ERR_INVALID_ARGUMENT, "lsh_knn_workspace_bytes")
+        ws = torch.empty(n, dtype=torch.uint8, device=qk.device)
+    _check(load().lsh_knn(_ptr(qk), _ptr(R), dt, B, H, L, d, n_buckets, n_rounds, chunk, k,
+                          _ptr(nn_idx), _ptr(nn_sim), _ptr(ws), ws.numel(), _stream(stream)),
+           "lsh_knn")
+    return nn_idx, nn_sim
 
 
 def lsh_attn_kernel_launches(B, H, L, d, n_buckets, n_rounds, chunk, dtype_code) -> int:

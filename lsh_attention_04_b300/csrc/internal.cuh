@@ -95,6 +95,12 @@ cudaError_t attn_bwd(const Problem &p, const void *qk, const void *v, const int3
 
 cudaError_t selftest_wait_launch(StatusBlock *status, cudaStream_t st);
 
+// LSH k-nearest-neighbour search: per-round lists (cand_idx, cand_sim: [seg][L][k]), then
+// the merged top k per token (nn_idx, nn_sim: [B][H][L][k])
+cudaError_t knn_launch(const Problem &p, int k, const void *qk, const int32_t *buckets,
+                       const int32_t *perm, const float *inv_norm, int32_t *cand_idx,
+                       float *cand_sim, int32_t *nn_idx, float *nn_sim, cudaStream_t st);
+
 cudaError_t combine_launch(const Problem &p, const void *o_r, const float *lse_r,
                            const int32_t *inv, float *out, float *lse, cudaStream_t st,
                            StatusBlock *status = nullptr);

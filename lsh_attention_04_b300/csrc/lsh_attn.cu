@@ -384,6 +384,70 @@ lsh_status_t lsh_unsort_combine(const void *o_r, const float *lse_r, const int32
     return cuda_status(combine_launch(p, o_r, lse_r, inv, out, lse, (cudaStream_t)stream));
 }
 
+}  // extern "C"
+
+namespace {
+
+// Workspace of the k-nearest-neighbour search: the backward pass's (hash and sort
+// outputs, no per-round attention outputs) followed by the per-round candidate lists.
+struct KnnLayout {
+    Layout base;
+    size_t cand_idx, cand_sim, total;
+};
+
+bool knn_k_ok(int n_rounds, int k) { return k >= 1 && k <= 32 && (long)n_rounds * k <= 256; }
+
+KnnLayout knn_layout(const Problem &p, int k)
+{
+    KnnLayout w;
+    w.base = layout(p, false);
+    const size_t n = (size_t)p.n_seg() * p.L * k;
+    size_t o = w.base.total;
+    w.cand_idx = o; o = align_up(o + sizeof(int32_t) * n);
+    w.cand_sim = o; o = align_up(o + sizeof(float) * n);
+    w.total = o;
+    return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t lsh_knn_workspace_bytes(int B, int H, int L, int d, int n_buckets, int n_rounds, int chunk,
+                               int k, lsh_dtype_t dtype)
+{
+    const Problem p = make_problem(B, H, L, d, n_buckets, n_rounds, chunk, 0, 1.f, dtype);
+    if (validate(p) != LSH_OK || !knn_k_ok(n_rounds, k)) return 0;
+    return knn_layout(p, k).total;
+}
+
+lsh_status_t lsh_knn(const void *qk, const void *R, lsh_dtype_t dtype, int B, int H, int L, int d,
+                     int n_buckets, int n_rounds, int chunk, int k, int32_t *nn_idx, float *nn_sim,
+                     void *workspace, size_t workspace_bytes, void *stream)
+{
+    const Problem p = make_problem(B, H, L, d, n_buckets, n_rounds, chunk, 0, 1.f, dtype);
+    lsh_status_t s = validate(p);
+    if (s != LSH_OK) return s;
+    if (!knn_k_ok(n_rounds, k)) return LSH_ERR_INVALID_ARGUMENT;
+    if (!qk || !R || !nn_idx || !nn_sim || !workspace) return LSH_ERR_INVALID_ARGUMENT;
+    if (((uintptr_t)workspace) % 256 != 0) return LSH_ERR_INVALID_ARGUMENT;
+    const KnnLayout w = knn_layout(p, k);
+    if (workspace_bytes < w.total) return LSH_ERR_WORKSPACE_TOO_SMALL;
+    cudaStream_t st = (cudaStream_t)stream;
+    int32_t *buckets = at<int32_t>(workspace, w.base.buckets);
+    float *inv_norm = at<float>(workspace, w.base.inv_norm);
+    int32_t *perm = at<int32_t>(workspace, w.base.perm);
+    if ((s = clear_status(workspace, st)) != LSH_OK) return s;
+    if ((s = run_hash(p, qk, R, buckets, inv_norm, workspace, at<void>(workspace, w.base.rpack), st)) != LSH_OK)
+        return s;
+    if ((s = cuda_status(sort_launch(p, buckets, perm, at<int32_t>(workspace, w.base.inv),
+                                     at<int32_t>(workspace, w.base.bstart),
+                                     at<int32_t>(workspace, w.base.counts), st))) != LSH_OK)
+        return s;
+    return cuda_status(knn_launch(p, k, qk, buckets, perm, inv_norm, at<int32_t>(workspace, w.cand_idx),
+                                  at<float>(workspace, w.cand_sim), nn_idx, nn_sim, st));
+}
+
 lsh_status_t lsh_selftest_wait_timeout(void *workspace, size_t workspace_bytes, void *stream)
 {
     if (!workspace || workspace_bytes < sizeof(StatusBlock)) return LSH_ERR_INVALID_ARGUMENT;

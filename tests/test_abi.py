@@ -213,3 +213,35 @@ def test_backward_timed_needs_four_events(lib):
             P(1), P(1), P(1), None, P(1), P(1), P(256), 1 << 30, None]
     assert lib.lsh_attn_backward_timed(*args, None) == lsh.LSH_ERR_INVALID_ARGUMENT
     assert lib.lsh_attn_backward_timed(*args, ev) == lsh.LSH_ERR_INVALID_ARGUMENT
+
+
+def test_knn_workspace_sizing(lib):
+    f = lib.lsh_knn_workspace_bytes
+    n = f(1, 8, 65536, 128, 1024, 8, 64, 16, lsh.LSH_BF16)
+    # the per-round candidate lists alone are B*H*R*L*k*(4 + 4) bytes
+    assert n > 1 * 8 * 8 * 65536 * 16 * 8 and n % 256 == 0
+    assert f(1, 1, 1024, 64, 32, 2, 64, 0, lsh.LSH_BF16) == 0      # k < 1
+    assert f(1, 1, 1024, 64, 32, 2, 64, 33, lsh.LSH_BF16) == 0     # k > 32
+    assert f(1, 1, 1024, 64, 32, 16, 64, 32, lsh.LSH_BF16) == 0    # rounds * k > 256
+    assert f(1, 1, 1000, 64, 32, 2, 64, 8, lsh.LSH_BF16) == 0      # L % chunk
+
+
+@no_device
+@pytest.mark.parametrize("kw,expect", [
+    (dict(qk=0), lsh.LSH_ERR_INVALID_ARGUMENT),
+    (dict(idx=0), lsh.LSH_ERR_INVALID_ARGUMENT),
+    (dict(ws=4), lsh.LSH_ERR_INVALID_ARGUMENT),
+    (dict(k=0), lsh.LSH_ERR_INVALID_ARGUMENT),
+    (dict(k=40), lsh.LSH_ERR_INVALID_ARGUMENT),
+    (dict(d=96), lsh.LSH_ERR_UNSUPPORTED),
+    (dict(wsb=256), lsh.LSH_ERR_WORKSPACE_TOO_SMALL),
+])
+def test_knn_argument_checks(lib, kw, expect):
+    a = dict(qk=1, R=1, dtype=lsh.LSH_BF16, B=1, H=1, L=1024, d=64, nb=32, R_=2, chunk=64, k=8,
+             idx=1, sim=1, ws=256, wsb=1 << 30)
+    a.update(kw)
+    P = ctypes.c_void_p
+    st = lib.lsh_knn(P(a["qk"]), P(a["R"]), a["dtype"], a["B"], a["H"], a["L"], a["d"], a["nb"],
+                     a["R_"], a["chunk"], a["k"], P(a["idx"]), P(a["sim"]), P(a["ws"]), a["wsb"],
+                     None)
+    assert st == expect
