@@ -30,7 +30,8 @@ namespace {
 
 using namespace nvcuda;
 
-constexpr int kKnnWarps = 4;
+constexpr int kKnnWarps = 8;
+constexpr int kRowsInFlight = 4;       // rows a warp selects for at once (independent chains)
 constexpr int kWinMax = 128;           // window rows: two chunks of at most 64
 constexpr int kSPitch = kWinMax + 4;   // fp32 similarity tile row pitch
 
@@ -38,24 +39,51 @@ template <typename T> struct XRow;
 template <> struct XRow<__nv_bfloat16> { static constexpr int pad = 8; };   // 16-byte rows for wmma
 template <> struct XRow<float> { static constexpr int pad = 1; };           // odd pitch: no bank conflicts
 
-// Best untaken (largest similarity, then smallest index) among a lane's NE entries,
-// then across the warp.  Returns the winner's index (INT_MAX when every entry is taken).
-template <int NE>
-__device__ __forceinline__ int warp_best(const float (&sim)[NE], const int (&idx)[NE],
-                                         const bool (&live)[NE], float &best) {
-    float bs = -INFINITY;
-    int bj = INT_MAX;
+// k best (largest similarity, then smallest index) of Q independent lists held across a
+// warp, lane-major: list q has entries sim[q][m], idx[q][m], live[q][m] on every lane.
+// k rounds of a warp-wide argmax; the Q lists' shuffle chains are independent, so they
+// overlap.  Lane a < k ends with entry a of each list in out_idx[q], out_sim[q] (-1, -2
+// when the list has fewer than k live entries).  Every copy of a winner's index retires.
+template <int Q, int NE>
+__device__ __forceinline__ void warp_top_k(const float (&sim)[Q][NE], const int (&idx)[Q][NE],
+                                           bool (&live)[Q][NE], int k, int lane,
+                                           int (&out_idx)[Q], float (&out_sim)[Q]) {
 #pragma unroll
-    for (int m = 0; m < NE; ++m)
-        if (live[m] && (sim[m] > bs || (sim[m] == bs && idx[m] < bj))) { bs = sim[m]; bj = idx[m]; }
+    for (int q = 0; q < Q; ++q) { out_idx[q] = -1; out_sim[q] = -2.f; }
+    for (int a = 0; a < k; ++a) {
+        float bs[Q];
+        int bj[Q];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float os = __shfl_xor_sync(0xffffffffu, bs, off);
-        const int oj = __shfl_xor_sync(0xffffffffu, bj, off);
-        if (os > bs || (os == bs && oj < bj)) { bs = os; bj = oj; }
+        for (int q = 0; q < Q; ++q) {
+            bs[q] = -INFINITY;
+            bj[q] = INT_MAX;
+#pragma unroll
+            for (int m = 0; m < NE; ++m)
+                if (live[q][m] && (sim[q][m] > bs[q] || (sim[q][m] == bs[q] && idx[q][m] < bj[q]))) {
+                    bs[q] = sim[q][m];
+                    bj[q] = idx[q][m];
+                }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+#pragma unroll
+            for (int q = 0; q < Q; ++q) {
+                const float os = __shfl_xor_sync(0xffffffffu, bs[q], off);
+                const int oj = __shfl_xor_sync(0xffffffffu, bj[q], off);
+                if (os > bs[q] || (os == bs[q] && oj < bj[q])) { bs[q] = os; bj[q] = oj; }
+            }
+        }
+        bool any = false;
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+            if (bj[q] == INT_MAX) continue;          // this list has run out
+            any = true;
+            if (lane == a) { out_idx[q] = bj[q]; out_sim[q] = bs[q]; }
+#pragma unroll
+            for (int m = 0; m < NE; ++m) live[q][m] = live[q][m] && idx[q][m] != bj[q];
+        }
+        if (!any) break;                             // warp-uniform: every list ran out
     }
-    best = bs;
-    return bj;
 }
 
 template <typename T, int D>
@@ -146,79 +174,87 @@ knn_round_kernel(const T *__restrict__ qk, const int32_t *__restrict__ buckets,
     }
     __syncthreads();
 
-    // ---- per row: the k best same-bucket candidates of the window (self left out)
-    for (int r = warp; r < chunk; r += kKnnWarps) {
-        const int ws = r0 + r;
-        const int bs_ = sb[ws];
-        const float ns = sn[ws];
-        float sim[kWinMax / 32];
-        int idx[kWinMax / 32];
-        bool live[kWinMax / 32];
+    // ---- per row: the k best same-bucket candidates of the window (self left out),
+    // kRowsInFlight rows of a warp at once
+    constexpr int NE = kWinMax / 32;
+    for (int rb = warp * kRowsInFlight; rb < chunk; rb += kKnnWarps * kRowsInFlight) {
+        float sim[kRowsInFlight][NE];
+        int idx[kRowsInFlight][NE];
+        bool live[kRowsInFlight][NE];
 #pragma unroll
-        for (int m = 0; m < kWinMax / 32; ++m) {
-            const int w = lane + 32 * m;
-            live[m] = w < n_win && w != ws && sb[w] == bs_;
-            sim[m] = live[m] ? S[r * kSPitch + w] * ns * sn[w] : -INFINITY;
-            idx[m] = live[m] ? sj[w] : INT_MAX;
-        }
-        int my_idx = -1;
-        float my_sim = -2.f;
-        for (int a = 0; a < k; ++a) {
-            float best;
-            const int bj = warp_best(sim, idx, live, best);
-            if (bj == INT_MAX) break;                    // no candidate left
-            if (lane == a) { my_idx = bj; my_sim = best; }
+        for (int q = 0; q < kRowsInFlight; ++q) {
+            const int r = rb + q;
+            const bool row_ok = r < chunk;
+            const int ws = r0 + (row_ok ? r : 0);
+            const int bs_ = sb[ws];
+            const float ns = sn[ws];
 #pragma unroll
-            for (int m = 0; m < kWinMax / 32; ++m) live[m] = live[m] && idx[m] != bj;
+            for (int m = 0; m < NE; ++m) {
+                const int w = lane + 32 * m;
+                live[q][m] = row_ok && w < n_win && w != ws && sb[w] == bs_;
+                sim[q][m] = live[q][m] ? S[r * kSPitch + w] * ns * sn[w] : -INFINITY;
+                idx[q][m] = live[q][m] ? sj[w] : INT_MAX;
+            }
         }
+        int out_idx[kRowsInFlight];
+        float out_sim[kRowsInFlight];
+        warp_top_k(sim, idx, live, k, lane, out_idx, out_sim);
         if (lane < k) {
-            const size_t o = ((size_t)seg * L + sj[ws]) * k + lane;
-            cand_idx[o] = my_idx;
-            cand_sim[o] = my_sim;
+#pragma unroll
+            for (int q = 0; q < kRowsInFlight; ++q) {
+                const int r = rb + q;
+                if (r >= chunk) break;
+                const size_t o = ((size_t)seg * L + sj[r0 + r]) * k + lane;
+                cand_idx[o] = out_idx[q];
+                cand_sim[o] = out_sim[q];
+            }
         }
     }
 }
 
-template <int NE>
+// NE entries per lane; a warp merges Q tokens at once
+template <int NE, int Q>
 __global__ void __launch_bounds__(256)
 knn_merge_kernel(const int32_t *__restrict__ cand_idx, const float *__restrict__ cand_sim,
                  long n_tok, int L, int n_rounds, int k, int32_t *__restrict__ nn_idx,
                  float *__restrict__ nn_sim)
 {
-    const long tok = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const long tok0 = ((long)blockIdx.x * 8 + (threadIdx.x >> 5)) * Q;
     const int lane = threadIdx.x & 31;
-    if (tok >= n_tok) return;
-    const long bh = tok / L, l = tok % L;
+    if (tok0 >= n_tok) return;
     const int n_e = n_rounds * k;
-    float sim[NE];
-    int idx[NE];
-    bool live[NE];
+    float sim[Q][NE];
+    int idx[Q][NE];
+    bool live[Q][NE];
 #pragma unroll
-    for (int m = 0; m < NE; ++m) {
-        const int e = lane + 32 * m;
-        live[m] = false;
-        sim[m] = -INFINITY;
-        idx[m] = INT_MAX;
-        if (e < n_e) {
-            const int r = e / k, a = e % k;
-            const size_t o = (((size_t)bh * n_rounds + r) * L + l) * k + a;
-            const int j = cand_idx[o];
-            if (j >= 0) { live[m] = true; idx[m] = j; sim[m] = cand_sim[o]; }
+    for (int q = 0; q < Q; ++q) {
+        const long tok = tok0 + q;
+        const long bh = tok / L, l = tok % L;
+#pragma unroll
+        for (int m = 0; m < NE; ++m) {
+            const int e = lane + 32 * m;
+            live[q][m] = false;
+            sim[q][m] = -INFINITY;
+            idx[q][m] = INT_MAX;
+            if (tok < n_tok && e < n_e) {
+                const int r = e / k, a = e % k;
+                const size_t o = (((size_t)bh * n_rounds + r) * L + l) * k + a;
+                const int j = cand_idx[o];
+                if (j >= 0) { live[q][m] = true; idx[q][m] = j; sim[q][m] = cand_sim[o]; }
+            }
         }
     }
-    int my_idx = -1;
-    float my_sim = -2.f;
-    for (int a = 0; a < k; ++a) {
-        float best;
-        const int bj = warp_best(sim, idx, live, best);
-        if (bj == INT_MAX) break;
-        if (lane == a) { my_idx = bj; my_sim = best; }
-#pragma unroll
-        for (int m = 0; m < NE; ++m) live[m] = live[m] && idx[m] != bj;   // every copy retires
-    }
+    int out_idx[Q];
+    float out_sim[Q];
+    warp_top_k(sim, idx, live, k, lane, out_idx, out_sim);
     if (lane < k) {
-        nn_idx[(size_t)tok * k + lane] = my_idx;
-        nn_sim[(size_t)tok * k + lane] = my_sim;
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+            const long tok = tok0 + q;
+            if (tok >= n_tok) break;
+            nn_idx[(size_t)tok * k + lane] = out_idx[q];
+            nn_sim[(size_t)tok * k + lane] = out_sim[q];
+        }
     }
 }
 
@@ -253,16 +289,16 @@ cudaError_t knn_launch(const Problem &p, int k, const void *qk, const int32_t *b
                       : launch_round<float, 128>(p, k, qk, buckets, perm, inv_norm, cand_idx, cand_sim, st);
     if (e != cudaSuccess) return e;
     const long n = p.n_tok();
-    const unsigned grid = (unsigned)((n + 7) / 8);
+    const unsigned g4 = (unsigned)((n + 31) / 32), g2 = (unsigned)((n + 15) / 16);
     const int ne = (p.n_rounds * k + 31) / 32;
     if (ne <= 1)
-        knn_merge_kernel<1><<<grid, 256, 0, st>>>(cand_idx, cand_sim, n, p.L, p.n_rounds, k, nn_idx, nn_sim);
+        knn_merge_kernel<1, 4><<<g4, 256, 0, st>>>(cand_idx, cand_sim, n, p.L, p.n_rounds, k, nn_idx, nn_sim);
     else if (ne <= 2)
-        knn_merge_kernel<2><<<grid, 256, 0, st>>>(cand_idx, cand_sim, n, p.L, p.n_rounds, k, nn_idx, nn_sim);
+        knn_merge_kernel<2, 4><<<g4, 256, 0, st>>>(cand_idx, cand_sim, n, p.L, p.n_rounds, k, nn_idx, nn_sim);
     else if (ne <= 4)
-        knn_merge_kernel<4><<<grid, 256, 0, st>>>(cand_idx, cand_sim, n, p.L, p.n_rounds, k, nn_idx, nn_sim);
+        knn_merge_kernel<4, 4><<<g4, 256, 0, st>>>(cand_idx, cand_sim, n, p.L, p.n_rounds, k, nn_idx, nn_sim);
     else
-        knn_merge_kernel<8><<<grid, 256, 0, st>>>(cand_idx, cand_sim, n, p.L, p.n_rounds, k, nn_idx, nn_sim);
+        knn_merge_kernel<8, 2><<<g2, 256, 0, st>>>(cand_idx, cand_sim, n, p.L, p.n_rounds, k, nn_idx, nn_sim);
     return cudaGetLastError();
 }
 
