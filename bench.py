@@ -31,6 +31,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "LSH-attention fwd tokens/s (B·H·L per sec) at L=64K, 8 rounds; % of roofline"
 METRIC_BWD = "LSH-attention bwd tokens/s (B·H·L per sec) at L=64K, 8 rounds: dqk, dv"
+METRIC_KNN = "LSH approximate k-NN tokens/s (B·H·L per sec) at L=64K, 8 rounds, k=16; recall@k"
+KNN_K = 16
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 L2_BYTES = 126 * 2 ** 20
@@ -331,6 +333,12 @@ def run_reference(args, w):
     if args.pass_ == "backward":
         max_tokens = 4096 if n <= 10 else max(2 * w.chunk, 4096 * 10 // n)
         tokens, times, used, desc = time_oracle_backward(w, steps=n, max_tokens=max_tokens)
+    elif args.pass_ == "knn":
+        max_tokens = 8192 if n <= 10 else max(2 * w.chunk, 8192 * 10 // n)
+        times, used = [], 1
+        for _ in range(n):
+            tokens, t, desc = time_oracle_knn(w, KNN_K, max_tokens)
+            times.append(t)
     else:
         max_tokens = 32768 if n <= 40 else max(2 * w.chunk, 32768 * 40 // n)
         tokens, times, used, desc = time_oracle(w, threads, steps=n, max_tokens=max_tokens)
@@ -338,7 +346,8 @@ def run_reference(args, w):
     t = sum(timed) / len(timed)
     value = tokens / t
     line = {
-        "impl": "reference", "metric": METRIC_BWD if args.pass_ == "backward" else METRIC,
+        "impl": "reference",
+        "metric": {"backward": METRIC_BWD, "knn": METRIC_KNN}.get(args.pass_, METRIC),
         "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * t, "higher_is_better": True, "scaling": "weak",
@@ -666,6 +675,171 @@ def run_backward(args, w):
     return 0
 
 
+def work_knn(w, k):
+    """Algorithmic FLOPs and bytes of one lsh_knn call: the hash and sort, then per chunk
+    the c x 2c similarity tile (4 c d flops per token and round) over window rows
+    gathered once per chunk (own and previous chunk: 2 d e bytes per token and round),
+    per-round lists written and read back, and the final lists written."""
+    N, R, d, c = w.tokens, w.n_rounds, w.d, w.chunk
+    e = 2 if w.dtype == "bf16" else 4
+    base = work(w)
+    return {"hash": base["hash"], "sort": base["sort"],
+            "knn": dict(flops=4 * N * R * c * d,
+                        bytes=2 * N * R * d * e + N * R * 12 + 2 * N * R * k * 8 + N * k * 8)}
+
+
+def run_knn(args, w):
+    """LSH approximate k-nearest-neighbour search (lsh_knn) at workload w's shape: K timed
+    calls on device-resident qk and R, recall@k of 512 sampled queries against an
+    exhaustive cosine search of the same head (numpy on the host), end-to-end calls from
+    pinned host buffers, and the oracle's search on a bounded sample as CPU baseline."""
+    import torch
+    import lsh_attention_04_b300 as lsh
+    from lsh_attention_04_b300 import inputs as gen
+
+    world, rank, local, dist = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lib = lsh.load()
+    dt_code = lsh.LSH_BF16 if w.dtype == "bf16" else lsh.LSH_F32
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    k = KNN_K
+    qk, _, R = gen.make_inputs(w, seed=w.seed + 7919 * rank)
+    h_qk = torch.from_numpy(qk).to(tdt).pin_memory()
+    h_R = torch.from_numpy(R).to(tdt).pin_memory()
+    d_qk, d_R = h_qk.to(dev), h_R.to(dev)
+    nn_idx = torch.empty((w.B, w.H, w.L, k), dtype=torch.int32, device=dev)
+    nn_sim = torch.empty((w.B, w.H, w.L, k), dtype=torch.float32, device=dev)
+    n_ws = int(lib.lsh_knn_workspace_bytes(w.B, w.H, w.L, w.d, w.n_buckets, w.n_rounds, w.chunk,
+                                           k, dt_code))
+    ws = torch.empty(n_ws, dtype=torch.uint8, device=dev)
+    K, Wm = args.steps, args.warmup
+
+    def call():
+        lsh.lsh_knn(d_qk, d_R, w.n_buckets, w.chunk, k, nn_idx, nn_sim, ws)
+
+    for _ in range(Wm):
+        call()
+    torch.cuda.synchronize()
+    st, dd = lsh.lsh_workspace_status(ws)
+    if st != lsh.LSH_OK:
+        raise RuntimeError(f"device check failed after warm-up: {lsh.lsh_status_string(st)} {dd}")
+    stream = torch.cuda.current_stream(dev)
+    uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    clocks = ClockSampler(uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier(dist)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t0.record(stream)
+    for _ in range(K):
+        call()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms_max = allmax(dist, t0.elapsed_time(t1) / K)
+
+    # recall@k of sampled queries against an exhaustive search of the same head
+    rng = np.random.default_rng(w.seed)
+    heads = qk.reshape(-1, w.L, w.d).astype(np.float64)
+    got = nn_idx.cpu().numpy().reshape(-1, w.L, k)
+    hits = []
+    for h in rng.choice(len(heads), size=min(2, len(heads)), replace=False):
+        x = heads[h]
+        nrm = np.linalg.norm(x, axis=1)
+        xn = x / np.where(nrm > 0, nrm, 1.0)[:, None]
+        for t in rng.choice(w.L, size=256, replace=False):
+            sim = xn @ xn[t]
+            sim[t] = -np.inf
+            top = np.lexsort((np.arange(w.L), -sim))[:k]
+            hits.append(len(set(top.tolist()) & set(got[h, t].tolist())) / k)
+
+    # end to end: H2D of qk and R, the search, D2H of both lists
+    h_idx = torch.empty(nn_idx.shape, dtype=torch.int32).pin_memory()
+    h_sim = torch.empty(nn_sim.shape, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        d_qk.copy_(h_qk, non_blocking=True)
+        d_R.copy_(h_R, non_blocking=True)
+        call()
+        h_idx.copy_(nn_idx, non_blocking=True)
+        h_sim.copy_(nn_sim, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = allmax(dist, e0.elapsed_time(e1) / K)
+    barrier(dist)
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_src = load_peaks()
+    wk = work_knn(w, k)
+    F = sum(x["flops"] for x in wk.values())
+    Bts = sum(x["bytes"] for x in wk.values())
+    t_roof = max(F / (peaks["bf16_tflops"] * 1e12), Bts / (peaks["hbm_gbs"] * 1e9))
+    line = {
+        "metric": METRIC_KNN, "value": job_value(w.tokens, world, ms_max), "unit": "tokens/s",
+        "n_gpus": world, "steps": K, "warmup": Wm, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic", "pass": "knn",
+        "config": dict(config_of(w), k=k, parallelism=f"replicas{world}",
+                       l2="inputs and per-round lists larger than L2; no flush"),
+        "recall": {"at_k": k, "value": float(np.mean(hits)), "queries": len(hits),
+                   "against": "exhaustive cosine search of the same head (numpy, host)"},
+        "roofline": {"bound": "tensor" if F / (peaks["bf16_tflops"] * 1e12) > Bts / (peaks["hbm_gbs"] * 1e9) else "hbm",
+                     "kernel": "whole call (hash, sort, similarity tiles, selection, merge)",
+                     "t_roof_ms": 1e3 * t_roof, "frac": 1e3 * t_roof / ms_max,
+                     "algorithmic_flops": F, "algorithmic_bytes": Bts, "peaks": peak_src,
+                     "traffic": None},
+        "e2e": {"value": w.tokens * world / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(h_qk.nbytes + h_R.nbytes),
+                "d2h_bytes_per_step": int(h_idx.nbytes + h_sim.nbytes), "ms_per_step": e2e_ms},
+        "clocks": clk,
+        # the forward's hash and sort launches, then the round and merge kernels in place
+        # of the attention and combination (the same count)
+        "gpu_launches": int(lib.lsh_attn_kernel_launches(w.B, w.H, w.L, w.d, w.n_buckets,
+                                                         w.n_rounds, w.chunk, dt_code)) * K,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        tok, tsec, desc = time_oracle_knn(w, k)
+        line["cpu_baseline"] = {"value": tok / tsec, "unit": "tokens/s", "cores": 1,
+                                "cpu_model": cpu_model(), "kind": "oracle", "sample": desc}
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def time_oracle_knn(w, k, max_tokens=8192):
+    """The oracle's search on a bounded sample: head 0, the first max_tokens tokens, all
+    rounds (its hash and sort included), one thread."""
+    import oracle
+    sub, qk, v, R, desc = oracle_sample(w, max_tokens)
+    oracle.build()
+    x = qk.reshape(-1, sub.L, sub.d)[0].astype(np.float64)
+    t0 = time.perf_counter()
+    b = np.empty((sub.n_rounds, sub.L), np.int32)
+    p, iv = np.empty_like(b), np.empty_like(b)
+    for r in range(sub.n_rounds):
+        b[r], _ = oracle.hash(x, R[r], sub.n_buckets)
+        p[r], iv[r], _ = oracle.sort(b[r], sub.n_buckets)
+    oracle.knn(x, b, p, iv, sub.chunk, k)
+    return sub.tokens, time.perf_counter() - t0, desc + f"; k-NN search, k = {k}"
+
+
 def main():
     from lsh_attention_04_b300 import inputs as gen
     ap = argparse.ArgumentParser(description=__doc__)
@@ -675,8 +849,9 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=gen.HEADLINE, choices=sorted(gen.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--pass", dest="pass_", choices=("forward", "backward"), default="forward",
-                    help="time the forward pass (default) or the backward pass")
+    ap.add_argument("--pass", dest="pass_", choices=("forward", "backward", "knn"), default="forward",
+                    help="time the forward pass (default), the backward pass, or the LSH "
+                         "k-nearest-neighbour search (k = 16)")
     ap.add_argument("--heads", type=int, default=0,
                     help="run the workload with this many heads instead (small ncu captures); "
                          "the printed line then names the reduced workload")
@@ -689,6 +864,8 @@ def main():
         return run_reference(args, w)
     if args.pass_ == "backward":
         return run_backward(args, w)
+    if args.pass_ == "knn":
+        return run_knn(args, w)
     return run_ours(args, w)
 
 
