@@ -60,7 +60,7 @@ def feed_forward(y, p, q16=None, chunk=None):
     when chunk is None)."""
     B, L, dm = y.shape
     c = L if chunk is None else chunk
-    out = np.empty((B, L, dm))
+    out = np.zeros((B, L, dm))
     for i in range(0, L, c):
         yi = _q(y[:, i:i + c], q16)
         h = _q(np.maximum(yi @ p["W1"].T + p["b1"], 0.0), q16)
