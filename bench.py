@@ -2,7 +2,7 @@
 """Forward throughput of multi-round LSH attention on B300 (tokens/s = B*H*L per second).
 
     python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference] [--workload NAME]
-                    [--pass forward|backward]
+                    [--pass forward|backward|knn|revblock]
 
 Default workload: the long-text shape B=1, H=8, L=65536, d=128, bf16, 1024 buckets,
 8 rounds, chunk 64, causal (the headline L = 64K, 8-round configuration).  Each rank runs
@@ -10,7 +10,9 @@ its own copy of the workload (independent heads: weak scaling, no data-path coll
 Rank 0 prints one JSON line.  ``--impl reference`` times the fp64 CPU oracle on a bounded
 sample of the same workload instead.  ``--pass backward`` times lsh_attn_backward (the
 gradients in qk and v) on the same workload instead of the forward pass, with its own
-metric line.
+metric line; ``--pass knn`` the LSH k-nearest-neighbour search (k = 16) on it;
+``--pass revblock`` one reversible residual block around the attention at the long-text
+shape (d_model 1024 = 8 heads of 128, d_ff 4096), forward.
 """
 from __future__ import annotations
 
@@ -32,6 +34,8 @@ sys.path.insert(0, ROOT)
 METRIC = "LSH-attention fwd tokens/s (B·H·L per sec) at L=64K, 8 rounds; % of roofline"
 METRIC_BWD = "LSH-attention bwd tokens/s (B·H·L per sec) at L=64K, 8 rounds: dqk, dv"
 METRIC_KNN = "LSH approximate k-NN tokens/s (B·H·L per sec) at L=64K, 8 rounds, k=16; recall@k"
+METRIC_REV = ("Reversible LSH-attention block fwd tokens/s (B·L per sec) at L=64K, d_model 1024, "
+              "8 heads, d_ff 4096, 8 rounds")
 KNN_K = 16
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
@@ -354,6 +358,38 @@ def run_reference(args, w):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_of(w),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": used, "kind": "oracle",
+                         "cpu_model": cpu_model(), "sample": desc},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_reference_revblock(args, bw):
+    """The oracle's reversible block as the reference arm: rank 0 only, each step a
+    bounded sample sized so the run ends within a few minutes."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return 0
+    n = args.warmup + args.steps
+    max_tokens = 2048 if n <= 10 else max(2 * bw.chunk, 2048 * 10 // n)
+    times = []
+    for _ in range(n):
+        tok, t, desc = time_oracle_revblock(bw, max_tokens)
+        times.append(t)
+    timed = times[args.warmup:]
+    t = sum(timed) / len(timed)
+    value = tok / t
+    line = {
+        "impl": "reference", "metric": METRIC_REV, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * t, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "pass": "revblock",
+        "config": {"workload": bw.name, "B": bw.B, "L": bw.L, "d_model": bw.d_model,
+                   "heads": bw.heads, "d_ff": bw.d_ff, "n_buckets": bw.n_buckets,
+                   "n_rounds": bw.n_rounds, "chunk": bw.chunk, "causal": bw.causal,
+                   "ff_chunk": bw.ff_chunk},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                          "cpu_model": cpu_model(), "sample": desc},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -840,6 +876,250 @@ def time_oracle_knn(w, k, max_tokens=8192):
     return sub.tokens, time.perf_counter() - t0, desc + f"; k-NN search, k = {k}"
 
 
+def attn_workload_of(bw):
+    """The attention step of block workload bw as an attention workload."""
+    from lsh_attention_04_b300 import inputs as gen
+    return gen.Workload(bw.name + "_attention", bw.B, bw.heads, bw.L, bw.d, "bf16", bw.n_buckets,
+                        bw.n_rounds, bw.chunk, bw.causal, 0, bw.seed)
+
+
+def block_gemms(bw):
+    """The block forward's matrix products: (name, M, N, K, launches, epilogue)."""
+    M, dm, dff, c = bw.B * bw.L, bw.d_model, bw.d_ff, bw.ff_chunk
+    n_chunks = -(-M // c)
+    return [("qk_projection", M, dm, dm, 1, "bf16 heads"),
+            ("v_projection", M, dm, dm, 1, "bf16 heads"),
+            ("output_projection", M, dm, dm, 1, "fp32 + residual"),
+            ("ffn_in", min(c, M), dff, dm, n_chunks, "bias + ReLU, bf16"),
+            ("ffn_out", min(c, M), dm, dff, n_chunks, "bias, fp32 + residual")]
+
+
+def revblock_launches(lib, bw):
+    """Kernels one lsh_revblock_forward call launches: the stream's bf16 copy, two
+    projections, the attention forward's launches, the status merge, the head merge, the
+    output projection, the bf16 copy of y1, and two products per feed-forward chunk."""
+    aw = attn_workload_of(bw)
+    n_chunks = -(-(bw.B * bw.L) // bw.ff_chunk)
+    attn = int(lib.lsh_attn_kernel_launches(aw.B, aw.H, aw.L, aw.d, aw.n_buckets, aw.n_rounds,
+                                            aw.chunk, 1))
+    return 1 + 2 + attn + 1 + 1 + 1 + 1 + 2 * n_chunks
+
+
+def run_revblock(args, bw):
+    """One reversible block forward (lsh_revblock_forward) at block workload bw: K timed
+    calls on device-resident x1, x2 and weights; every matrix product shape and the
+    attention forward then timed alone on the same device for the stage breakdown and the
+    GEMM roofline; end-to-end calls from pinned host buffers; the oracle's block on a
+    bounded sample as CPU baseline."""
+    import torch
+    import lsh_attention_04_b300 as lsh
+    from lsh_attention_04_b300 import inputs as gen
+
+    world, rank, local, dist = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lib = lsh.load()
+    inp = gen.make_block_inputs(bw, seed=bw.seed + 7919 * rank)
+    d = {}
+    for k, a in inp.items():
+        t = torch.from_numpy(a)
+        d[k] = t.to(dev).to(torch.bfloat16) if k in ("Wqk", "Wv", "Wo", "W1", "W2", "R") else t.to(dev)
+    h_x1, h_x2 = torch.from_numpy(inp["x1"]).pin_memory(), torch.from_numpy(inp["x2"]).pin_memory()
+    y1, y2 = torch.empty_like(d["x1"]), torch.empty_like(d["x2"])
+    ws = lsh.revblock_workspace(bw.B, bw.L, bw.d_model, bw.heads, bw.d_ff, bw.n_buckets,
+                                bw.n_rounds, bw.chunk, bw.ff_chunk, dev)
+    K, Wm = args.steps, args.warmup
+
+    def call():
+        lsh.lsh_revblock_forward(d["x1"], d["x2"], d, bw.heads, bw.n_buckets, bw.chunk,
+                                 bw.causal, bw.scale, bw.ff_chunk, y1, y2, ws)
+
+    for _ in range(Wm):
+        call()
+    torch.cuda.synchronize()
+    st, dd = lsh.lsh_workspace_status(ws)
+    if st != lsh.LSH_OK:
+        raise RuntimeError(f"device check failed after warm-up: {lsh.lsh_status_string(st)} {dd}")
+    stream = torch.cuda.current_stream(dev)
+    uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    clocks = ClockSampler(uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier(dist)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t0.record(stream)
+    for _ in range(K):
+        call()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms_max = allmax(dist, t0.elapsed_time(t1) / K)
+    st, dd = lsh.lsh_workspace_status(ws)
+    if st != lsh.LSH_OK:
+        raise RuntimeError(f"device check failed: {lsh.lsh_status_string(st)} {dd}")
+
+    # stage breakdown: every product shape and the attention forward, each timed alone
+    def timed(fn, reps):
+        for _ in range(3):
+            fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    M, dm = bw.B * bw.L, bw.d_model
+    a16 = torch.empty((M, max(dm, bw.d_ff)), dtype=torch.bfloat16, device=dev)
+    a16.normal_()
+    o32 = torch.empty((M, dm), dtype=torch.float32, device=dev)
+    o16 = torch.empty((M, max(dm, bw.d_ff)), dtype=torch.bfloat16, device=dev)
+    gws = torch.empty(256, dtype=torch.uint8, device=dev)
+    reps = max(5, min(50, K))
+    stages, g_flops, g_ms = {}, 0.0, 0.0
+    for name, m, n, k, launches, epi in block_gemms(bw):
+        A = a16[:m, :k].contiguous() if k != a16.shape[1] else a16[:m]
+        Wt = {"qk_projection": d["Wqk"], "v_projection": d["Wv"], "output_projection": d["Wo"],
+              "ffn_in": d["W1"], "ffn_out": d["W2"]}[name]
+        kw = {}
+        if epi.startswith("bf16 heads"):
+            kw = dict(f32=False, bf16=True, split=(bw.L, bw.d),
+                      out_bf16=o16[:m].view(-1)[: m * n].view(m // bw.L, n // bw.d, bw.L, bw.d))
+        elif epi.startswith("bias + ReLU"):
+            kw = dict(bias=d["b1"], relu=True, f32=False, bf16=True,
+                      out_bf16=o16[:m, :n].contiguous() if n != o16.shape[1] else o16[:m])
+        elif epi.startswith("bias, fp32"):
+            kw = dict(bias=d["b2"], res=o32[:m], out_f32=o32[:m])
+        else:
+            kw = dict(res=o32[:m], out_f32=o32[:m])
+        ms = timed(lambda: lsh.lsh_gemm_bf16(A, Wt, ws=gws, **kw), reps)
+        fl = 2.0 * m * n * k
+        stages[name] = {"M": m, "N": n, "K": k, "launches": launches, "ms_per_launch": ms,
+                        "tflops": fl / (ms / 1e3) / 1e12, "epilogue": epi}
+        g_flops += fl * launches
+        g_ms += ms * launches
+    del a16, o16, o32
+    aw = attn_workload_of(bw)
+    qk16 = torch.empty((aw.B, aw.H, aw.L, aw.d), dtype=torch.bfloat16, device=dev).normal_()
+    v16 = torch.empty_like(qk16).normal_()
+    aws = torch.empty(int(lib.lsh_attn_workspace_bytes(aw.B, aw.H, aw.L, aw.d, aw.n_buckets,
+                                                        aw.n_rounds, aw.chunk, 1)),
+                      dtype=torch.uint8, device=dev)
+    aout = torch.empty((aw.B, aw.H, aw.L, aw.d), dtype=torch.float32, device=dev)
+    alse = torch.empty((aw.B, aw.H, aw.L), dtype=torch.float32, device=dev)
+    attn_ms = timed(lambda: lsh.lsh_attn_forward(qk16, v16, d["R"], aw.n_buckets, aw.chunk,
+                                                 aw.causal, aw.scale, aout, alse, aws), reps)
+    del qk16, v16, aws, aout, alse
+
+    # end to end: H2D of x1 and x2, the block, D2H of y1 and y2
+    h_y1 = torch.empty(y1.shape, dtype=torch.float32).pin_memory()
+    h_y2 = torch.empty(y2.shape, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        d["x1"].copy_(h_x1, non_blocking=True)
+        d["x2"].copy_(h_x2, non_blocking=True)
+        call()
+        h_y1.copy_(y1, non_blocking=True)
+        h_y2.copy_(y2, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_e2e = max(3, min(K, 20))
+    e0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = allmax(dist, e0.elapsed_time(e1) / n_e2e)
+    barrier(dist)
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_src = load_peaks()
+    peak = peaks["bf16_tflops"]
+    achieved = g_flops / (g_ms / 1e3) / 1e12
+    tokens = bw.B * bw.L
+    line = {
+        "metric": METRIC_REV, "value": job_value(tokens, world, ms_max), "unit": "tokens/s",
+        "n_gpus": world, "steps": K, "warmup": Wm, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "pass": "revblock",
+        "config": {"workload": bw.name, "B": bw.B, "L": bw.L, "d_model": bw.d_model,
+                   "heads": bw.heads, "d": bw.d, "d_ff": bw.d_ff, "n_buckets": bw.n_buckets,
+                   "n_rounds": bw.n_rounds, "chunk": bw.chunk, "causal": bw.causal,
+                   "ff_chunk": bw.ff_chunk, "stream": "fp32", "products": "bf16 in, fp32 acc",
+                   "parallelism": f"replicas{world}",
+                   "l2": "inputs (256 MB per stream half) larger than L2; no flush"},
+        "roofline": {"bound": "tensor", "kernel": "gemm_tc_kernel (every matrix product of "
+                     "the block, each shape timed alone)",
+                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "peaks": f"{peak_src} bf16 burst",
+                     "algorithmic_flops": g_flops, "traffic": None},
+        "stages": {"gemm": stages, "gemm_ms_total": g_ms, "attention_ms": attn_ms,
+                   "sum_of_stages_ms": g_ms + attn_ms},
+        "e2e": {"value": tokens * world / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(h_x1.nbytes + h_x2.nbytes),
+                "d2h_bytes_per_step": int(h_y1.nbytes + h_y2.nbytes), "ms_per_step": e2e_ms},
+        "clocks": clk,
+        "gpu_launches": revblock_launches(lib, bw) * K,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        tok, tsec, desc = time_oracle_revblock(bw)
+        line["cpu_baseline"] = {"value": tok / tsec, "unit": "tokens/s", "cores": 1,
+                                "cpu_model": cpu_model(), "kind": "oracle", "sample": desc}
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def time_oracle_revblock(bw, max_tokens=4096):
+    """The oracle's reversible block on a bounded sample (see _oracle_revblock_sample), in
+    a child process whose BLAS runs one thread: returns (positions, seconds, description)."""
+    import dataclasses
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = (f"import sys, json; sys.path.insert(0, {ROOT!r}); import bench; "
+            f"print(json.dumps(bench._oracle_revblock_sample({json.dumps(dataclasses.asdict(bw))!r}, "
+            f"{int(max_tokens)})))")
+    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                         check=True)
+    tok, t, desc = json.loads(out.stdout.strip().splitlines()[-1])
+    return tok, t, desc
+
+
+def _oracle_revblock_sample(bw_json, max_tokens):
+    """The first max_tokens positions of batch row 0 of block workload bw with its widths,
+    heads, buckets and rounds, through the oracle's block forward on one thread."""
+    import dataclasses
+    import oracle
+    from oracle import reversible as orev
+    from lsh_attention_04_b300 import inputs as gen
+    bw = gen.BlockWorkload(**json.loads(bw_json))
+    Ls = min(bw.L, max(2 * bw.chunk, (max_tokens // (2 * bw.chunk)) * (2 * bw.chunk)))
+    sub = dataclasses.replace(bw, B=1, L=Ls, ff_chunk=min(bw.ff_chunk, Ls))
+    inp = gen.make_block_inputs(sub, seed=bw.seed)
+    p = {k: inp[k].astype(np.float64) for k in ("Wqk", "Wv", "Wo", "W1", "b1", "W2", "b2", "R")}
+    p.update(heads=sub.heads, n_buckets=sub.n_buckets, chunk=sub.chunk, causal=sub.causal,
+             scale=sub.scale, ff_chunk=sub.ff_chunk, threads=1)
+    oracle.build()
+    t0 = time.perf_counter()
+    orev.forward(inp["x1"].astype(np.float64), inp["x2"].astype(np.float64), p)
+    t = time.perf_counter() - t0
+    desc = (f"batch row 0 of {bw.name}: first {Ls} positions, d_model {bw.d_model}, "
+            f"{bw.heads} heads, d_ff {bw.d_ff}, {bw.n_rounds} rounds, {bw.n_buckets} buckets "
+            "(fp64, one thread)")
+    return Ls, t, desc
+
+
 def main():
     from lsh_attention_04_b300 import inputs as gen
     ap = argparse.ArgumentParser(description=__doc__)
@@ -849,9 +1129,11 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=gen.HEADLINE, choices=sorted(gen.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--pass", dest="pass_", choices=("forward", "backward", "knn"), default="forward",
-                    help="time the forward pass (default), the backward pass, or the LSH "
-                         "k-nearest-neighbour search (k = 16)")
+    ap.add_argument("--pass", dest="pass_", choices=("forward", "backward", "knn", "revblock"),
+                    default="forward",
+                    help="time the forward pass (default), the backward pass, the LSH "
+                         "k-nearest-neighbour search (k = 16), or one reversible block "
+                         "around the attention (forward)")
     ap.add_argument("--heads", type=int, default=0,
                     help="run the workload with this many heads instead (small ncu captures); "
                          "the printed line then names the reduced workload")
@@ -860,6 +1142,9 @@ def main():
     w = gen.WORKLOADS[args.workload]
     if args.heads > 0 and args.heads != w.H:
         w = w.replace(H=args.heads, name=w.name.replace(f"_H{w.H}_", f"_H{args.heads}_"))
+    if args.pass_ == "revblock":
+        return run_reference_revblock(args, gen.BLOCK_LONG) if args.impl == "reference" else \
+            run_revblock(args, gen.BLOCK_LONG)
     if args.impl == "reference":
         return run_reference(args, w)
     if args.pass_ == "backward":

@@ -298,6 +298,83 @@ lsh_status_t lsh_knn(const void *qk, const void *R, lsh_dtype_t dtype, int B, in
                      int d, int n_buckets, int n_rounds, int chunk, int k, int32_t *nn_idx,
                      float *nn_sim, void *workspace, size_t workspace_bytes, void *stream);
 
+/* ---------------------------------------------------------------- reversible block */
+
+/*
+ * The dense projections of the reversible block (below) on the tensor cores, exported on
+ * their own:  C = epilogue(A W^T),  A bf16 [M][K], W bf16 [N][K] (K contiguous in both,
+ * row = output feature as in a linear layer's weight), accumulated in fp32.  Epilogue, in
+ * this order: + bias[N] (fp32, optional); ReLU (relu = 1); with res (fp32 [M][N],
+ * optional) out = res + res_sign * value.  The result goes to out_f32 (fp32 [M][N]) and/or
+ * out_bf16 (bf16, rounded to nearest even): row-major [M][N] when split_L = split_d = 0,
+ * else split into heads, row m = (b, l) = (m / split_L, m % split_L) and column
+ * n = (h, c) = (n / split_d, n % split_d) stored at [b][h][l][c] (M % split_L == 0,
+ * N % split_d == 0, split_d % 32 == 0).  N % 128 == 0 and K % 64 == 0, else
+ * LSH_ERR_UNSUPPORTED; any M >= 1.  A, W, res and the outputs 16-byte aligned.
+ * Workspace: device, 256-byte aligned, >= 256 bytes (the status block only).
+ * The matrix products of the pages' attention and feed-forward layers are plain linear
+ * layers; nothing in the pages fixes their arithmetic beyond that.
+ */
+lsh_status_t lsh_gemm_bf16(const void *A, const void *W, int M, int N, int K,
+                           const float *bias, int relu, const float *res, float res_sign,
+                           float *out_f32, void *out_bf16, int split_L, int split_d,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * The reversible residual block around the LSH attention (ai-scholar.tech Reformer
+ * article, sections "什么是可逆残余层？" and "RevNet 中的反向传播"; "Reformer" glossary,
+ * ultralytics.com, section "Capas reversibles y división en fragmentos"; modulabs-hub
+ * notes, "Reversible Transformer" and "Chunking"):
+ *     y1 = x1 + Attention(x2),        y2 = x2 + FeedForward(y1)          (forward)
+ *     x2 = y2 - FeedForward(y1),      x1 = y1 - Attention(x2)            (inverse)
+ * Attention(x) = LSHAttention(x Wqk^T, x Wv^T) Wo^T: one shared query/key projection, the
+ * d_model columns split into `heads` heads of d = d_model / heads (64 or 128), steps 1-6
+ * above on each head (n_buckets, n_rounds, chunk, causal, scale as lsh_attn_forward), the
+ * heads merged back.  FeedForward(y) = relu(y W1^T + b1) W2^T + b2, evaluated over chunks
+ * of ff_chunk positions (rows of [B*L][d_model]), so only one chunk's hidden layer exists.
+ *   x1, x2, y1, y2   fp32 [B][L][d_model]   (the residual stream; four distinct arrays)
+ * Every pointer must be 16-byte aligned (b1 and b2 included); a NULL or misaligned pointer,
+ * or two residual-stream arguments that are the same array, give LSH_ERR_INVALID_ARGUMENT.
+ *   Wqk, Wv, Wo      bf16 [d_model][d_model]   (row = output feature, [out][in])
+ *   W1               bf16 [d_ff][d_model];  b1 fp32 [d_ff]
+ *   W2               bf16 [d_model][d_ff];  b2 fp32 [d_model]
+ *   R                bf16 [n_rounds][d][n_buckets/2]
+ * d_model and d_ff must be multiples of 128.  Matrix products take bf16 copies of their
+ * inputs and accumulate in fp32 on the tensor cores; the attention runs in bf16 as
+ * lsh_attn_forward does.  The inverse recomputes the forward's inputs up to the rounding
+ * of the fp32 residual additions (and, where a recomputed input rounds differently to
+ * bf16, the near-tie effects of that on the hash).  Workspace: device, 256-byte aligned,
+ * caller-owned, lsh_revblock_workspace_bytes() bytes (0: invalid sizes); its first 256
+ * bytes are the status block lsh_workspace_status reads.  Asynchronous on `stream`.
+ */
+size_t lsh_revblock_workspace_bytes(int B, int L, int d_model, int heads, int d_ff,
+                                    int n_buckets, int n_rounds, int chunk, int ff_chunk);
+lsh_status_t lsh_revblock_forward(const float *x1, const float *x2, const void *Wqk,
+                                  const void *Wv, const void *Wo, const void *W1,
+                                  const float *b1, const void *W2, const float *b2,
+                                  const void *R, int B, int L, int d_model, int heads, int d_ff,
+                                  int n_buckets, int n_rounds, int chunk, int causal,
+                                  float scale, int ff_chunk, float *y1, float *y2,
+                                  void *workspace, size_t workspace_bytes, void *stream);
+lsh_status_t lsh_revblock_inverse(const float *y1, const float *y2, const void *Wqk,
+                                  const void *Wv, const void *Wo, const void *W1,
+                                  const float *b1, const void *W2, const float *b2,
+                                  const void *R, int B, int L, int d_model, int heads, int d_ff,
+                                  int n_buckets, int n_rounds, int chunk, int causal,
+                                  float scale, int ff_chunk, float *x1, float *x2,
+                                  void *workspace, size_t workspace_bytes, void *stream);
+/*
+ * Byte offsets of the block's intermediates inside its workspace, for callers (and
+ * tests) that inspect them: the attention's own workspace (lsh_attn_forward's layout,
+ * status block first), the per-head projections qk and v (bf16 [B][heads][L][d]), the
+ * attention output (fp32 [B][heads][L][d]) and the merged heads (bf16 [B*L][d_model]),
+ * as left by the last forward or inverse call.  Any pointer may be NULL.
+ */
+lsh_status_t lsh_revblock_workspace_layout(int B, int L, int d_model, int heads, int d_ff,
+                                           int n_buckets, int n_rounds, int chunk, int ff_chunk,
+                                           size_t *off_attn_ws, size_t *off_qk, size_t *off_v,
+                                           size_t *off_attn_out, size_t *off_merged);
+
 /*
  * Self test of the bounded waits the tensor-core kernels use (the pages have no
  * counterpart: it exists to test this library's failure reporting).  Clears the status

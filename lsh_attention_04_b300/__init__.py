@@ -34,7 +34,8 @@ EXPORTS = (
     "lsh_chunk_attn", "lsh_unsort_combine", "lsh_workspace_status", "lsh_attn_forward_timed",
     "lsh_attn_kernel_launches", "lsh_bucket_sort_noalloc", "lsh_selftest_wait_timeout",
     "lsh_attn_backward_workspace_bytes", "lsh_attn_backward", "lsh_attn_backward_timed",
-    "lsh_knn_workspace_bytes", "lsh_knn",
+    "lsh_knn_workspace_bytes", "lsh_knn", "lsh_revblock_workspace_bytes", "lsh_revblock_forward",
+    "lsh_revblock_inverse", "lsh_revblock_workspace_layout", "lsh_gemm_bf16",
 )
 
 _lib = None
@@ -83,6 +84,17 @@ def load():
     lib.lsh_knn_workspace_bytes.restype = S
     lib.lsh_knn.argtypes = [P, P, I] + [I] * 8 + [P, P, P, S, P]
     lib.lsh_knn.restype = I
+    lib.lsh_revblock_workspace_bytes.argtypes = [I] * 9
+    lib.lsh_revblock_workspace_bytes.restype = S
+    rev = [P] * 10 + [I] * 9 + [F, I, P, P, P, S, P]
+    lib.lsh_revblock_forward.argtypes = rev
+    lib.lsh_revblock_forward.restype = I
+    lib.lsh_revblock_inverse.argtypes = rev
+    lib.lsh_revblock_inverse.restype = I
+    lib.lsh_revblock_workspace_layout.argtypes = [I] * 9 + [ctypes.POINTER(S)] * 5
+    lib.lsh_revblock_workspace_layout.restype = I
+    lib.lsh_gemm_bf16.argtypes = [P, P, I, I, I, P, I, P, F, P, P, I, I, P, S, P]
+    lib.lsh_gemm_bf16.restype = I
     lib.lsh_unsort_combine.argtypes = [P, P, P, I] + [I] * 5 + [P, P, P]
     lib.lsh_unsort_combine.restype = I
     lib.lsh_workspace_status.argtypes = [P, ctypes.POINTER(I), P]
@@ -284,6 +296,89 @@ def lsh_knn(qk, R, n_buckets, chunk, k, nn_idx=None, nn_sim=None, ws=None, strea
                           _ptr(nn_idx), _ptr(nn_sim), _ptr(ws), ws.numel(), _stream(stream)),
            "lsh_knn")
     return nn_idx, nn_sim
+
+
+def lsh_gemm_bf16(A, W, bias=None, relu=False, res=None, res_sign=1.0, f32=True, bf16=False,
+                  split=None, out_f32=None, out_bf16=None, ws=None, stream=None):
+    """C = epilogue(A W^T) on the tensor cores: A bf16 [M, K], W bf16 [N, K]; + bias (fp32
+    [N]), ReLU, then res + res_sign * value (res fp32 [M, N]).  Returns (fp32 [M, N] or
+    None, bf16 or None); the bf16 result is [M, N], or with split = (L, d) the heads
+    layout [M / L, N / d, L, d]."""
+    torch = _torch()
+    if A.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
+        raise TypeError("A and W must be bfloat16")
+    M, K = A.shape
+    N = W.shape[0]
+    if f32 and out_f32 is None:
+        out_f32 = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    if bf16 and out_bf16 is None:
+        shape = (M, N) if split is None else (M // split[0], N // split[1], split[0], split[1])
+        out_bf16 = torch.empty(shape, dtype=torch.bfloat16, device=A.device)
+    if ws is None:
+        ws = torch.empty(256, dtype=torch.uint8, device=A.device)
+    sL, sd = (0, 0) if split is None else split
+    _check(load().lsh_gemm_bf16(_ptr(A), _ptr(W), M, N, K, _ptr(bias), int(relu), _ptr(res),
+                                float(res_sign), _ptr(out_f32), _ptr(out_bf16), sL, sd, _ptr(ws),
+                                ws.numel(), _stream(stream)), "lsh_gemm_bf16")
+    return out_f32, out_bf16
+
+
+def revblock_workspace(B, L, d_model, heads, d_ff, n_buckets, n_rounds, chunk, ff_chunk,
+                       device="cuda"):
+    """A device workspace tensor (uint8) for lsh_revblock_forward / lsh_revblock_inverse."""
+    torch = _torch()
+    n = int(load().lsh_revblock_workspace_bytes(B, L, d_model, heads, d_ff, n_buckets, n_rounds,
+                                                chunk, ff_chunk))
+    if n == 0:
+        raise LshError(LSH_ERR_INVALID_ARGUMENT, "lsh_revblock_workspace_bytes")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def lsh_revblock_workspace_layout(B, L, d_model, heads, d_ff, n_buckets, n_rounds, chunk,
+                                  ff_chunk) -> dict:
+    offs = [ctypes.c_size_t() for _ in range(5)]
+    _check(load().lsh_revblock_workspace_layout(B, L, d_model, heads, d_ff, n_buckets, n_rounds,
+                                                chunk, ff_chunk, *[ctypes.byref(o) for o in offs]),
+           "lsh_revblock_workspace_layout")
+    return dict(zip(("attn_ws", "qk", "v", "attn_out", "merged"), (o.value for o in offs)))
+
+
+def _revblock(fn, a1, a2, w, heads, n_buckets, chunk, causal, scale, ff_chunk, o1, o2, ws,
+              stream):
+    torch = _torch()
+    B, L, dm = a1.shape
+    for t in (a1, a2):
+        if t.dtype != torch.float32:
+            raise TypeError("the residual stream is float32")
+    for k in ("Wqk", "Wv", "Wo", "W1", "W2", "R"):
+        if w[k].dtype != torch.bfloat16:
+            raise TypeError(f"{k} must be bfloat16")
+    d_ff, n_rounds = w["W1"].shape[0], w["R"].shape[0]
+    o1 = torch.empty_like(a1) if o1 is None else o1
+    o2 = torch.empty_like(a2) if o2 is None else o2
+    if ws is None:
+        ws = revblock_workspace(B, L, dm, heads, d_ff, n_buckets, n_rounds, chunk, ff_chunk, a1.device)
+    _check(fn(_ptr(a1), _ptr(a2), _ptr(w["Wqk"]), _ptr(w["Wv"]), _ptr(w["Wo"]), _ptr(w["W1"]),
+              _ptr(w["b1"]), _ptr(w["W2"]), _ptr(w["b2"]), _ptr(w["R"]), B, L, dm, heads, d_ff,
+              n_buckets, n_rounds, chunk, int(causal), float(scale), ff_chunk, _ptr(o1), _ptr(o2),
+              _ptr(ws), ws.numel(), _stream(stream)), fn.__name__)
+    return o1, o2
+
+
+def lsh_revblock_forward(x1, x2, w, heads, n_buckets, chunk, causal, scale, ff_chunk, y1=None,
+                         y2=None, ws=None, stream=None):
+    """Reversible block forward: (y1, y2) = (x1 + Attention(x2), x2 + FeedForward(y1)).
+    x1, x2 fp32 [B, L, d_model]; w: dict of Wqk, Wv, Wo [d_model, d_model], W1 [d_ff,
+    d_model], W2 [d_model, d_ff], R [n_rounds, d, n_buckets/2] (bf16) and b1, b2 (fp32)."""
+    return _revblock(load().lsh_revblock_forward, x1, x2, w, heads, n_buckets, chunk, causal,
+                     scale, ff_chunk, y1, y2, ws, stream)
+
+
+def lsh_revblock_inverse(y1, y2, w, heads, n_buckets, chunk, causal, scale, ff_chunk, x1=None,
+                         x2=None, ws=None, stream=None):
+    """Reversible block inverse: x2 = y2 - FeedForward(y1), x1 = y1 - Attention(x2)."""
+    return _revblock(load().lsh_revblock_inverse, y1, y2, w, heads, n_buckets, chunk, causal,
+                     scale, ff_chunk, x1, x2, ws, stream)
 
 
 def lsh_attn_kernel_launches(B, H, L, d, n_buckets, n_rounds, chunk, dtype_code) -> int:

@@ -95,6 +95,24 @@ cudaError_t attn_bwd(const Problem &p, const void *qk, const void *v, const int3
 
 cudaError_t selftest_wait_launch(StatusBlock *status, cudaStream_t st);
 
+// Dense projection on the tensor cores: C = epilogue(A W^T), A [M][K], W [N][K] bf16.
+// Epilogue: + bias[n] (optional), ReLU (optional), out = res + res_sign * x (optional
+// residual, fp32 [M][N]); written to out_f32 [M][N] and/or out_bf16 ([M][N], or split into
+// heads [M / split_L][N / split_d][split_L][split_d] when split_heads).
+struct GemmArgs {
+    const __nv_bfloat16 *A = nullptr, *W = nullptr;
+    int M = 0, N = 0, K = 0;
+    const float *bias = nullptr;
+    int relu = 0;
+    const float *res = nullptr;
+    float res_sign = 1.f;
+    float *out_f32 = nullptr;
+    __nv_bfloat16 *out_bf16 = nullptr;
+    int split_heads = 0, split_L = 1, split_d = 1;
+};
+bool gemm_tc_supported(int M, int N, int K);
+cudaError_t gemm_tc(const GemmArgs &g, StatusBlock *status, cudaStream_t st);
+
 // LSH k-nearest-neighbour search: per-round lists (cand_idx, cand_sim: [seg][L][k]), then
 // the merged top k per token (nn_idx, nn_sim: [B][H][L][k])
 cudaError_t knn_launch(const Problem &p, int k, const void *qk, const int32_t *buckets,

@@ -125,6 +125,64 @@ def make_inputs(w: Workload, seed: int | None = None):
     return qk, v, R
 
 
+@dataclasses.dataclass(frozen=True)
+class BlockWorkload:
+    """One reversible residual block around the LSH attention: residual stream
+    [B, L, d_model] split into heads of d = d_model / heads, feed-forward width d_ff run
+    over chunks of ff_chunk positions."""
+    name: str
+    B: int
+    L: int
+    d_model: int
+    heads: int
+    d_ff: int
+    n_buckets: int
+    n_rounds: int
+    chunk: int
+    causal: bool
+    ff_chunk: int
+    seed: int
+
+    @property
+    def d(self) -> int:
+        return self.d_model // self.heads
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def tokens(self) -> int:
+        return self.B * self.L
+
+
+#: The reversible block at the long-text shape: 8 heads of 128 (d_model 1024), a
+#: feed-forward four times as wide, run over chunks of 8192 positions.
+BLOCK_LONG = BlockWorkload("block_B1_L65536_dm1024_H8_ff4096_R8", 1, 65536, 1024, 8, 4096,
+                           1024, 8, 64, True, 8192, 1005)
+
+
+def make_block_inputs(w: BlockWorkload, seed: int | None = None) -> dict:
+    """Inputs of one reversible block as float32 numpy arrays: the two halves of the
+    residual stream x1, x2 ~ N(0, 1) [B, L, d_model]; weights [out][in] drawn N(0, 1/fan_in)
+    and rounded to bf16 (Wqk, Wv, Wo [d_model, d_model], W1 [d_ff, d_model], W2
+    [d_model, d_ff]); biases b1 [d_ff], b2 [d_model] ~ N(0, 0.01), float32; rotations
+    R ~ N(0, 1) [n_rounds, d, n_buckets/2], rounded to bf16."""
+    rng = np.random.default_rng(w.seed if seed is None else seed)
+    shape = (w.B, w.L, w.d_model)
+
+    def lin(o, i):
+        return round_bf16(_gauss(rng, (o, i)) / np.float32(math.sqrt(i)))
+
+    out = dict(x1=_gauss(rng, shape), x2=_gauss(rng, shape))
+    out.update(Wqk=lin(w.d_model, w.d_model), Wv=lin(w.d_model, w.d_model),
+               Wo=lin(w.d_model, w.d_model), W1=lin(w.d_ff, w.d_model),
+               b1=np.float32(0.1) * _gauss(rng, (w.d_ff,)), W2=lin(w.d_model, w.d_ff),
+               b2=np.float32(0.1) * _gauss(rng, (w.d_model,)),
+               R=round_bf16(_gauss(rng, (w.n_rounds, w.d, w.n_buckets // 2))))
+    return out
+
+
 def synthetic_buckets(rng: np.random.Generator, n_segments: int, L: int, n_buckets: int,
                       alpha: float = 1.0) -> np.ndarray:
     """int32 [n_segments, L] bucket ids with uneven occupancy (Dirichlet(alpha) weights)."""

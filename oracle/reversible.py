@@ -27,7 +27,8 @@ the activation.  Weight layout: W [out][in], as the GPU library takes it.
 
 `q16`, when given, rounds the inputs of every matrix product and of the attention to
 16-bit values at the points the GPU path does (the residual stream itself stays exact);
-the pins run with q16 = None (pure fp64).
+the pins run with q16 = None (pure fp64).  An optional "threads" entry of the parameters
+sets the C attention oracle's thread count (all cores when absent).
 """
 from __future__ import annotations
 
@@ -50,7 +51,7 @@ def attention(x2, p, q16=None, orc=None):
     qk = _q((xq @ p["Wqk"].T).reshape(B, L, H, d).transpose(0, 2, 1, 3), q16)
     v = _q((xq @ p["Wv"].T).reshape(B, L, H, d).transpose(0, 2, 1, 3), q16)
     out, _ = orc.forward(qk, v, _q(p["R"], q16), p["n_buckets"], p["chunk"], p["causal"],
-                         p["scale"])
+                         p["scale"], threads=p.get("threads"))
     merged = _q(out.transpose(0, 2, 1, 3).reshape(B, L, dm), q16)
     return merged @ p["Wo"].T
 

@@ -11,6 +11,8 @@ from __future__ import annotations
 
 import numpy as np
 
+from lsh_attention_04_b300.inputs import round_bf16
+
 TOL_OUT = {"bf16": 2e-2, "f32": 1e-4}
 NEAR_TIE = 1e-5
 SELF_LOGIT = -1.0e5
@@ -79,3 +81,74 @@ def check_lse(gpu, ref, tol, what):
         rel = np.abs(gpu[selfish] - ref[selfish]) / np.abs(ref[selfish])
         assert rel.max() <= 1e-6, f"{what}: self-only lse relative error {rel.max():.2e}"
     return check_close(gpu[~selfish], ref[~selfish], tol, what)
+
+
+# ---- products on the tensor cores ---------------------------------------------------
+
+def acc_bound(K):
+    """Relative error bound of an fp32-accumulated dot product of K bf16 pairs, as a
+    multiple of the sum of the terms' magnitudes.  Products of bf16 values are exact in
+    fp32; the tensor cores add them in K/16 steps of 16-term blocks into the fp32
+    accumulator, so at most K/16 + 5 roundings touch any partial sum.  The unit 2^-23,
+    twice round-to-nearest's, also covers adders that truncate."""
+    return (K / 16 + 5) * 2.0 ** -23
+
+
+def bf16_interval(A, W, bias=None, relu=False):
+    """The bf16 values fp32-accumulated A W^T (+ bias, then ReLU) may round to: [lo, hi]."""
+    ref = A @ W.T
+    mag = np.abs(A) @ np.abs(W).T
+    if bias is not None:
+        ref = ref + bias
+    e = acc_bound(A.shape[1]) * mag + 2.0 ** -23 * (np.abs(ref) + (0 if bias is None else np.abs(bias)))
+    lo, hi = ref - e, ref + e
+    if relu:
+        lo, hi = np.maximum(lo, 0.0), np.maximum(hi, 0.0)
+    return (round_bf16(lo.astype(np.float32)).astype(np.float64),
+            round_bf16(hi.astype(np.float32)).astype(np.float64))
+
+
+def check_bf16_in(gpu, lo, hi, what):
+    bad = (gpu < lo) | (gpu > hi)
+    assert not bad.any(), (f"{what}: {int(bad.sum())} of {bad.size} values outside their "
+                           f"rounding interval; first {gpu[bad][:3]} not in "
+                           f"[{lo[bad][:3]}, {hi[bad][:3]}]")
+    return float(np.mean(lo != hi))
+
+
+def check_residual(gpu, res, A, W, bias, what, extra=0.0):
+    """gpu = res + A W^T (+ bias) in fp32, within ACC + the final rounding (+ extra)."""
+    acc = A @ W.T + (0 if bias is None else bias)
+    ref = res + acc
+    mag = np.abs(A) @ np.abs(W).T + (0 if bias is None else np.abs(bias))
+    tol = acc_bound(A.shape[1]) * mag + 2.0 ** -23 * (np.abs(ref) + np.abs(res) + np.abs(acc)) + extra
+    err = np.abs(gpu - ref)
+    assert (err <= tol).all(), (f"{what}: {int((err > tol).sum())} values outside the bound, "
+                                f"worst excess {float((err - tol).max()):.3e}")
+    return float(err.max())
+
+
+
+
+def comparable_tokens(chunk, g_b, o_b, g_perm, o_perm, g_inv, o_inv):
+    """[n_heads, L] mask of tokens whose every round saw the same window and buckets in two
+    evaluations g and o of one attention (a bucket flip moves the sorted positions between
+    its old and new place, and with them the chunk windows there).  Arrays [n_heads,
+    n_rounds, L]."""
+    nh, n_rounds, L = g_b.shape
+    ok = np.ones((nh, L), bool)
+    for h in range(nh):
+        for r in range(n_rounds):
+            if np.array_equal(g_b[h, r], o_b[h, r]):
+                continue
+            same_pos = g_perm[h, r] == o_perm[h, r]
+            same_bucket = g_b[h, r][g_perm[h, r]] == o_b[h, r][o_perm[h, r]]
+            good = (same_pos & same_bucket).astype(np.int64)
+            cum = np.concatenate([[0], np.cumsum(good)])
+            s = o_inv[h, r]
+            k = s // chunk
+            lo = np.maximum(0, (k - 1) * chunk)
+            hi = np.minimum(L, (k + 1) * chunk)
+            whole = (cum[hi] - cum[lo]) == (hi - lo)
+            ok[h] &= whole & (g_inv[h, r] == s)
+    return ok

@@ -245,3 +245,79 @@ def test_knn_argument_checks(lib, kw, expect):
                      a["R_"], a["chunk"], a["k"], P(a["idx"]), P(a["sim"]), P(a["ws"]), a["wsb"],
                      None)
     assert st == expect
+
+
+def test_revblock_workspace_sizing(lib):
+    f = lib.lsh_revblock_workspace_bytes
+    n = f(1, 65536, 1024, 8, 4096, 1024, 8, 64, 4096)
+    # the attention's own workspace plus qk, v (bf16), the attention output (fp32), two
+    # bf16 copies of the stream and one chunk of the hidden layer
+    M = 65536
+    assert n > lib.lsh_attn_workspace_bytes(1, 8, M, 128, 1024, 8, 64, lsh.LSH_BF16) + \
+        M * 1024 * (2 + 2 + 4 + 2 + 2) + 4096 * 4096 * 2
+    assert n % 256 == 0
+    assert f(1, 1024, 192, 2, 512, 32, 2, 64, 256) == 0     # d_model % 128
+    assert f(1, 1024, 256, 2, 500, 32, 2, 64, 256) == 0     # d_ff % 128
+    assert f(1, 1024, 256, 3, 512, 32, 2, 64, 256) == 0     # d_model % heads
+    assert f(1, 1024, 256, 2, 512, 32, 2, 64, 0) == 0       # ff_chunk
+    assert f(1, 1024, 384, 4, 512, 32, 2, 64, 256) == 0     # head size 96
+    assert f(1, 1000, 256, 2, 512, 32, 2, 64, 256) == 0     # L % chunk
+
+
+def test_revblock_layout(lib):
+    lay = lsh.lsh_revblock_workspace_layout(2, 1024, 256, 2, 512, 32, 4, 64, 300)
+    n = lib.lsh_revblock_workspace_bytes(2, 1024, 256, 2, 512, 32, 4, 64, 300)
+    assert lay["attn_ws"] >= 256 and all(v % 256 == 0 for v in lay.values())
+    assert lay["attn_ws"] < lay["qk"] < lay["v"] < lay["attn_out"] < lay["merged"] < n
+
+
+@no_device
+@pytest.mark.parametrize("fn", ["lsh_revblock_forward", "lsh_revblock_inverse"])
+@pytest.mark.parametrize("kw,expect", [
+    (dict(x1=0), lsh.LSH_ERR_INVALID_ARGUMENT),
+    (dict(W1=0), lsh.LSH_ERR_INVALID_ARGUMENT),
+    (dict(b2=0x104), lsh.LSH_ERR_INVALID_ARGUMENT),       # misaligned
+    (dict(y2=0x100), lsh.LSH_ERR_INVALID_ARGUMENT),       # the same array as x1
+    (dict(ws=0x110), lsh.LSH_ERR_INVALID_ARGUMENT),
+    (dict(dm=192), lsh.LSH_ERR_INVALID_ARGUMENT),
+    (dict(causal=2), lsh.LSH_ERR_INVALID_ARGUMENT),
+    (dict(wsb=256), lsh.LSH_ERR_WORKSPACE_TOO_SMALL),
+])
+def test_revblock_argument_checks(lib, fn, kw, expect):
+    a = dict(x1=0x100, x2=0x200, Wqk=0x300, Wv=0x400, Wo=0x500, W1=0x600, b1=0x700, W2=0x800,
+             b2=0x900, R=0xa00, B=1, L=1024, dm=256, H=2, dff=512, nb=32, R_=2, chunk=64,
+             causal=1, ff_chunk=256, y1=0xb00, y2=0xc00, ws=0x1000, wsb=1 << 30)
+    a.update(kw)
+    P = ctypes.c_void_p
+    st = getattr(lib, fn)(
+        *[P(a[k]) for k in ("x1", "x2", "Wqk", "Wv", "Wo", "W1", "b1", "W2", "b2", "R")],
+        a["B"], a["L"], a["dm"], a["H"], a["dff"], a["nb"], a["R_"], a["chunk"], a["causal"],
+        ctypes.c_float(0.125), a["ff_chunk"], P(a["y1"]), P(a["y2"]), P(a["ws"]), a["wsb"], None)
+    assert st == expect
+
+
+@no_device
+@pytest.mark.parametrize("kw,expect", [
+    (dict(A=0), lsh.LSH_ERR_INVALID_ARGUMENT),
+    (dict(A=0x108), lsh.LSH_ERR_INVALID_ARGUMENT),            # misaligned
+    (dict(of=0, ob=0), lsh.LSH_ERR_INVALID_ARGUMENT),         # no output
+    (dict(relu=2), lsh.LSH_ERR_INVALID_ARGUMENT),
+    (dict(M=0), lsh.LSH_ERR_INVALID_ARGUMENT),
+    (dict(sL=64, sd=0), lsh.LSH_ERR_INVALID_ARGUMENT),
+    (dict(sL=100, sd=64), lsh.LSH_ERR_INVALID_ARGUMENT),      # M % split_L
+    (dict(sL=64, sd=48), lsh.LSH_ERR_INVALID_ARGUMENT),       # split_d % 32
+    (dict(sL=64, sd=64, ob=0), lsh.LSH_ERR_INVALID_ARGUMENT),  # split needs the bf16 output
+    (dict(ws=0x180), lsh.LSH_ERR_INVALID_ARGUMENT),
+    (dict(N=200), lsh.LSH_ERR_UNSUPPORTED),
+    (dict(K=96), lsh.LSH_ERR_UNSUPPORTED),
+    (dict(wsb=128), lsh.LSH_ERR_WORKSPACE_TOO_SMALL),
+])
+def test_gemm_argument_checks(lib, kw, expect):
+    a = dict(A=0x100, W=0x200, M=256, N=256, K=128, bias=0x300, relu=0, res=0, of=0x400,
+             ob=0x500, sL=0, sd=0, ws=0x1000, wsb=256)
+    a.update(kw)
+    P = ctypes.c_void_p
+    st = lib.lsh_gemm_bf16(P(a["A"]), P(a["W"]), a["M"], a["N"], a["K"], P(a["bias"]), a["relu"],
+                           P(a["res"]), ctypes.c_float(1.0), P(a["of"]), P(a["ob"]), a["sL"],
+                           a["sd"], P(a["ws"]), a["wsb"], None)
+    assert st == expect

@@ -249,25 +249,7 @@ def _ws_view(w, ws, name):
 
 
 def _comparable_tokens(w, g_b, o_b, g_perm, o_perm, g_inv, o_inv):
-    """[n_heads, L] mask of tokens whose every round saw the same window and buckets on
-    both sides (a near-tie bucket flip moves the sorted positions around it)."""
-    nh = g_b.shape[0]
-    ok = np.ones((nh, w.L), bool)
-    for h in range(nh):
-        for r in range(w.n_rounds):
-            if np.array_equal(g_b[h, r], o_b[h, r]):
-                continue
-            same_pos = g_perm[h, r] == o_perm[h, r]
-            same_bucket = g_b[h, r][g_perm[h, r]] == o_b[h, r][o_perm[h, r]]
-            good = (same_pos & same_bucket).astype(np.int64)
-            cum = np.concatenate([[0], np.cumsum(good)])
-            s = o_inv[h, r]
-            k = s // w.chunk
-            lo = np.maximum(0, (k - 1) * w.chunk)
-            hi = np.minimum(w.L, (k + 1) * w.chunk)
-            whole = (cum[hi] - cum[lo]) == (hi - lo)
-            ok[h] &= whole & (g_inv[h, r] == s)
-    return ok
+    return P.comparable_tokens(w.chunk, g_b, o_b, g_perm, o_perm, g_inv, o_inv)
 
 
 # The long-text workload's inner shape (d = 128, 1024 buckets, 8 rounds, chunk 64,
