@@ -137,3 +137,37 @@ def test_knn_full_size_sampled():
                     for q, t in enumerate(toks)]
     print(f"recall@{k} on the long-text shape: {np.mean(recalls):.3f}")
     assert np.mean(recalls) > 0.5
+
+
+def test_knn_recall_vs_rounds_and_buckets():
+    """Recall@16 of the GPU search against exhaustive cosine search on the long-text shape
+    (L = 65536, d = 128, clustered, chunk 64), one head, 512 sampled queries, for rounds
+    1, 2, 4, 8 and 256 / 1024 / 2048 buckets (the kernels' largest).  More rounds find
+    more of the true neighbours, their candidate sets being unions over the rounds; the
+    table is printed."""
+    base = gen.WORKLOADS[gen.HEADLINE].replace(H=1, name="knn_recall_L65536_d128")
+    k = 16
+    qk, _, _ = gen.make_inputs(base)
+    rng = np.random.default_rng(11)
+    toks = np.sort(rng.choice(base.L, 512, replace=False))
+    e_idx, _ = oracle.exact_knn(qk.reshape(base.L, base.d), k, toks)
+    rows = []
+    for nb in (256, 1024, 2048):
+        rec = []
+        for R_ in (1, 2, 4, 8):
+            w = base.replace(n_buckets=nb, n_rounds=R_)
+            _, _, R = gen.make_inputs(w)
+            dqk, dR = P.to_device(qk, "bf16"), P.to_device(R, "bf16")
+            idx, _ = lsh.lsh_knn(dqk, dR, nb, w.chunk, k)
+            got = idx.cpu().numpy().reshape(base.L, k)[toks]
+            rec.append(np.mean([len(set(got[q].tolist()) & set(e_idx[q].tolist())) / k
+                                for q in range(len(toks))]))
+        rows.append((nb, rec))
+        # the inputs draw the rotations in order, so the first rounds of a larger count
+        # are the rounds of a smaller one and the candidate sets are nested; a true
+        # neighbour among the candidates is always kept (only true neighbours can rank
+        # above it), so recall cannot fall as rounds are added
+        assert all(b >= a for a, b in zip(rec, rec[1:])), rec
+    print("recall@16 (rows: buckets; columns: rounds 1, 2, 4, 8)")
+    for nb, rec in rows:
+        print(f"  {nb:5d}: " + "  ".join(f"{r:.3f}" for r in rec))
