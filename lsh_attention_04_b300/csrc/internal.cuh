@@ -32,6 +32,8 @@ inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a
 // Sort tile: keys per CTA of the counting-sort passes.
 constexpr int kSortTile = 4096;
 inline int sort_tiles(int L) { return (L + kSortTile - 1) / kSortTile; }
+// dynamic shared memory the one-launch segment sort may use
+constexpr size_t kSortSegSmemMax = 220 * 1024;
 
 // Element loads widened to fp32.
 __device__ __forceinline__ float ld_f32(const float *p, size_t i) { return p[i]; }

@@ -109,7 +109,8 @@ def test_hash_parity(w):
 SORT_CASES = [
     (6, 1344, 64, 1.0), (2, 8256, 128, 1.0), (4, 65536, 1024, 1.0), (3, 4096, 1, 1.0),
     (2, 64, 2048, 1.0), (4, 12288, 192, 0.05), (5, 1000, 7, 0.3), (1, 4097, 2, 1.0),
-    (2, 65536, 16, 0.02), (1, 70000, 64, 1.0), (1, 65536, 2048, 1.0),
+    (2, 65536, 16, 0.02), (1, 70000, 64, 1.0), (1, 65536, 2048, 1.0), (2, 131072, 1024, 0.3),
+    (7, 2, 16, 1.0),
 ]
 
 
@@ -530,3 +531,22 @@ def test_full_size_staged(name):
         co, cl = oracle.combine(ref_o, ref_l, o_inv, tokens=rows)
         P.check_close(out2[h][rows], co, tol, "out")
         P.check_lse(lse2[h][rows], cl, tol, "lse")
+
+
+def test_sort_outputs_at_odd_offsets():
+    """perm and inv starting 4 bytes past a 16-byte boundary (the segment sort then writes
+    perm with 4-byte stores); same results as the oracle."""
+    segs, L, nb = 3, 8192, 128
+    rng = np.random.default_rng(5)
+    keys = gen.synthetic_buckets(rng, segs, L, nb, 0.5)
+    d = torch.from_numpy(keys).cuda().reshape(1, segs, 1, L)
+    pbuf = torch.empty(segs * L + 1, dtype=torch.int32, device="cuda")
+    ibuf = torch.empty(segs * L + 1, dtype=torch.int32, device="cuda")
+    perm, inv = pbuf[1:].view(1, segs, 1, L), ibuf[1:].view(1, segs, 1, L)
+    assert perm.data_ptr() % 16 == 4
+    lsh.lsh_bucket_sort(d, nb, perm=perm, inv=inv)
+    torch.cuda.synchronize()
+    for s in range(segs):
+        p, i, _ = oracle.sort(keys[s], nb)
+        assert np.array_equal(perm[0, s, 0].cpu().numpy(), p)
+        assert np.array_equal(inv[0, s, 0].cpu().numpy(), i)
