@@ -55,7 +55,7 @@ KERNEL_SOURCES = {
     "sort": ["sort.cu"],
     "attn": ["attn_tc.cu", "sm100.cuh"],
     "combine": ["combine.cu", "combine_tma.cu", "sm100.cuh"],
-    "attn_bwd": ["attn_bwd.cu"],
+    "attn_bwd": ["attn_bwd.cu", "attn_bwd_tc.cu"],
 }
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
@@ -679,9 +679,10 @@ def run_backward(args, w):
     Bts = sum(k["bytes"] for k in wk.values())
     t_roof = max(F / (peak_c * 1e12), Bts / (peaks["hbm_gbs"] * 1e9))
     # kernels per call: the forward's hash and sort launches plus the backward kernel
-    # (the forward's count less its attention and combination, plus one)
+    # (the forward's count less its attention and combination, plus one), and for bf16
+    # the prepass of the tensor-core kernel (g_out in bf16, g_out . out)
     launches = int(lib.lsh_attn_kernel_launches(w.B, w.H, w.L, w.d, w.n_buckets, w.n_rounds,
-                                                w.chunk, dt_code)) - 1
+                                                w.chunk, dt_code)) - 1 + (w.dtype == "bf16")
     line = {
         "metric": METRIC_BWD, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": Wm, "ms_per_step": ms_max, "higher_is_better": True,

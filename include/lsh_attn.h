@@ -123,7 +123,8 @@ lsh_status_t lsh_attn_forward_timed(const void *qk, const void *v, const void *R
 
 /*
  * Bytes of device workspace lsh_attn_backward needs (0 when the arguments are invalid
- * or unsupported).  Smaller than the forward's: no per-round outputs.
+ * or unsupported): the forward's without per-round outputs, plus, for LSH_BF16, g_out in
+ * bf16 and one fp32 per token.
  */
 size_t lsh_attn_backward_workspace_bytes(int B, int H, int L, int d, int n_buckets,
                                          int n_rounds, int chunk, lsh_dtype_t dtype);
@@ -153,6 +154,11 @@ size_t lsh_attn_backward_workspace_bytes(int B, int H, int L, int d, int n_bucke
  * in dv from each round (it copies v_i).  dqk and dv must not alias any input or the
  * workspace.  The gradients are summed with fp32 atomics, so the order of additions,
  * and with it the last bits, can change from call to call.
+ * Arithmetic: LSH_F32 runs in fp32 on the CUDA cores.  LSH_BF16 (d in {64, 128}, chunk
+ * in {32, 64}) runs its five contractions on the tensor cores with bf16 operands and
+ * fp32 accumulation: g_out, the weights exp(s_ij - lse_i) and the score gradients are
+ * rounded to bf16 for the products (scores, their softmax and g_out . out stay fp32);
+ * out, g_out, dqk and dv must then be 16-byte aligned (else LSH_ERR_INVALID_ARGUMENT).
  */
 lsh_status_t lsh_attn_backward(const void *qk, const void *v, const void *R, lsh_dtype_t dtype,
                                int B, int H, int L, int d, int n_buckets, int n_rounds,

@@ -79,6 +79,7 @@ cudaError_t hash_tc(const Problem &p, const void *qk, const void *R, void *rpack
 bool hash_tc_supported(const Problem &p);
 int hash_tc_launches(const Problem &p);
 
+int sort_launches(const Problem &p);   // kernels one sort_launch call launches
 cudaError_t sort_launch(const Problem &p, const int32_t *buckets, int32_t *perm, int32_t *inv,
                         int32_t *bstart, int32_t *counts, cudaStream_t st);
 
@@ -94,6 +95,15 @@ cudaError_t attn_tc(const Problem &p, const void *qk, const void *v, const int32
 cudaError_t attn_bwd(const Problem &p, const void *qk, const void *v, const int32_t *buckets,
                      const int32_t *perm, const float *inv_norm, const float *out, const float *lse,
                      const float *g_out, const float *g_lse, float *dqk, float *dv, cudaStream_t st);
+// bf16 inputs, d in {64, 128}, chunk in {32, 64}: the tensor-core backward, which needs
+// attn_bwd_tc_scratch_bytes() of scratch (g_out in bf16 and g_out . out per token) and
+// 16-byte aligned out, g_out, dqk and dv.
+bool attn_bwd_tc_supported(const Problem &p);
+size_t attn_bwd_tc_scratch_bytes(const Problem &p);
+cudaError_t attn_bwd_tc(const Problem &p, const void *qk, const void *v, const int32_t *buckets,
+                        const int32_t *perm, const float *inv_norm, const float *out,
+                        const float *lse, const float *g_out, const float *g_lse, float *dqk,
+                        float *dv, void *scratch, cudaStream_t st);
 
 cudaError_t selftest_wait_launch(StatusBlock *status, cudaStream_t st);
 

@@ -187,6 +187,13 @@ lsh_status_t forward(const void *qk, const void *v, const void *R, lsh_dtype_t d
     return record(events, 4, st);
 }
 
+// Workspace of the backward pass: the forward's layout without per-round outputs, then
+// the tensor-core kernel's scratch.
+size_t backward_bytes(const Problem &p)
+{
+    return align_up(layout(p, false).total + attn_bwd_tc_scratch_bytes(p));
+}
+
 // The backward pass; `events`, when not null, are recorded before the hash, the sort and
 // the backward kernel, and after it.
 lsh_status_t backward(const void *qk, const void *v, const void *R, lsh_dtype_t dtype, int B,
@@ -202,7 +209,12 @@ lsh_status_t backward(const void *qk, const void *v, const void *R, lsh_dtype_t 
         return LSH_ERR_INVALID_ARGUMENT;
     if (((uintptr_t)workspace) % 256 != 0) return LSH_ERR_INVALID_ARGUMENT;
     const Layout w = layout(p, false);
-    if (workspace_bytes < w.total) return LSH_ERR_WORKSPACE_TOO_SMALL;
+    const bool tc = attn_bwd_tc_supported(p);
+    if (tc) {
+        const auto a16 = [](const void *x) { return ((uintptr_t)x) % 16 == 0; };
+        if (!a16(out) || !a16(g_out) || !a16(dqk) || !a16(dv)) return LSH_ERR_INVALID_ARGUMENT;
+    }
+    if (workspace_bytes < backward_bytes(p)) return LSH_ERR_WORKSPACE_TOO_SMALL;
     cudaStream_t st = (cudaStream_t)stream;
     int32_t *buckets = at<int32_t>(workspace, w.buckets);
     float *inv_norm = at<float>(workspace, w.inv_norm);
@@ -221,9 +233,13 @@ lsh_status_t backward(const void *qk, const void *v, const void *R, lsh_dtype_t 
                                      at<int32_t>(workspace, w.counts), st))) != LSH_OK)
         return s;
     if ((s = record(events, 2, st)) != LSH_OK) return s;
-    if ((s = cuda_status(attn_bwd(p, qk, v, buckets, perm, inv_norm, out, lse, g_out, g_lse, dqk,
-                                  dv, st))) != LSH_OK)
-        return s;
+    if (tc)
+        s = cuda_status(attn_bwd_tc(p, qk, v, buckets, perm, inv_norm, out, lse, g_out, g_lse, dqk,
+                                    dv, at<void>(workspace, w.total), st));
+    else
+        s = cuda_status(attn_bwd(p, qk, v, buckets, perm, inv_norm, out, lse, g_out, g_lse, dqk,
+                                 dv, st));
+    if (s != LSH_OK) return s;
     return record(events, 3, st);
 }
 
@@ -259,7 +275,7 @@ size_t lsh_attn_backward_workspace_bytes(int B, int H, int L, int d, int n_bucke
 {
     const Problem p = make_problem(B, H, L, d, n_buckets, n_rounds, chunk, 0, 1.f, dtype);
     if (validate(p) != LSH_OK) return 0;
-    return layout(p, false).total;
+    return backward_bytes(p);
 }
 
 lsh_status_t lsh_attn_backward(const void *qk, const void *v, const void *R, lsh_dtype_t dtype,
@@ -294,7 +310,7 @@ int lsh_attn_kernel_launches(int B, int H, int L, int d, int n_buckets, int n_ro
     const Problem p = make_problem(B, H, L, d, n_buckets, n_rounds, chunk, 0, 1.f, dtype);
     if (validate(p) != LSH_OK) return 0;
     const int hash = hash_tc_supported(p) ? hash_tc_launches(p) : 1;
-    const int sort = 3;
+    const int sort = sort_launches(p);
     const int attn = 1;
     const int combine = 1;
     return hash + sort + attn + combine;

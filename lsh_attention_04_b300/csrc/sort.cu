@@ -388,6 +388,13 @@ cudaError_t launch_cluster_sort(const Problem &p, int C, int Lc, int lc_shift,
 
 }  // namespace
 
+// The one-launch path takes every segment of up to 65536 keys: its shared memory stays
+// below the limit for every bucket count the library accepts (<= 2048).
+int sort_launches(const Problem &p)
+{
+    return p.L <= kSegMaxL ? 1 : 3;
+}
+
 cudaError_t sort_launch(const Problem &p, const int32_t *buckets, int32_t *perm, int32_t *inv,
                         int32_t *bstart, int32_t *counts, cudaStream_t st)
 {

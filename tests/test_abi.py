@@ -165,16 +165,20 @@ def test_backward_workspace_sizing(lib):
     args = (1, 8, 65536, 128, 1024, 8, 64, lsh.LSH_BF16)
     fwd = lib.lsh_attn_workspace_bytes(*args)
     bwd = lib.lsh_attn_backward_workspace_bytes(*args)
-    # no per-round outputs (o_r alone is B*H*R*L*d*2 bytes), but buckets, perm, inv
-    assert 0 < bwd < fwd - 1 * 8 * 8 * 65536 * 128 * 2
-    assert bwd > 3 * 4 * 8 * 8 * 65536 and bwd % 256 == 0
+    # no per-round outputs (o_r alone is B*H*R*L*d*2 bytes), but buckets, perm, inv, and
+    # for bf16 the tensor-core kernel's g_out in bf16 plus one fp32 per token
+    n_tok = 8 * 65536
+    assert 0 < bwd < fwd - 1 * 8 * 8 * 65536 * 128 * 2 + n_tok * (2 * 128 + 4)
+    assert bwd > 3 * 4 * 8 * 8 * 65536 + n_tok * (2 * 128 + 4) and bwd % 256 == 0
+    f32 = lib.lsh_attn_backward_workspace_bytes(*args[:-1], lsh.LSH_F32)
+    assert f32 < bwd
     assert lib.lsh_attn_backward_workspace_bytes(1, 1, 100, 64, 32, 1, 64, lsh.LSH_F32) == 0
 
 
 def _bwd(lib, **kw):
-    a = dict(qk=1, v=1, R=1, dtype=lsh.LSH_BF16, B=1, H=1, L=1024, d=64, nb=32, R_=1,
-             chunk=64, causal=1, scale=0.125, out=1, lse=1, g_out=1, g_lse=0, dqk=1, dv=1,
-             ws=256, wsb=1 << 30, st=None)
+    a = dict(qk=0x100, v=0x200, R=0x300, dtype=lsh.LSH_BF16, B=1, H=1, L=1024, d=64, nb=32,
+             R_=1, chunk=64, causal=1, scale=0.125, out=0x400, lse=0x500, g_out=0x600, g_lse=0,
+             dqk=0x700, dv=0x800, ws=0x1000, wsb=1 << 30, st=None)
     a.update(kw)
     P = ctypes.c_void_p
     return lib.lsh_attn_backward(P(a["qk"]), P(a["v"]), P(a["R"]), a["dtype"], a["B"], a["H"],
@@ -199,6 +203,9 @@ def _bwd(lib, **kw):
     (dict(chunk=128, L=1024), lsh.LSH_ERR_UNSUPPORTED),
     (dict(nb=40), lsh.LSH_ERR_UNSUPPORTED),
     (dict(wsb=1024), lsh.LSH_ERR_WORKSPACE_TOO_SMALL),
+    (dict(g_out=0x604), lsh.LSH_ERR_INVALID_ARGUMENT),   # bf16: 16-byte aligned gradients
+    (dict(dv=0x804), lsh.LSH_ERR_INVALID_ARGUMENT),
+    (dict(g_out=0x604, dtype=lsh.LSH_F32, wsb=1024), lsh.LSH_ERR_WORKSPACE_TOO_SMALL),
 ])
 @no_device
 def test_backward_validation(lib, kw, expect):

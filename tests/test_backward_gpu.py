@@ -3,10 +3,15 @@
 Each case is compared on the GPU's own buckets, so hash near-ties do not enter:
 
 * kernel parity -- lsh_attn_backward is given the oracle's out and lse (rounded to fp32),
-  so only the kernel's fp32 arithmetic differs from the oracle's fp64 backward.  Its dot
-  products of up to 128 terms carry relative errors near 1e-5, and g_out.v_j - D_i can
-  cancel by about a factor 10: the bar is 1e-3 of the largest gradient, far below what a
-  dropped or misplaced term gives (an error the size of the gradient itself);
+  so only the kernel's arithmetic differs from the oracle's fp64 backward.  fp32 inputs
+  (CUDA-core kernel): dot products of up to 128 terms carry relative errors near 1e-5, and
+  g_out.v_j - D_i can cancel by about a factor 10: the bar is 1e-3 of the largest
+  gradient.  bf16 inputs (tensor-core kernel): g_out, the weights pi and the score
+  gradients are rounded to bf16 for the products (2^-9 relative each, at most two on any
+  term's path), and the rounding of g_out enters ds through g_out.v_j - D_i, which the
+  same factor 10 can amplify: about 2e-2 per term, so the bar is 3e-2 of the largest
+  gradient.  Both are far below what a dropped or misplaced term gives (an error the size
+  of the gradient itself);
 * end to end -- lsh_attn_forward's own out and lse go into lsh_attn_backward.  With bf16
   inputs the forward keeps each round's rows in 16 bits (out off by up to ~1e-2), which
   moves D_i = g_out_i . out_i by a few 1e-2: the bar is 5e-2 of the largest gradient
@@ -79,8 +84,9 @@ def _cuda_f32(a):
 
 
 def _check(got, ref, frac, what):
-    tol = frac * float(np.abs(ref).max())
-    P.check_close(got.cpu().numpy(), ref, tol, what)
+    """Max abs error within frac of the largest gradient; returns that ratio."""
+    scale = float(np.abs(ref).max())
+    return P.check_close(got.cpu().numpy(), ref, frac * scale, what) / scale
 
 
 @pytest.mark.parametrize("w", CASES, ids=ids)
@@ -101,8 +107,10 @@ def test_backward_parity(w):
     dqk, dv = lsh.lsh_attn_backward(dq_, dv_, dR, w.n_buckets, w.chunk, w.causal, w.scale,
                                     _cuda_f32(out_o), _cuda_f32(lse_o), g_out_d, g_lse_d)
     torch.cuda.synchronize()
-    _check(dqk, dqk_o, 1e-3, f"{w.name} dqk (kernel)")
-    _check(dv, dv_o, 1e-3, f"{w.name} dv (kernel)")
+    bar = 3e-2 if w.dtype == "bf16" else 1e-3
+    e_q = _check(dqk, dqk_o, bar, f"{w.name} dqk (kernel)")
+    e_v = _check(dv, dv_o, bar, f"{w.name} dv (kernel)")
+    print(f"{w.name}: kernel errors / largest gradient: dqk {e_q:.2e}, dv {e_v:.2e}")
 
     # end to end: the GPU forward's out and lse
     out, lse = lsh.lsh_attn_forward(dq_, dv_, dR, w.n_buckets, w.chunk, w.causal, w.scale)

@@ -3,8 +3,8 @@
 A zero row has inverse norm 0 (it scores 0 as a key), projects to 0 in every round (bucket 0
 by the first-index rule) and, as a query, weights its candidates uniformly.  The forward and
 the backward pass are compared with the oracle on the GPU's own buckets, with the bars of the
-other parity tests: 2e-2 (bf16) / 1e-4 (fp32) for out and lse, and 1e-3 of the largest
-gradient for the backward fed the oracle's out and lse.
+other parity tests: 2e-2 (bf16) / 1e-4 (fp32) for out and lse, and 3e-2 (bf16, tensor-core
+kernel) / 1e-3 (fp32) of the largest gradient for the backward fed the oracle's out and lse.
 """
 from __future__ import annotations
 
@@ -83,5 +83,6 @@ def test_zero_rows(w):
     dqk, dv = lsh.lsh_attn_backward(dq_, dv_, dR, w.n_buckets, w.chunk, w.causal, w.scale,
                                     as_dev(out_o), as_dev(lse_o), as_dev(g_out), as_dev(g_lse))
     torch.cuda.synchronize()
-    P.check_close(dqk.cpu().numpy(), dqk_o, 1e-3 * float(np.abs(dqk_o).max()), f"{w.name} dqk")
-    P.check_close(dv.cpu().numpy(), dv_o, 1e-3 * float(np.abs(dv_o).max()), f"{w.name} dv")
+    bar = 3e-2 if w.dtype == "bf16" else 1e-3     # the kernel-parity bars of test_backward_gpu
+    P.check_close(dqk.cpu().numpy(), dqk_o, bar * float(np.abs(dqk_o).max()), f"{w.name} dqk")
+    P.check_close(dv.cpu().numpy(), dv_o, bar * float(np.abs(dv_o).max()), f"{w.name} dv")
