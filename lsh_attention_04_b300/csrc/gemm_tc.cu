@@ -2,16 +2,19 @@
 // C = epilogue(A W^T) with A [M][K] and W [N][K] bf16 (both K contiguous), fp32
 // accumulation in tensor memory.
 //
-// Persistent CTAs walk 128 x 128 output tiles (tile t = m_block * n_blocks + n_block, so
-// neighbouring CTAs share A's row block in L2).  Warp roles (6 warps):
+// Persistent CTAs walk 128 x 256 output tiles (tile t = m_block * n_blocks + n_block, so
+// neighbouring CTAs share A's row block in L2; a last tile 128 columns wide when
+// N % 256 = 128 reads zeros past W's last row and stores only its live columns).  Warp
+// roles (6 warps):
 //   0-3  epilogue: warp w reads TMEM lanes 32w .. 32w+31 (one output row per thread),
 //        32 columns at a time, and applies bias, ReLU and a residual (out = res + s * x),
 //        writing fp32 and/or bf16, row-major or split into heads [B][H][L][d];
-//   4    producer: TMA loads of 128 x 64 tiles of A and W (128-byte swizzle) into a
-//        4-stage ring;
-//   5    MMA issuer and TMEM owner: 4 tcgen05.mma (M=128, N=128, K=16) per stage into one
-//        of two 128-column accumulators, so the epilogue of a tile overlaps the MMAs of the
-//        next one.
+//   4    producer: TMA loads of 64-column tiles of A (128 rows) and W (256 rows),
+//        128-byte swizzle, into a 4-stage ring of 48 KB stages;
+//   5    MMA issuer and TMEM owner: 4 tcgen05.mma (M=128, N=256, K=16) per stage into one
+//        of two 256-column accumulators (all 512 columns), so the epilogue of a tile
+//        overlaps the MMAs of the next one.  At N = 256 an MMA reads 12 KB of operands in
+//        128 cycles, inside the shared-memory bandwidth (N = 128 would need all of it).
 // Every wait is bounded (sm100::wait); on a timeout the kernel records where in the
 // workspace status block and winds down.
 #include "sm100.cuh"
@@ -21,9 +24,9 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kTM = 128, kTN = 128, kTK = 64;
+constexpr int kTM = 128, kTN = 256, kTK = 64;
 constexpr int kStages = 4;
-constexpr int kStageBytes = (kTM + kTN) * kTK * 2;   // 32 KB
+constexpr int kStageBytes = (kTM + kTN) * kTK * 2;   // 48 KB
 constexpr int kGemmThreads = 6 * 32;
 
 struct __align__(8) GemmBarriers {
@@ -48,7 +51,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int *abort_flag = &sb.abort_flag;
-    const int m_blocks = (g.M + kTM - 1) / kTM, n_blocks = g.N / kTN, k_steps = g.K / kTK;
+    const int m_blocks = (g.M + kTM - 1) / kTM, n_blocks = (g.N + kTN - 1) / kTN, k_steps = g.K / kTK;
     const int n_tiles = m_blocks * n_blocks;
 
     if (threadIdx.x == 0) {
@@ -64,7 +67,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__
         sb.abort_flag = 0;
         mbar_fence_init();
     }
-    if (warp == 5) tmem_alloc(&sb.tmem_base, 256);
+    if (warp == 5) tmem_alloc(&sb.tmem_base, 512);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -137,6 +140,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__
             const int m = m0 + warp * 32 + lane;
             const bool live = m < g.M;
             for (int q = 0; q < kTN / 32; ++q) {
+                if (n0 + 32 * q >= g.N) break;               // past N: a half-width last tile
                 uint32_t v[32];
                 tmem_ld32(tl + b * kTN + 32 * q, v);
                 tmem_wait_ld(v);
@@ -195,7 +199,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__
     if (warp == 5) {
         __syncwarp();
         fence_after_sync();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc(tmem, 512);
     }
 }
 
@@ -203,7 +207,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__
 
 bool gemm_tc_supported(int M, int N, int K)
 {
-    return M > 0 && N > 0 && K > 0 && N % kTN == 0 && K % kTK == 0;
+    return M > 0 && N > 0 && K > 0 && N % 128 == 0 && K % kTK == 0;
 }
 
 cudaError_t gemm_tc(const GemmArgs &g, StatusBlock *status, cudaStream_t st)
@@ -215,7 +219,7 @@ cudaError_t gemm_tc(const GemmArgs &g, StatusBlock *status, cudaStream_t st)
         return cudaErrorNotSupported;
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int tiles = ((g.M + kTM - 1) / kTM) * (g.N / kTN);
+    const int tiles = ((g.M + kTM - 1) / kTM) * ((g.N + kTN - 1) / kTN);
     const int grid = tiles < sms ? tiles : sms;
     const size_t smem = 1024 + (size_t)kStages * kStageBytes;
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
