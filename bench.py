@@ -47,7 +47,18 @@ FP32_ALU_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
 # Where each kernel's arithmetic runs: the bf16 contractions (hash projection, QK^T and
 # P V) on the tensor cores, the fp32 ones on the CUDA cores' FFMA lanes.  A kernel's
 # bound is the slower of its FLOPs at that peak and its bytes at HBM bandwidth.
-COMPUTE_UNIT = {"bf16": "tensor", "f32": "alu"}
+COMPUTE_UNIT = {"bf16": "tensor", "f16": "tensor", "f32": "alu"}
+# fp16 and bf16 have the same nominal dense tensor rate, so fp16 contractions use the
+# measured bf16 peak.
+ESIZE = {"f32": 4, "bf16": 2, "f16": 2}
+
+
+def dt_code_of(lsh, w):
+    return {"f32": lsh.LSH_F32, "bf16": lsh.LSH_BF16, "f16": lsh.LSH_F16}[w.dtype]
+
+
+def torch_dtype_of(torch, w):
+    return {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[w.dtype]
 # Kernel sources per stage: a DRAM-traffic figure recorded from ncu counts only while
 # these files are unchanged.
 KERNEL_SOURCES = {
@@ -96,7 +107,7 @@ def recorded_traffic(workload, stage):
 def work(w):
     """Algorithmic FLOPs and bytes per kernel for one forward pass of workload w."""
     N, R, d, nb, c = w.tokens, w.n_rounds, w.d, w.n_buckets, w.chunk
-    e = 2 if w.dtype == "bf16" else 4
+    e = ESIZE[w.dtype]
     wr = e                                   # o_r element width
     S = w.B * w.H * R
     k = {}
@@ -117,7 +128,7 @@ def work_backward(w):
     gradients in q, k and v), 4 c d flops each; it reads qk, v, out, g_out, lse, g_lse,
     the inverse norms, buckets and perm once and writes dqk and dv once."""
     N, R, d, c = w.tokens, w.n_rounds, w.d, w.chunk
-    e = 2 if w.dtype == "bf16" else 4
+    e = ESIZE[w.dtype]
     k = work(w)
     return {
         "hash": k["hash"],
@@ -260,7 +271,7 @@ def near_tie_report(lsh, dev, keep, band=1e-5):
     R_r); the line reports both counts."""
     import torch
     sub = keep["sub"]
-    tdt = torch.bfloat16 if sub.dtype == "bf16" else torch.float32
+    tdt = torch_dtype_of(torch, sub)
     d_qk = torch.from_numpy(keep["qk"]).to(dev).to(tdt).contiguous()
     d_R = torch.from_numpy(keep["R"]).to(dev).to(tdt).contiguous()
     b, _ = lsh.lsh_hash(d_qk, d_R, sub.n_buckets)
@@ -414,8 +425,8 @@ def run_ours(args, w):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     lib = lsh.load()
-    dt_code = lsh.LSH_BF16 if w.dtype == "bf16" else lsh.LSH_F32
-    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    dt_code = dt_code_of(lsh, w)
+    tdt = torch_dtype_of(torch, w)
 
     qk, v, R = gen.make_inputs(w, seed=w.seed + 7919 * rank)
     h_qk = torch.from_numpy(qk).to(tdt).pin_memory()
@@ -527,8 +538,8 @@ def run_ours(args, w):
         "steps": K, "warmup": Wm, "ms_per_step": ms_max, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": dict(config_of(w), parallelism=f"replicas{world}",
-                       l2=f"inputs larger than L2: qk+v {2 * w.tokens * w.d * (2 if w.dtype == 'bf16' else 4) / 2**20:.0f} MiB, "
-                          f"per-round outputs {w.tokens * w.n_rounds * w.d * (2 if w.dtype == 'bf16' else 4) / 2**20:.0f} MiB "
+                       l2=f"inputs larger than L2: qk+v {2 * w.tokens * w.d * ESIZE[w.dtype] / 2**20:.0f} MiB, "
+                          f"per-round outputs {w.tokens * w.n_rounds * w.d * ESIZE[w.dtype] / 2**20:.0f} MiB "
                           f"> L2 126 MiB; no flush"),
         "roofline": roof(dom),
         "kernels": {n: roof(n) for n in stage_names},
@@ -566,8 +577,8 @@ def run_backward(args, w):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     lib = lsh.load()
-    dt_code = lsh.LSH_BF16 if w.dtype == "bf16" else lsh.LSH_F32
-    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    dt_code = dt_code_of(lsh, w)
+    tdt = torch_dtype_of(torch, w)
 
     qk, v, R = gen.make_inputs(w, seed=w.seed + 7919 * rank)
     rng = np.random.default_rng(w.seed + 5 + 7919 * rank)
@@ -690,7 +701,7 @@ def run_backward(args, w):
         "pass": "backward",
         "config": dict(config_of(w), parallelism=f"replicas{world}",
                        l2="inputs larger than L2: qk, v, out, g_out, dqk, dv "
-                          f"{w.tokens * w.d * (2 * (2 if w.dtype == 'bf16' else 4) + 16) / 2**20:.0f} MiB "
+                          f"{w.tokens * w.d * (2 * ESIZE[w.dtype] + 16) / 2**20:.0f} MiB "
                           "> L2 126 MiB; no flush"),
         "roofline": kernels[dom],
         "kernels": kernels,
@@ -718,7 +729,7 @@ def work_knn(w, k):
     gathered once per chunk (own and previous chunk: 2 d e bytes per token and round),
     per-round lists written and read back, and the final lists written."""
     N, R, d, c = w.tokens, w.n_rounds, w.d, w.chunk
-    e = 2 if w.dtype == "bf16" else 4
+    e = ESIZE[w.dtype]
     base = work(w)
     return {"hash": base["hash"], "sort": base["sort"],
             "knn": dict(flops=4 * N * R * c * d,
@@ -752,8 +763,8 @@ def run_knn(args, w):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     lib = lsh.load()
-    dt_code = lsh.LSH_BF16 if w.dtype == "bf16" else lsh.LSH_F32
-    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    dt_code = dt_code_of(lsh, w)
+    tdt = torch_dtype_of(torch, w)
     k = KNN_K
     qk, _, R = gen.make_inputs(w, seed=w.seed + 7919 * rank)
     h_qk = torch.from_numpy(qk).to(tdt).pin_memory()

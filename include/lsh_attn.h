@@ -36,7 +36,7 @@
  *        bstart    int32 [B][H][n_rounds][n_buckets+1]  first sorted index of each
  *                  bucket; bstart[n_buckets] = L
  *        o_r       [B][H][n_rounds][L][d] in SORTED order; bf16 when dtype is
- *                  LSH_BF16, fp32 when dtype is LSH_F32
+ *                  LSH_BF16 or LSH_F16, fp32 when dtype is LSH_F32
  *        lse_r     fp32 [B][H][n_rounds][L] in sorted order (natural log)
  *        out       fp32 [B][H][L][d];  lse fp32 [B][H][L]
  *  - Keys are L2-normalised and queries are not: the score of query i and key j is
@@ -71,13 +71,19 @@ typedef enum {
 
 typedef enum {
     LSH_F32 = 0,   /* fp32 inputs; CUDA-core arithmetic in fp32 */
-    LSH_BF16 = 1   /* bf16 inputs; tensor-core products with fp32 accumulation */
+    LSH_BF16 = 1,  /* bf16 inputs; tensor-core products with fp32 accumulation */
+    LSH_F16 = 2    /* fp16 inputs; as LSH_BF16 with fp16 operands (the softmax weights are
+                      packed to fp16 for P V, and rows whose score bound exceeds 7 in log2
+                      units take the exact row maximum, so the weights that matter stay
+                      normal fp16 numbers, >= 2^-14); per-round rows (o_r) are bf16 as for
+                      LSH_BF16.  Not taken by lsh_knn (LSH_ERR_UNSUPPORTED); the backward
+                      pass runs it on the CUDA cores in fp32. */
 } lsh_dtype_t;
 
 /*
  * Supported range (anything else returns LSH_ERR_UNSUPPORTED):
  *   d in {64, 128};  chunk in {32, 64};  2 <= n_buckets <= 2048;
- *   n_buckets % 16 == 0 for LSH_BF16;  B*H*n_rounds*L < 2^31.
+ *   n_buckets % 16 == 0 for LSH_BF16 and LSH_F16;  B*H*n_rounds*L < 2^31.
  */
 
 /* Human-readable name of a status code (static storage). */
@@ -269,7 +275,7 @@ lsh_status_t lsh_chunk_attn(const void *qk, const void *v, lsh_dtype_t dtype,
 /*
  * Steps 5-6, un-sort and combine rounds: for token i,
  * lse_i = logsumexp_r lse_r[inv_r[i]] and out_i = sum_r exp(lse_r[inv_r[i]] - lse_i)
- * o_r[inv_r[i]].  o_r is bf16 when dtype is LSH_BF16 and fp32 when LSH_F32.
+ * o_r[inv_r[i]].  o_r is bf16 when dtype is LSH_BF16 or LSH_F16 and fp32 when LSH_F32.
  * Every inv entry must lie in [0, L), as lsh_bucket_sort writes it.  An entry outside
  * that range is replaced by 0 (no read leaves the round's rows); that token's results
  * are then meaningless.

@@ -25,6 +25,7 @@ LSH_ERR_DEVICE_CHECK = 5
 
 LSH_F32 = 0
 LSH_BF16 = 1
+LSH_F16 = 2
 
 #: Every symbol the header declares.
 EXPORTS = (
@@ -133,7 +134,9 @@ def _dtype_code(t) -> int:
         return LSH_F32
     if t.dtype == torch.bfloat16:
         return LSH_BF16
-    raise TypeError(f"unsupported dtype {t.dtype}; use float32 or bfloat16")
+    if t.dtype == torch.float16:
+        return LSH_F16
+    raise TypeError(f"unsupported dtype {t.dtype}; use float32, bfloat16 or float16")
 
 
 def _ptr(t):
@@ -432,7 +435,10 @@ def lsh_chunk_attn(qk, v, buckets, perm, bstart, inv_norm, n_buckets, chunk, cau
     n_rounds = perm.shape[2]
     dt = _dtype_code(qk)
     if o_r is None:
-        o_r = torch.empty((B, H, n_rounds, L, d), dtype=qk.dtype, device=qk.device)
+        # per-round rows: fp32 for fp32 inputs, bf16 for both 16-bit input types
+        o_r = torch.empty((B, H, n_rounds, L, d),
+                          dtype=torch.float32 if qk.dtype == torch.float32 else torch.bfloat16,
+                          device=qk.device)
     if lse_r is None:
         lse_r = torch.empty((B, H, n_rounds, L), dtype=torch.float32, device=qk.device)
     if ws is None:
@@ -450,6 +456,8 @@ def lsh_unsort_combine(o_r, lse_r, inv, out=None, lse=None, stream=None):
     """Steps 5-6.  o_r [B, H, n_rounds, L, d] (sorted order) -> (out, lse)."""
     torch = _torch()
     B, H, n_rounds, L, d = o_r.shape
+    if o_r.dtype == torch.float16:
+        raise TypeError("per-round rows are float32 or bfloat16 (also for float16 inputs)")
     dt = _dtype_code(o_r)
     if out is None:
         out = torch.empty((B, H, L, d), dtype=torch.float32, device=o_r.device)

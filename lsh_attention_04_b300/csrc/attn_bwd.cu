@@ -265,6 +265,9 @@ cudaError_t attn_bwd(const Problem &p, const void *qk, const void *v, const int3
     if (p.dtype == LSH_BF16)
         return dispatch<__nv_bfloat16>(p, qk, v, buckets, perm, inv_norm, out, lse, g_out, g_lse,
                                        dqk, dv, st);
+    if (p.dtype == LSH_F16)
+        return dispatch<__half>(p, qk, v, buckets, perm, inv_norm, out, lse, g_out, g_lse, dqk,
+                                dv, st);
     return dispatch<float>(p, qk, v, buckets, perm, inv_norm, out, lse, g_out, g_lse, dqk, dv, st);
 }
 

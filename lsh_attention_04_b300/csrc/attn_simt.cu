@@ -21,13 +21,15 @@ namespace {
 
 constexpr int kWarps = 16;
 
-template <typename T, int D, int C>
+// T: input element type; TO: per-round row type (fp32 for fp32 inputs, bf16 for both
+// 16-bit input types)
+template <typename T, typename TO, int D, int C>
 __global__ void __launch_bounds__(kWarps * 32)
 attn_simt_kernel(const T *__restrict__ qk, const T *__restrict__ v,
                  const int32_t *__restrict__ buckets, const int32_t *__restrict__ perm,
                  const int32_t *__restrict__ bstart, const float *__restrict__ inv_norm, int L,
                  int n_rounds, int nb, int causal, float scale, int token_order,
-                 T *__restrict__ o_r, float *__restrict__ lse_r)
+                 TO *__restrict__ o_r, float *__restrict__ lse_r)
 {
     constexpr int KS = D + 1;  // padded key row: lanes reading different rows hit different banks
     extern __shared__ float smem[];
@@ -125,32 +127,32 @@ attn_simt_kernel(const T *__restrict__ qk, const T *__restrict__ v,
     }
 }
 
-template <typename T, int D, int C>
+template <typename T, typename TO, int D, int C>
 cudaError_t launch(const Problem &p, const void *qk, const void *v, const int32_t *buckets,
                    const int32_t *perm, const int32_t *bstart, const float *inv_norm, void *o_r,
                    float *lse_r, cudaStream_t st)
 {
     const size_t smem = sizeof(float) * (2 * C * (D + 1) + 2 * C * D + 2 * C) + sizeof(int) * 2 * C;
-    auto k = attn_simt_kernel<T, D, C>;
+    auto k = attn_simt_kernel<T, TO, D, C>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(p.L / C), (unsigned)p.n_seg());
     k<<<grid, kWarps * 32, smem, st>>>((const T *)qk, (const T *)v, buckets, perm, bstart,
                                        inv_norm, p.L, p.n_rounds, p.nb, p.causal, p.scale,
-                                       p.token_order, (T *)o_r, lse_r);
+                                       p.token_order, (TO *)o_r, lse_r);
     return cudaGetLastError();
 }
 
-template <typename T>
+template <typename T, typename TO>
 cudaError_t dispatch(const Problem &p, const void *qk, const void *v, const int32_t *buckets,
                      const int32_t *perm, const int32_t *bstart, const float *inv_norm, void *o_r,
                      float *lse_r, cudaStream_t st)
 {
     if (p.d == 64)
-        return p.chunk == 32 ? launch<T, 64, 32>(p, qk, v, buckets, perm, bstart, inv_norm, o_r, lse_r, st)
-                             : launch<T, 64, 64>(p, qk, v, buckets, perm, bstart, inv_norm, o_r, lse_r, st);
-    return p.chunk == 32 ? launch<T, 128, 32>(p, qk, v, buckets, perm, bstart, inv_norm, o_r, lse_r, st)
-                         : launch<T, 128, 64>(p, qk, v, buckets, perm, bstart, inv_norm, o_r, lse_r, st);
+        return p.chunk == 32 ? launch<T, TO, 64, 32>(p, qk, v, buckets, perm, bstart, inv_norm, o_r, lse_r, st)
+                             : launch<T, TO, 64, 64>(p, qk, v, buckets, perm, bstart, inv_norm, o_r, lse_r, st);
+    return p.chunk == 32 ? launch<T, TO, 128, 32>(p, qk, v, buckets, perm, bstart, inv_norm, o_r, lse_r, st)
+                         : launch<T, TO, 128, 64>(p, qk, v, buckets, perm, bstart, inv_norm, o_r, lse_r, st);
 }
 
 }  // namespace
@@ -160,8 +162,10 @@ cudaError_t attn_simt(const Problem &p, const void *qk, const void *v, const int
                       void *o_r, float *lse_r, cudaStream_t st)
 {
     if (p.dtype == LSH_F32)
-        return dispatch<float>(p, qk, v, buckets, perm, bstart, inv_norm, o_r, lse_r, st);
-    return dispatch<__nv_bfloat16>(p, qk, v, buckets, perm, bstart, inv_norm, o_r, lse_r, st);
+        return dispatch<float, float>(p, qk, v, buckets, perm, bstart, inv_norm, o_r, lse_r, st);
+    if (p.dtype == LSH_F16)
+        return dispatch<__half, __nv_bfloat16>(p, qk, v, buckets, perm, bstart, inv_norm, o_r, lse_r, st);
+    return dispatch<__nv_bfloat16, __nv_bfloat16>(p, qk, v, buckets, perm, bstart, inv_norm, o_r, lse_r, st);
 }
 
 }  // namespace lsh

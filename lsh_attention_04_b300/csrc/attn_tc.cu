@@ -1,5 +1,5 @@
-// attn_tc.cu -- chunked look-one-back LSH attention on the tcgen05 tensor cores (bf16
-// inputs, fp32 accumulation, chunk 64, d = 64 or 128).
+// attn_tc.cu -- chunked look-one-back LSH attention on the tcgen05 tensor cores (bf16 or
+// fp16 inputs, fp32 accumulation, chunk 64, d = 64 or 128).
 //
 // "Reformer" glossary (ultralytics.com), section "Atencion LSH": the bucket-sorted
 // sequence is cut into equal chunks; each token attends to its own chunk and the
@@ -35,7 +35,9 @@
 // score is also at least -m_i, so in log2 units p >= 2^(-2 m2) with m2 = m_i log2 e.
 // While m2 <= 32 that is >= 2^-64: far inside the normal range of fp32 and bf16 (ex2's
 // flush-to-zero starts below 2^-126), so no row can end with a zero sum.  Above that the
-// warp first takes the exact row maximum instead.  lse = m_i + log(sum p).
+// warp first takes the exact row maximum instead.  lse = m_i + log(sum p).  With fp16
+// inputs P is packed to fp16 for P V, whose smallest normal number is 2^-14, so there
+// the exact maximum takes over above m2 = 7.
 // Data movement: a ring of 6 chunk slots (chunk c in slot c mod 6) holds each chunk's
 // Q/K rows, V rows and row metadata, loaded once and released after the last P V that
 // reads the chunk.  Rows are gathered through the sort permutation by 16-byte cp.async
@@ -76,6 +78,9 @@ constexpr int kLBufs = 4;         // tiles of partial row sums kept in shared me
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kExactMaxLog2 = 32.f;   // bound path keeps every p >= 2^-64
+// fp16 P: the bound path keeps every p >= 2^-14, fp16's smallest normal number (its
+// subnormals carry too few bits: a weight near 2^-20 would keep four)
+constexpr float kExactMaxLog2F16 = 7.f;
 constexpr size_t kL2Budget = 48ull << 20;
 
 struct AttnPlan {
@@ -158,6 +163,10 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
@@ -186,6 +195,7 @@ __device__ __forceinline__ uint32_t range_mask(int lo, int hi) {
 // One 16-column quarter of a row: p_j = 2^(s_j * cs_j - m2) for the columns whose bit
 // is set in the low 16 bits of `vm`, 0 elsewhere (ex2 of -inf), packed to bf16 pairs.
 // Returns sum_j p_j.  `cs` is 16-byte aligned shared memory.
+template <bool F16>
 __device__ __forceinline__ float softmax_quarter(const uint32_t (&s16)[16], const float *cs,
                                                  uint32_t vm, float m2, uint32_t (&pk)[8]) {
     float la = 0.f, lb = 0.f;
@@ -200,14 +210,15 @@ __device__ __forceinline__ float softmax_quarter(const uint32_t (&s16)[16], cons
             const float x = fmaf(__uint_as_float(s16[jj]), c[e], -m2);
             p[e] = ex2((vm >> jj) & 1u ? x : -INFINITY);
         }
-        pk[2 * q] = pack_bf16(p[0], p[1]);
-        pk[2 * q + 1] = pack_bf16(p[2], p[3]);
+        pk[2 * q] = F16 ? pack_f16(p[0], p[1]) : pack_bf16(p[0], p[1]);
+        pk[2 * q + 1] = F16 ? pack_f16(p[2], p[3]) : pack_bf16(p[2], p[3]);
         la += p[0] + p[1];
         lb += p[2] + p[3];
     }
     return la + lb;
 }
 
+template <bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
 lsh_attn_tc_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *__restrict__ vv,
                    const AttnPlan P, const int32_t *__restrict__ buckets,
@@ -434,14 +445,14 @@ lsh_attn_tc_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *__
                         const uint64_t a = smem_desc(pb + s0 * kC * 128, 16, 1024);
                         if (joined) {
                             mma_ss(tmem + b * kWin, a, smem_desc(pb + (s0 - 1) * kC * 128, 16, 1024),
-                                   idesc_bf16(kRows, kWin, 0, 0), ks > 0);
+                                   idesc_16(kRows, kWin, 0, 0, F16), ks > 0);
                         } else {
                             if (t > 0)
                                 mma_ss(tmem + b * kWin, a,
                                        smem_desc(pb + (kSlots - 1) * kC * 128, 16, 1024),
-                                       idesc_bf16(kRows, kC, 0, 0), ks > 0);
+                                       idesc_16(kRows, kC, 0, 0, F16), ks > 0);
                             mma_ss(tmem + b * kWin + kC, a, smem_desc(pb + s0 * kC * 128, 16, 1024),
-                                   idesc_bf16(kRows, 2 * kC, 0, 0), ks > 0);
+                                   idesc_16(kRows, 2 * kC, 0, 0, F16), ks > 0);
                         }
                     }
                     mma_commit(smem_u32(&sb.s_full[b]));
@@ -456,7 +467,7 @@ lsh_attn_tc_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *__
         // ------------------------------------------------------------- P V issuer
         {
             const uint32_t v_base = smem_u32(V);
-            const uint32_t idesc = idesc_bf16(kRows, P.d, 0, 1);
+            const uint32_t idesc = idesc_16(kRows, P.d, 0, 1, F16);
             uint32_t v_bits = 0;
             int ctr = 0;
             auto needv = [&](int c) -> bool {
@@ -608,7 +619,7 @@ lsh_attn_tc_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *__
 
                 // optional exact maximum (huge |scale| |q|): both halves must agree on m2,
                 // so the warp pair computes it over the row's whole range
-                if (__any_sync(FULL, live && m2 > kExactMaxLog2)) {
+                if (__any_sync(FULL, live && m2 > (F16 ? kExactMaxLog2F16 : kExactMaxLog2))) {
                     float mx = -INFINITY;
                     const int cfull = hi_half ? kC : 0;
                     for (int c0 = cfull; c0 < cfull + 2 * kC; c0 += 32) {
@@ -657,12 +668,14 @@ lsh_attn_tc_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *__
                     const int h = q >> 1, hq = q & 1;
                     const int cc = colA + 32 * h;
                     uint32_t pk[8];
-                    l += softmax_quarter(sq, csb[h] + 16 * hq, vmb[h] >> (16 * hq), m2, pk);
+                    l += softmax_quarter<F16>(sq, csb[h] + 16 * hq, vmb[h] >> (16 * hq), m2, pk);
                     if (cc == self_c0) {
                         // a row with no key but itself: weight 1 on its own column (all
                         // its other columns are masked).  Selects, not a conditional store
                         // into pk, which would move pk to local memory.
-                        const uint32_t one = (lane & 1) ? 0x3F800000u : 0x00003F80u;
+                        // 1.0 in the operand type: bf16 0x3F80, fp16 0x3C00
+                        const uint32_t one16 = F16 ? 0x3C00u : 0x3F80u;
+                        const uint32_t one = (lane & 1) ? one16 << 16 : one16;
                         const int kself = self_only && (lane >> 4) == hq ? (lane & 15) >> 1 : -1;
 #pragma unroll
                         for (int k = 0; k < 8; ++k) pk[k] = k == kself ? one : pk[k];
@@ -752,7 +765,7 @@ size_t smem_bytes(const AttnPlan &P)
 
 bool attn_tc_supported(const Problem &p)
 {
-    return p.dtype == LSH_BF16 && p.chunk == kC && (p.d == 64 || p.d == 128);
+    return (p.dtype == LSH_BF16 || p.dtype == LSH_F16) && p.chunk == kC && (p.d == 64 || p.d == 128);
 }
 
 cudaError_t attn_tc(const Problem &p, const void *qk, const void *v, const int32_t *buckets,
@@ -765,11 +778,12 @@ cudaError_t attn_tc(const Problem &p, const void *qk, const void *v, const int32
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const size_t smem = smem_bytes(P);
-    cudaError_t e = cudaFuncSetAttribute(lsh_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    // qk and v rows are copied as bytes; only the MMA operand type and P's packing differ
+    auto kern = p.dtype == LSH_F16 ? lsh_attn_tc_kernel<true> : lsh_attn_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    lsh_attn_tc_kernel<<<sms, kThreads, smem, st>>>((const __nv_bfloat16 *)qk, (const __nv_bfloat16 *)v, P, buckets, perm, inv_norm,
-                                                    (__nv_bfloat16 *)o_r, lse_r, status);
+    kern<<<sms, kThreads, smem, st>>>((const __nv_bfloat16 *)qk, (const __nv_bfloat16 *)v, P, buckets, perm,
+                                      inv_norm, (__nv_bfloat16 *)o_r, lse_r, status);
     return cudaGetLastError();
 }
 

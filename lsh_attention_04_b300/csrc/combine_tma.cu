@@ -166,7 +166,7 @@ cudaError_t launch(const Problem &p, const void *o_r, const float *lse_r, float 
 
 bool combine_tma_supported(const Problem &p)
 {
-    return p.token_order && p.dtype == LSH_BF16 && p.n_rounds <= kMaxR && p.L % kT == 0 &&
+    return p.token_order && is16(p.dtype) && p.n_rounds <= kMaxR && p.L % kT == 0 &&
            (p.d == 64 || p.d == 128);
 }
 

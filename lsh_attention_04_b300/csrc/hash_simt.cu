@@ -103,6 +103,9 @@ cudaError_t hash_simt(const Problem &p, const void *qk, const void *R, int32_t *
     if (p.dtype == LSH_F32)
         return p.d == 64 ? launch<float, 64>(p, qk, R, buckets, inv_norm, st)
                          : launch<float, 128>(p, qk, R, buckets, inv_norm, st);
+    if (p.dtype == LSH_F16)
+        return p.d == 64 ? launch<__half, 64>(p, qk, R, buckets, inv_norm, st)
+                         : launch<__half, 128>(p, qk, R, buckets, inv_norm, st);
     return p.d == 64 ? launch<__nv_bfloat16, 64>(p, qk, R, buckets, inv_norm, st)
                      : launch<__nv_bfloat16, 128>(p, qk, R, buckets, inv_norm, st);
 }

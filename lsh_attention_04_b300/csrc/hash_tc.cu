@@ -1,4 +1,5 @@
-// hash_tc.cu -- angular LSH on the tcgen05 tensor cores (bf16 inputs, fp32 accumulation).
+// hash_tc.cu -- angular LSH on the tcgen05 tensor cores (bf16 or fp16 inputs, fp32
+// accumulation).
 //
 // "Reformer" glossary (ultralytics.com), section "Atencion LSH": project every token
 // with a random matrix R and take the position of the largest entry of [xR, -xR] as the
@@ -66,6 +67,7 @@ struct HashPlan {
     int n_groups, ctas_per_group, n_tiles;
     int group_bytes;      // bytes of one group's packed R image (stride in rpack)
     int x_stages;         // qk tile stages in shared memory
+    int f16;              // inputs are fp16 (else bf16)
 };
 
 // ---- geometry of chunk k of a group with nr rounds (host and device) ----
@@ -82,7 +84,7 @@ __host__ __device__ __forceinline__ int chunk_width(const HashPlan &P, int nr, i
 
 // ---- R pre-pack: R [n_rounds][d][half] -> per-group K-major SW128 images ----
 __global__ void __launch_bounds__(256)
-lsh_rpack_kernel(const __nv_bfloat16 *__restrict__ R, HashPlan P, uint8_t *__restrict__ rpack)
+lsh_rpack_kernel(const uint16_t *__restrict__ R, HashPlan P, uint8_t *__restrict__ rpack)
 {
     const int kch = P.d / 8;  // 16-byte pieces per packed row
     const long long total = (long long)P.n_rounds * P.hp * kch;
@@ -99,10 +101,10 @@ lsh_rpack_kernel(const __nv_bfloat16 *__restrict__ R, HashPlan P, uint8_t *__res
         const int width = chunk_width(P, nr, k);
         const size_t dst = (size_t)g * P.group_bytes + (size_t)chunk_col0(P, k) * P.d * 2 +
                            kmajor_sw128_off(n, c * 8, width);
-        __align__(16) __nv_bfloat16 v[8];
+        __align__(16) uint16_t v[8];       // 16-bit values moved as bits (zero is 0 in both types)
 #pragma unroll
         for (int e = 0; e < 8; ++e)
-            v[e] = jp < P.half ? R[((size_t)r * P.d + c * 8 + e) * P.half + jp] : __float2bfloat16_rn(0.f);
+            v[e] = jp < P.half ? R[((size_t)r * P.d + c * 8 + e) * P.half + jp] : (uint16_t)0;
         *reinterpret_cast<uint4 *>(rpack + dst) = *reinterpret_cast<const uint4 *>(v);
     }
 }
@@ -267,7 +269,7 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
                         if (!(ok = wait_w(&sb.tm_empty[b], ((use >> 1) & 1) ^ 1, abort_flag, status, 0x203))) break;
                         fence_after_sync();
                         const int width = chunk_width(P, nr, k);
-                        const uint32_t idesc = idesc_bf16(kTileM, width, 0, 0);
+                        const uint32_t idesc = idesc_16(kTileM, width, 0, 0, P.f16);
                         const uint32_t rbase = rs + chunk_col0(P, k) * P.d * 2;
                         for (int ks = 0; ks < P.d / 16; ++ks) {
                             const int kb = ks >> 2, ko = (ks & 3) * 32;
@@ -308,9 +310,10 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
                             const uint4 q = *reinterpret_cast<const uint4 *>(
                                 xt + kb * kTileM * 128 + row * 128 + ((c ^ (row & 7)) << 4));
                             const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&q);
+                            const __half2 *hh = reinterpret_cast<const __half2 *>(&q);
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
-                                const float2 f = __bfloat1622float2(h[e]);
+                                const float2 f = P.f16 ? __half22float2(hh[e]) : __bfloat1622float2(h[e]);
                                 acc = fmaf(f.x, f.x, acc);
                                 acc = fmaf(f.y, f.y, acc);
                             }
@@ -380,6 +383,7 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
 bool make_plan(const Problem &p, HashPlan &P, int num_sms)
 {
     P.n_tok = p.n_tok();
+    P.f16 = p.dtype == LSH_F16;
     P.L = p.L;
     P.d = p.d;
     P.half = p.nb / 2;
@@ -423,7 +427,7 @@ int num_sms_current()
 
 bool hash_tc_supported(const Problem &p)
 {
-    if (p.dtype != LSH_BF16) return false;
+    if (p.dtype != LSH_BF16 && p.dtype != LSH_F16) return false;
     HashPlan P;
     return make_plan(p, P, 148);
 }
@@ -442,13 +446,13 @@ cudaError_t hash_tc(const Problem &p, const void *qk, const void *R, void *rpack
 {
     HashPlan P;
     if (!make_plan(p, P, num_sms_current())) return cudaErrorNotSupported;
-    CUtensorMap xmap;
+    CUtensorMap xmap;       // the copy moves 16-bit values; the map's element type is only their size
     if (!make_tmap_2d_bf16(&xmap, qk, (uint64_t)P.n_tok, (uint64_t)p.d, 64, kTileM))
         return cudaErrorNotSupported;
     const long long pack_items = (long long)P.n_rounds * P.hp * (p.d / 8);
     const long long want = (pack_items + 255) / 256;
     const int pack_blocks = (int)(want < 4096 ? want : 4096);
-    lsh_rpack_kernel<<<pack_blocks, 256, 0, st>>>((const __nv_bfloat16 *)R, P, (uint8_t *)rpack);
+    lsh_rpack_kernel<<<pack_blocks, 256, 0, st>>>((const uint16_t *)R, P, (uint8_t *)rpack);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const size_t smem = smem_bytes(P);

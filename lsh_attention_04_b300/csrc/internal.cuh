@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -40,6 +41,9 @@ __device__ __forceinline__ float ld_f32(const float *p, size_t i) { return p[i];
 __device__ __forceinline__ float ld_f32(const __nv_bfloat16 *p, size_t i) {
     return __bfloat162float(p[i]);
 }
+__device__ __forceinline__ float ld_f32(const __half *p, size_t i) { return __half2float(p[i]); }
+// 16-bit inputs (bf16 or fp16) keep their per-round rows in bf16.
+inline bool is16(lsh_dtype_t t) { return t == LSH_BF16 || t == LSH_F16; }
 __device__ __forceinline__ void st_elem(float *p, size_t i, float x) { p[i] = x; }
 __device__ __forceinline__ void st_elem(__nv_bfloat16 *p, size_t i, float x) {
     p[i] = __float2bfloat16_rn(x);

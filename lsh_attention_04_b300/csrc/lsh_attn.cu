@@ -16,14 +16,14 @@ lsh_status_t validate(const Problem &p, bool check_chunk = true)
     if (nonpos(p.B) || nonpos(p.H) || nonpos(p.L) || nonpos(p.d) || nonpos(p.nb) ||
         nonpos(p.n_rounds) || (check_chunk && nonpos(p.chunk)))
         return LSH_ERR_INVALID_ARGUMENT;
-    if (p.dtype != LSH_F32 && p.dtype != LSH_BF16) return LSH_ERR_INVALID_ARGUMENT;
+    if (p.dtype != LSH_F32 && !is16(p.dtype)) return LSH_ERR_INVALID_ARGUMENT;
     if (p.nb % 2 != 0) return LSH_ERR_INVALID_ARGUMENT;          // R has nb/2 columns
     if (check_chunk && p.L % p.chunk != 0) return LSH_ERR_INVALID_ARGUMENT;  // equal chunks
     if (p.causal != 0 && p.causal != 1) return LSH_ERR_INVALID_ARGUMENT;
     if (p.d != 64 && p.d != 128) return LSH_ERR_UNSUPPORTED;
     if (check_chunk && p.chunk != 32 && p.chunk != 64) return LSH_ERR_UNSUPPORTED;
     if (p.nb > 2048) return LSH_ERR_UNSUPPORTED;
-    if (p.dtype == LSH_BF16 && p.nb % 16 != 0) return LSH_ERR_UNSUPPORTED;
+    if (is16(p.dtype) && p.nb % 16 != 0) return LSH_ERR_UNSUPPORTED;
     if ((long long)p.B * p.H * p.n_rounds * p.L >= (1LL << 31)) return LSH_ERR_UNSUPPORTED;
     return LSH_OK;
 }
@@ -392,7 +392,7 @@ lsh_status_t lsh_unsort_combine(const void *o_r, const float *lse_r, const int32
                                 float *out, float *lse, void *stream)
 {
     if (B <= 0 || H <= 0 || L <= 0 || n_rounds <= 0) return LSH_ERR_INVALID_ARGUMENT;
-    if (dtype != LSH_F32 && dtype != LSH_BF16) return LSH_ERR_INVALID_ARGUMENT;
+    if (dtype != LSH_F32 && !is16(dtype)) return LSH_ERR_INVALID_ARGUMENT;
     if (!o_r || !lse_r || !inv || !out || !lse) return LSH_ERR_INVALID_ARGUMENT;
     if (d != 64 && d != 128) return LSH_ERR_UNSUPPORTED;
     if ((long long)B * H * n_rounds * L >= (1LL << 31)) return LSH_ERR_UNSUPPORTED;
@@ -433,7 +433,7 @@ size_t lsh_knn_workspace_bytes(int B, int H, int L, int d, int n_buckets, int n_
                                int k, lsh_dtype_t dtype)
 {
     const Problem p = make_problem(B, H, L, d, n_buckets, n_rounds, chunk, 0, 1.f, dtype);
-    if (validate(p) != LSH_OK || !knn_k_ok(n_rounds, k)) return 0;
+    if (validate(p) != LSH_OK || !knn_k_ok(n_rounds, k) || dtype == LSH_F16) return 0;
     return knn_layout(p, k).total;
 }
 
@@ -444,6 +444,7 @@ lsh_status_t lsh_knn(const void *qk, const void *R, lsh_dtype_t dtype, int B, in
     const Problem p = make_problem(B, H, L, d, n_buckets, n_rounds, chunk, 0, 1.f, dtype);
     lsh_status_t s = validate(p);
     if (s != LSH_OK) return s;
+    if (dtype == LSH_F16) return LSH_ERR_UNSUPPORTED;        // bf16 or fp32 candidates only
     if (!knn_k_ok(n_rounds, k)) return LSH_ERR_INVALID_ARGUMENT;
     if (!qk || !R || !nn_idx || !nn_sim || !workspace) return LSH_ERR_INVALID_ARGUMENT;
     if (((uintptr_t)workspace) % 256 != 0) return LSH_ERR_INVALID_ARGUMENT;

@@ -37,6 +37,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+// The same for kind::f16 with fp16 A and B (operand format fields 0 instead of 1); the
+// two operands always share one type.
+__host__ __device__ constexpr uint32_t idesc_16(int M, int N, int a_mn, int b_mn, bool f16) {
+    return f16 ? (idesc_bf16(M, N, a_mn, b_mn) & ~((1u << 7) | (1u << 10)))
+               : idesc_bf16(M, N, a_mn, b_mn);
+}
 
 // Byte offset of element (row, k) of a K-major tile with 128-byte swizzle: 64 bf16 of K
 // per 128-byte row, blocks of `rows` rows per 64-wide K block, 8-row atoms of 1 KB.

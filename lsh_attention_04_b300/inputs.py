@@ -14,8 +14,8 @@ centres u_k = g / |g| with g ~ N(0, I_d); each token picks k uniformly and gets
 x = u_k * |h| + 0.3 * n with h, n ~ N(0, I_d) independent.  The cosine between
 x and its centre is then about 0.96, the "near" vector of the Reformer glossary
 page's hashing example.  Values v and the random rotations R are i.i.d. N(0, 1).
-bf16 workloads are rounded to bf16 (round-to-nearest-even) once, here, and both
-sides receive exactly those values.
+bf16 (fp16) workloads are rounded to bf16 (fp16) with round-to-nearest-even once, here,
+and both sides receive exactly those values.
 """
 from __future__ import annotations
 
@@ -32,7 +32,7 @@ class Workload:
     H: int
     L: int
     d: int
-    dtype: str          # "f32" or "bf16"
+    dtype: str          # "f32", "bf16" or "f16"
     n_buckets: int
     n_rounds: int
     chunk: int
@@ -76,6 +76,9 @@ WORKLOADS = {
     **_sweep(),
 }
 
+WORKLOADS["long_f16_B1_H8_L65536_d128_R8"] = WORKLOADS["long_B1_H8_L65536_d128_R8"].replace(
+    name="long_f16_B1_H8_L65536_d128_R8", dtype="f16")
+
 #: The headline workload: L = 64K, 8 rounds.
 HEADLINE = "long_B1_H8_L65536_d128_R8"
 
@@ -86,6 +89,11 @@ def round_bf16(a: np.ndarray) -> np.ndarray:
     u = a.view(np.uint32).astype(np.uint64)
     u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
     return u.astype(np.uint32).view(np.float32)
+
+
+def round_f16(a: np.ndarray) -> np.ndarray:
+    """Round float32 values to the nearest fp16 value (ties to even); returns float32."""
+    return np.asarray(a, np.float32).astype(np.float16).astype(np.float32)
 
 
 def _gauss(rng: np.random.Generator, shape) -> np.ndarray:
@@ -122,6 +130,8 @@ def make_inputs(w: Workload, seed: int | None = None):
     v = v.reshape(w.B, w.H, w.L, w.d)
     if w.dtype == "bf16":
         qk, v, R = round_bf16(qk), round_bf16(v), round_bf16(R)
+    elif w.dtype == "f16":
+        qk, v, R = round_f16(qk), round_f16(v), round_f16(R)
     return qk, v, R
 
 

@@ -231,6 +231,7 @@ def test_knn_workspace_sizing(lib):
     assert f(1, 1, 1024, 64, 32, 2, 64, 33, lsh.LSH_BF16) == 0     # k > 32
     assert f(1, 1, 1024, 64, 32, 16, 64, 32, lsh.LSH_BF16) == 0    # rounds * k > 256
     assert f(1, 1, 1000, 64, 32, 2, 64, 8, lsh.LSH_BF16) == 0      # L % chunk
+    assert f(1, 1, 1024, 64, 32, 2, 64, 8, lsh.LSH_F16) == 0       # fp16: not taken
 
 
 @no_device
@@ -241,6 +242,8 @@ def test_knn_workspace_sizing(lib):
     (dict(k=0), lsh.LSH_ERR_INVALID_ARGUMENT),
     (dict(k=40), lsh.LSH_ERR_INVALID_ARGUMENT),
     (dict(d=96), lsh.LSH_ERR_UNSUPPORTED),
+    (dict(dtype=lsh.LSH_F16), lsh.LSH_ERR_UNSUPPORTED),
+    (dict(dtype=3), lsh.LSH_ERR_INVALID_ARGUMENT),
     (dict(wsb=256), lsh.LSH_ERR_WORKSPACE_TOO_SMALL),
 ])
 def test_knn_argument_checks(lib, kw, expect):
@@ -328,3 +331,12 @@ def test_gemm_argument_checks(lib, kw, expect):
                            P(a["res"]), ctypes.c_float(1.0), P(a["of"]), P(a["ob"]), a["sL"],
                            a["sd"], P(a["ws"]), a["wsb"], None)
     assert st == expect
+
+
+def test_f16_workspace_matches_bf16(lib):
+    """fp16 inputs keep bf16 per-round rows: the same workspace as bf16."""
+    args = (1, 8, 65536, 128, 1024, 8, 64)
+    assert lib.lsh_attn_workspace_bytes(*args, lsh.LSH_F16) == \
+        lib.lsh_attn_workspace_bytes(*args, lsh.LSH_BF16)
+    assert lib.lsh_attn_workspace_bytes(1, 1, 1024, 64, 40, 1, 64, lsh.LSH_F16) == 0   # nb % 16
+    assert lib.lsh_attn_workspace_bytes(1, 1, 1024, 64, 32, 1, 64, 3) == 0

@@ -33,6 +33,12 @@ SMALL = [
     W("bf16_nb2048_L4096_d128", 1, 1, 4096, 128, "bf16", 2048, 1, 64, True, 64, 16),
     W("f32_nb2_B1_H2_L256", 1, 2, 256, 64, "f32", 2, 3, 32, True, 0, 17),
     W("bf16_chunk32_L1024_d64", 1, 2, 1024, 64, "bf16", 32, 2, 32, True, 16, 18),
+    # fp16 inputs: the tensor-core hash and attention with fp16 operands (chunk 64), the
+    # SIMT attention (chunk 32) and the SIMT hash (an R group too large at nb = 2048)
+    W("f16_B2_H2_L1344_d64_R4", 2, 2, 1344, 64, "f16", 64, 4, 64, True, 16, 19),
+    W("f16_B1_H2_L2048_d128_R3_noncausal", 1, 2, 2048, 128, "f16", 32, 3, 64, False, 8, 20),
+    W("f16_chunk32_L1024_d128", 1, 1, 1024, 128, "f16", 32, 2, 32, True, 16, 21),
+    W("f16_nb2048_L4096_d128", 1, 1, 4096, 128, "f16", 2048, 1, 64, True, 64, 22),
 ]
 ids = [w.name for w in SMALL]
 
@@ -180,11 +186,12 @@ def test_unsort_combine_parity(w):
         for r in range(w.n_rounds):
             _, inv[h, r], _ = oracle.sort(keys[h, r], w.n_buckets)
     o, lse = gen.synthetic_round_outputs(rng, nh * w.n_rounds, w.L, w.d)
-    if w.dtype == "bf16":
+    o_dtype = "f32" if w.dtype == "f32" else "bf16"       # per-round rows of 16-bit inputs
+    if o_dtype == "bf16":
         o = gen.round_bf16(o)
     o = o.reshape(nh, w.n_rounds, w.L, w.d)
     lse = lse.reshape(nh, w.n_rounds, w.L)
-    do = P.to_device(o, w.dtype).reshape(w.B, w.H, w.n_rounds, w.L, w.d)
+    do = P.to_device(o, o_dtype).reshape(w.B, w.H, w.n_rounds, w.L, w.d)
     dl = torch.from_numpy(lse).cuda().reshape(w.B, w.H, w.n_rounds, w.L)
     di = torch.from_numpy(inv).cuda().reshape(w.B, w.H, w.n_rounds, w.L)
     out, l = lsh.lsh_unsort_combine(do, dl, di)
@@ -237,14 +244,14 @@ def test_unsort_combine_bad_inv_is_clamped():
 
 def _forward_gpu(w, dqk, dv, dR):
     ws = lsh.workspace(w.B, w.H, w.L, w.d, w.n_buckets, w.n_rounds, w.chunk,
-                       lsh.LSH_BF16 if w.dtype == "bf16" else lsh.LSH_F32)
+                       P.dtype_code(w.dtype))
     out, lse = lsh.lsh_attn_forward(dqk, dv, dR, w.n_buckets, w.chunk, w.causal, w.scale, ws=ws)
     return out, lse, ws
 
 
 def _ws_view(w, ws, name):
     lay = lsh.lsh_attn_workspace_layout(w.B, w.H, w.L, w.d, w.n_buckets, w.n_rounds, w.chunk,
-                                        lsh.LSH_BF16 if w.dtype == "bf16" else lsh.LSH_F32)
+                                        P.dtype_code(w.dtype))
     n = w.B * w.H * w.n_rounds * w.L
     return ws[lay[name]: lay[name] + 4 * n].view(torch.int32).reshape(-1, w.n_rounds, w.L)
 
@@ -366,6 +373,8 @@ def _antiparallel_inputs(w, m2_lo, m2_hi):
     R = np.zeros((w.n_rounds, w.d, w.n_buckets // 2), np.float32)
     if w.dtype == "bf16":
         qk, v = gen.round_bf16(qk), gen.round_bf16(v)
+    elif w.dtype == "f16":
+        qk, v = gen.round_f16(qk), gen.round_f16(v)
     return qk, v, R
 
 
@@ -378,6 +387,10 @@ BOUND_CASES = [
     (W("bound_bf16_m2_55_70_d128_noncausal", 1, 1, 1024, 128, "bf16", 16, 1, 64, False, 0, 43),
      55.0, 70.0),
     (W("bound_f32_m2_55_70", 1, 2, 1024, 64, "f32", 2, 2, 64, True, 0, 44), 55.0, 70.0),
+    # fp16: the bound path down to 2^-14 (m2 = 7), fp16's smallest normal weight, and the
+    # exact maximum past it
+    (W("bound_f16_m2_4_10", 1, 2, 1024, 64, "f16", 16, 2, 64, True, 0, 46), 4.0, 10.0),
+    (W("bound_f16_m2_10_20_d128", 1, 2, 1024, 128, "f16", 16, 1, 64, True, 0, 47), 10.0, 20.0),
 ]
 
 
@@ -403,7 +416,8 @@ def test_softmax_bound_extremes(w, lo, hi):
 
 # Every workload: the three small-to-image ones and all 24 points of the length sweep.
 FULL_ALL = ["gauss_f32_B1_H1_L1024_d64", "clustered_B8_H8_L4096_d64_R4",
-            "image_B8_H8_L12288_d128_R8", "long_B1_H8_L65536_d128_R8"] + \
+            "image_B8_H8_L12288_d128_R8", "long_B1_H8_L65536_d128_R8",
+            "long_f16_B1_H8_L65536_d128_R8"] + \
     sorted(n for n in gen.WORKLOADS if n.startswith("sweep_"))
 FULL = ["gauss_f32_B1_H1_L1024_d64", "clustered_B8_H8_L4096_d64_R4", "image_B8_H8_L12288_d128_R8",
         "long_B1_H8_L65536_d128_R8", "sweep_B128_H8_L1024_d64_R8", "sweep_B4_H8_L32768_d64_R8",

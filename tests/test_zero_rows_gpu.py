@@ -24,6 +24,7 @@ W = gen.Workload
 CASES = [
     W("zero_rows_bf16_B1_H2_L1344_d128_R2", 1, 2, 1344, 128, "bf16", 32, 2, 64, True, 16, 61),
     W("zero_rows_f32_B1_H1_L1024_d64_R2_noncausal", 1, 1, 1024, 64, "f32", 16, 2, 32, False, 0, 62),
+    W("zero_rows_f16_B1_H1_L1024_d128_R2", 1, 1, 1024, 128, "f16", 32, 2, 64, True, 16, 63),
 ]
 ZERO = [0, 1, 2, 63, 64, 500, 1023]       # first rows, a chunk boundary, a middle row
 
@@ -75,7 +76,7 @@ def test_zero_rows(w):
 
     out, lse = lsh.lsh_attn_forward(dq_, dv_, dR, w.n_buckets, w.chunk, w.causal, w.scale)
     torch.cuda.synchronize()
-    tol = 2e-2 if w.dtype == "bf16" else 1e-4
+    tol = P.TOL_OUT[w.dtype]
     P.check_close(out.cpu().numpy(), out_o, tol, f"{w.name} out")
     P.check_lse(lse.cpu().numpy(), lse_o, tol, f"{w.name} lse")
 
