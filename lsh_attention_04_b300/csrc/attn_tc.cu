@@ -1,5 +1,7 @@
 // attn_tc.cu -- chunked look-one-back LSH attention on the tcgen05 tensor cores (bf16 or
-// fp16 inputs, fp32 accumulation, chunk 64, d = 64 or 128).
+// fp16 inputs, fp32 accumulation, chunk 64 or 32, d = 64 or 128).  Chunk 32 runs on the
+// same 64-row chunks with each row's keys clipped to its own 32-row chunk and the one
+// before (a sub-window of its 64-row window), so L must then be a multiple of 64.
 //
 // "Reformer" glossary (ultralytics.com), section "Atencion LSH": the bucket-sorted
 // sequence is cut into equal chunks; each token attends to its own chunk and the
@@ -86,7 +88,8 @@ constexpr size_t kL2Budget = 48ull << 20;
 struct AttnPlan {
     int L, d, nb, n_rounds, causal, token_order;
     float scale;
-    int nchunks, tps;            // chunks and 128-row tiles per segment
+    int nchunks, tps;            // 64-row chunks and 128-row tiles per segment
+    int window;                  // the attention chunk: 64, or 32 (a sub-window, see below)
     int n_heads, heads_per_group, n_groups;
 };
 
@@ -603,6 +606,13 @@ lsh_attn_tc_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *__
                              : (cq - 1) * kC + 63 - __clzll((long long)sp);
                     const unsigned long long em = mq.ends & (~0ull << r);
                     khi = P.causal ? srow : (em ? cq * kC + __ffsll((long long)em) : (cq + 1) * kC);
+                    if (P.window == 32) {
+                        // chunks of 32: the row's window is its 32-chunk and the one before,
+                        // which lie inside its 64-row window; clip the run to it
+                        const int w0 = (srow & ~31) - 32;
+                        klo = max(klo, w0);
+                        khi = min(khi, w0 + 64);
+                    }
                     m2 = mq.m2[r];
                 }
                 // keys other than the row itself?
@@ -744,6 +754,7 @@ bool make_plan(const Problem &p, AttnPlan &P)
     P.token_order = p.token_order;
     P.scale = p.scale;
     P.nchunks = p.L / kC;
+    P.window = p.chunk;
     P.tps = (P.nchunks + 1) / 2;
     P.n_heads = p.B * p.H;
     const size_t head_bytes = (size_t)p.L * p.d * 2 * 2;
@@ -765,7 +776,9 @@ size_t smem_bytes(const AttnPlan &P)
 
 bool attn_tc_supported(const Problem &p)
 {
-    return (p.dtype == LSH_BF16 || p.dtype == LSH_F16) && p.chunk == kC && (p.d == 64 || p.d == 128);
+    // chunk 32 runs as 64-row chunks with each row's keys clipped to its 32-row window
+    return (p.dtype == LSH_BF16 || p.dtype == LSH_F16) && (p.d == 64 || p.d == 128) &&
+           (p.chunk == kC || (p.chunk == 32 && p.L % kC == 0));
 }
 
 cudaError_t attn_tc(const Problem &p, const void *qk, const void *v, const int32_t *buckets,

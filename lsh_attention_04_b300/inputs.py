@@ -79,6 +79,9 @@ WORKLOADS = {
 WORKLOADS["long_f16_B1_H8_L65536_d128_R8"] = WORKLOADS["long_B1_H8_L65536_d128_R8"].replace(
     name="long_f16_B1_H8_L65536_d128_R8", dtype="f16")
 
+WORKLOADS["long_chunk32_B1_H8_L65536_d128_R8"] = WORKLOADS["long_B1_H8_L65536_d128_R8"].replace(
+    name="long_chunk32_B1_H8_L65536_d128_R8", chunk=32)
+
 #: The headline workload: L = 64K, 8 rounds.
 HEADLINE = "long_B1_H8_L65536_d128_R8"
 

@@ -33,6 +33,10 @@ SMALL = [
     W("bf16_nb2048_L4096_d128", 1, 1, 4096, 128, "bf16", 2048, 1, 64, True, 64, 16),
     W("f32_nb2_B1_H2_L256", 1, 2, 256, 64, "f32", 2, 3, 32, True, 0, 17),
     W("bf16_chunk32_L1024_d64", 1, 2, 1024, 64, "bf16", 32, 2, 32, True, 16, 18),
+    # chunk 32 on the tensor-core path (L % 64 = 0), non-causal too; and the SIMT path
+    # (L = 1056 is not a multiple of 64)
+    W("bf16_chunk32_L2048_d128_noncausal", 1, 2, 2048, 128, "bf16", 64, 3, 32, False, 32, 23),
+    W("bf16_chunk32_L1056_d64_simt", 1, 1, 1056, 64, "bf16", 32, 2, 32, True, 16, 24),
     # fp16 inputs: the tensor-core hash and attention with fp16 operands (chunk 64), the
     # SIMT attention (chunk 32) and the SIMT hash (an R group too large at nb = 2048)
     W("f16_B2_H2_L1344_d64_R4", 2, 2, 1344, 64, "f16", 64, 4, 64, True, 16, 19),
