@@ -421,7 +421,7 @@ def test_softmax_bound_extremes(w, lo, hi):
 # Every workload: the three small-to-image ones and all 24 points of the length sweep.
 FULL_ALL = ["gauss_f32_B1_H1_L1024_d64", "clustered_B8_H8_L4096_d64_R4",
             "image_B8_H8_L12288_d128_R8", "long_B1_H8_L65536_d128_R8",
-            "long_f16_B1_H8_L65536_d128_R8"] + \
+            "long_f16_B1_H8_L65536_d128_R8", "long_chunk32_B1_H8_L65536_d128_R8"] + \
     sorted(n for n in gen.WORKLOADS if n.startswith("sweep_"))
 FULL = ["gauss_f32_B1_H1_L1024_d64", "clustered_B8_H8_L4096_d64_R4", "image_B8_H8_L12288_d128_R8",
         "long_B1_H8_L65536_d128_R8", "sweep_B128_H8_L1024_d64_R8", "sweep_B4_H8_L32768_d64_R8",
