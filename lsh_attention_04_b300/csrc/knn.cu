@@ -14,11 +14,13 @@
 //      through the permutation into shared memory; the chunk x window similarity tile is
 //      computed on the tensor cores with warp-level bf16 MMA (fp32 accumulation; fp32
 //      inputs use an fp32 FMA loop), then each warp takes rows and keeps the k best
-//      same-bucket candidates by k rounds of a warp-wide argmax.  Lists go to a per-round
-//      buffer at the token's position.
-//   2. knn_merge_kernel, one warp per token: the rounds' lists merged by the same k-round
-//      argmax; a token found in several rounds has the same similarity in each (same
-//      arithmetic), and every copy of a winner is retired at once, so it is listed once.
+//      same-bucket candidates: 64-bit keys (similarity, then smaller index) sorted in
+//      32-entry blocks by a bitonic network across the lanes and the blocks' top 32
+//      merged.  Lists go to a per-round buffer at the token's position.
+//   2. knn_merge_kernel, four tokens per warp: the rounds' sorted lists folded in one at a
+//      time by the bitonic top-32 merge; a token found in several rounds has the same key
+//      in each (the same similarity by the same arithmetic), so before each fold the list
+//      drops the keys the running result already holds.
 #include <limits.h>
 #include <math.h>
 #include <mma.h>
@@ -39,51 +41,56 @@ template <typename T> struct XRow;
 template <> struct XRow<__nv_bfloat16> { static constexpr int pad = 8; };   // 16-byte rows for wmma
 template <> struct XRow<float> { static constexpr int pad = 1; };           // odd pitch: no bank conflicts
 
-// k best (largest similarity, then smallest index) of Q independent lists held across a
-// warp, lane-major: list q has entries sim[q][m], idx[q][m], live[q][m] on every lane.
-// k rounds of a warp-wide argmax; the Q lists' shuffle chains are independent, so they
-// overlap.  Lane a < k ends with entry a of each list in out_idx[q], out_sim[q] (-1, -2
-// when the list has fewer than k live entries).  Every copy of a winner's index retires.
-template <int Q, int NE>
-__device__ __forceinline__ void warp_top_k(const float (&sim)[Q][NE], const int (&idx)[Q][NE],
-                                           bool (&live)[Q][NE], int k, int lane,
-                                           int (&out_idx)[Q], float (&out_sim)[Q]) {
+// Candidate keys: (similarity, then smaller token index) as one 64-bit integer, so a
+// larger key is a better candidate: the float's bits in an order-preserving form in the
+// high word, the complement of the index in the low word; 0 for a dead entry (every live
+// key is larger, the smallest finite float mapping to 0x00800000 in the high word).
+__device__ __forceinline__ unsigned long long cand_key(float sim, int idx, bool live)
+{
+    unsigned u = sim == 0.f ? 0u : __float_as_uint(sim);       // -0 ranks as +0
+    u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return live ? ((unsigned long long)u << 32) | (unsigned)(~idx) : 0ull;
+}
+
+__device__ __forceinline__ float key_sim(unsigned long long key)
+{
+    unsigned u = (unsigned)(key >> 32);
+    u = (u & 0x80000000u) ? (u & 0x7fffffffu) : ~u;
+    return __uint_as_float(u);
+}
+
+__device__ __forceinline__ unsigned long long kmax(unsigned long long a, unsigned long long b) { return a > b ? a : b; }
+__device__ __forceinline__ unsigned long long kmin(unsigned long long a, unsigned long long b) { return a < b ? a : b; }
+
+// One key per lane sorted descending across the warp (lane 0 the largest): a bitonic
+// network of 15 compare-exchange stages over lane pairs.
+__device__ __forceinline__ unsigned long long warp_sort_desc(unsigned long long x, int lane)
+{
 #pragma unroll
-    for (int q = 0; q < Q; ++q) { out_idx[q] = -1; out_sim[q] = -2.f; }
-    for (int a = 0; a < k; ++a) {
-        float bs[Q];
-        int bj[Q];
+    for (int size = 2; size <= 32; size <<= 1) {
 #pragma unroll
-        for (int q = 0; q < Q; ++q) {
-            bs[q] = -INFINITY;
-            bj[q] = INT_MAX;
-#pragma unroll
-            for (int m = 0; m < NE; ++m)
-                if (live[q][m] && (sim[q][m] > bs[q] || (sim[q][m] == bs[q] && idx[q][m] < bj[q]))) {
-                    bs[q] = sim[q][m];
-                    bj[q] = idx[q][m];
-                }
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const unsigned long long y = __shfl_xor_sync(0xffffffffu, x, stride);
+            const bool keep_max = ((lane & stride) == 0) == ((lane & size) == 0);
+            x = keep_max ? kmax(x, y) : kmin(x, y);
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-#pragma unroll
-            for (int q = 0; q < Q; ++q) {
-                const float os = __shfl_xor_sync(0xffffffffu, bs[q], off);
-                const int oj = __shfl_xor_sync(0xffffffffu, bj[q], off);
-                if (os > bs[q] || (os == bs[q] && oj < bj[q])) { bs[q] = os; bj[q] = oj; }
-            }
-        }
-        bool any = false;
-#pragma unroll
-        for (int q = 0; q < Q; ++q) {
-            if (bj[q] == INT_MAX) continue;          // this list has run out
-            any = true;
-            if (lane == a) { out_idx[q] = bj[q]; out_sim[q] = bs[q]; }
-#pragma unroll
-            for (int m = 0; m < NE; ++m) live[q][m] = live[q][m] && idx[q][m] != bj[q];
-        }
-        if (!any) break;                             // warp-uniform: every list ran out
     }
+    return x;
+}
+
+// The 32 largest of two descending lane-sorted sequences, sorted descending: the
+// elementwise maximum of one and the other reversed is bitonic and holds them; five
+// merge stages sort it.
+__device__ __forceinline__ unsigned long long warp_top32_of_two(unsigned long long a,
+                                                                unsigned long long b, int lane)
+{
+    unsigned long long x = kmax(a, __shfl_sync(0xffffffffu, b, 31 - lane));
+#pragma unroll
+    for (int stride = 16; stride > 0; stride >>= 1) {
+        const unsigned long long y = __shfl_xor_sync(0xffffffffu, x, stride);
+        x = (lane & stride) == 0 ? kmax(x, y) : kmin(x, y);
+    }
+    return x;
 }
 
 template <typename T, int D>
@@ -175,12 +182,14 @@ knn_round_kernel(const T *__restrict__ qk, const int32_t *__restrict__ buckets,
     __syncthreads();
 
     // ---- per row: the k best same-bucket candidates of the window (self left out),
-    // kRowsInFlight rows of a warp at once
+    // kRowsInFlight rows of a warp at once.  The row's candidates are its bucket's run in
+    // the window, cut into 32-entry blocks across the lanes: each block is sorted by key
+    // and the blocks' top 32 are merged; lane a ends with the row's a-th best.
     constexpr int NE = kWinMax / 32;
+    static_assert(NE == 4, "four 32-entry blocks per window");
     for (int rb = warp * kRowsInFlight; rb < chunk; rb += kKnnWarps * kRowsInFlight) {
-        float sim[kRowsInFlight][NE];
-        int idx[kRowsInFlight][NE];
-        bool live[kRowsInFlight][NE];
+        unsigned long long key[kRowsInFlight][NE], top[kRowsInFlight];
+        int nblk = 0;                                      // warp-uniform, over the rows
 #pragma unroll
         for (int q = 0; q < kRowsInFlight; ++q) {
             const int r = rb + q;
@@ -188,32 +197,95 @@ knn_round_kernel(const T *__restrict__ qk, const int32_t *__restrict__ buckets,
             const int ws = r0 + (row_ok ? r : 0);
             const int bs_ = sb[ws];
             const float ns = sn[ws];
+            // the window is in sorted order, so the row's bucket is one run [a, b) of it:
+            // only the blocks that run covers are sorted
+            int a = kWinMax, b = 0;
 #pragma unroll
             for (int m = 0; m < NE; ++m) {
-                const int w = lane + 32 * m;
-                live[q][m] = row_ok && w < n_win && w != ws && sb[w] == bs_;
-                sim[q][m] = live[q][m] ? S[r * kSPitch + w] * ns * sn[w] : -INFINITY;
-                idx[q][m] = live[q][m] ? sj[w] : INT_MAX;
+                const unsigned bal = __ballot_sync(0xffffffffu, lane + 32 * m < n_win && sb[lane + 32 * m] == bs_);
+                if (bal) {
+                    a = min(a, 32 * m + __ffs(bal) - 1);
+                    b = max(b, 32 * m + 32 - __clz(bal));
+                }
             }
+            if (row_ok && b > a) nblk = max(nblk, (b - a + 31) / 32);
+#pragma unroll
+            for (int m = 0; m < NE; ++m) {
+                const int w = a + lane + 32 * m;
+                const bool live = row_ok && w < b && w != ws;
+                key[q][m] = cand_key(live ? S[r * kSPitch + w] * ns * sn[w] : 0.f,
+                                     live ? sj[w] : 0, live);
+            }
+            top[q] = 0ull;
         }
-        int out_idx[kRowsInFlight];
-        float out_sim[kRowsInFlight];
-        warp_top_k(sim, idx, live, k, lane, out_idx, out_sim);
+        // the rows' sorting networks interleave (independent shuffle chains)
+        if (nblk >= 1) {
+#pragma unroll
+            for (int q = 0; q < kRowsInFlight; ++q) top[q] = warp_sort_desc(key[q][0], lane);
+        }
+        if (nblk >= 2) {
+#pragma unroll
+            for (int q = 0; q < kRowsInFlight; ++q)
+                top[q] = warp_top32_of_two(top[q], warp_sort_desc(key[q][1], lane), lane);
+        }
+        if (nblk == 3) {
+#pragma unroll
+            for (int q = 0; q < kRowsInFlight; ++q)
+                top[q] = warp_top32_of_two(top[q], warp_sort_desc(key[q][2], lane), lane);
+        }
+        if (nblk == 4) {
+#pragma unroll
+            for (int q = 0; q < kRowsInFlight; ++q)
+                top[q] = warp_top32_of_two(top[q], warp_top32_of_two(warp_sort_desc(key[q][2], lane),
+                                                                     warp_sort_desc(key[q][3], lane), lane), lane);
+        }
         if (lane < k) {
 #pragma unroll
             for (int q = 0; q < kRowsInFlight; ++q) {
                 const int r = rb + q;
                 if (r >= chunk) break;
                 const size_t o = ((size_t)seg * L + sj[r0 + r]) * k + lane;
-                cand_idx[o] = out_idx[q];
-                cand_sim[o] = out_sim[q];
+                cand_idx[o] = top[q] ? (int)~(unsigned)top[q] : -1;
+                cand_sim[o] = top[q] ? key_sim(top[q]) : -2.f;
             }
         }
     }
 }
 
-// NE entries per lane; a warp merges Q tokens at once
-template <int NE, int Q>
+// Closes the gaps of a descending lane-sorted sequence whose dropped entries are 0:
+// lane l takes the l-th kept entry, the freed lanes at the end become 0.
+__device__ __forceinline__ unsigned long long warp_compact_desc(unsigned long long x, int lane)
+{
+    const unsigned mask = __ballot_sync(0xffffffffu, x != 0ull);
+    const int n = __popc(mask);
+    const int src = lane < n ? (int)__fns(mask, 0, lane + 1) : 0;
+    const unsigned long long y = __shfl_sync(0xffffffffu, x, src);
+    return lane < n ? y : 0ull;
+}
+
+// x (descending lane-sorted, distinct keys) without the keys that also occur in acc
+// (descending lane-sorted, distinct): each lane finds its key in acc by a five-step binary
+// search over the lanes, then the sequence is compacted.
+__device__ __forceinline__ unsigned long long warp_remove_present(unsigned long long x,
+                                                                  unsigned long long acc, int lane)
+{
+    int lo = 0;                                   // entries of acc greater than x
+#pragma unroll
+    for (int step = 16; step > 0; step >>= 1) {
+        const unsigned long long v = __shfl_sync(0xffffffffu, acc, lo + step - 1);
+        if (v > x) lo += step;
+    }
+    const unsigned long long at = __shfl_sync(0xffffffffu, acc, lo & 31);
+    const bool present = x != 0ull && lo < 32 && at == x;
+    return warp_compact_desc(present ? 0ull : x, lane);
+}
+
+// One warp merges the rounds' lists of Q tokens: each list is sorted (the round kernel
+// writes entry a at lane a), so the lists are folded in one at a time by the bitonic
+// top-32 merge; before each fold the list loses the tokens the running result already
+// holds (the same key: the same similarity by the same arithmetic, and the same index),
+// so the merged 32 are distinct.
+template <int Q>
 __global__ void __launch_bounds__(256)
 knn_merge_kernel(const int32_t *__restrict__ cand_idx, const float *__restrict__ cand_sim,
                  long n_tok, int L, int n_rounds, int k, int32_t *__restrict__ nn_idx,
@@ -221,39 +293,33 @@ knn_merge_kernel(const int32_t *__restrict__ cand_idx, const float *__restrict__
 {
     const long tok0 = ((long)blockIdx.x * 8 + (threadIdx.x >> 5)) * Q;
     const int lane = threadIdx.x & 31;
-    if (tok0 >= n_tok) return;
-    const int n_e = n_rounds * k;
-    float sim[Q][NE];
-    int idx[Q][NE];
-    bool live[Q][NE];
-#pragma unroll
-    for (int q = 0; q < Q; ++q) {
+    if (tok0 >= n_tok) return;                          // warp-uniform
+    auto list = [&](int q, int r) -> unsigned long long {
         const long tok = tok0 + q;
+        if (tok >= n_tok || lane >= k) return 0ull;
         const long bh = tok / L, l = tok % L;
+        const size_t o = (((size_t)bh * n_rounds + r) * L + l) * k + lane;
+        const int j = cand_idx[o];
+        return j >= 0 ? cand_key(cand_sim[o], j, true) : 0ull;
+    };
+    unsigned long long acc[Q];
 #pragma unroll
-        for (int m = 0; m < NE; ++m) {
-            const int e = lane + 32 * m;
-            live[q][m] = false;
-            sim[q][m] = -INFINITY;
-            idx[q][m] = INT_MAX;
-            if (tok < n_tok && e < n_e) {
-                const int r = e / k, a = e % k;
-                const size_t o = (((size_t)bh * n_rounds + r) * L + l) * k + a;
-                const int j = cand_idx[o];
-                if (j >= 0) { live[q][m] = true; idx[q][m] = j; sim[q][m] = cand_sim[o]; }
-            }
-        }
+    for (int q = 0; q < Q; ++q) acc[q] = list(q, 0);
+    for (int r = 1; r < n_rounds; ++r) {
+        unsigned long long nx[Q];
+#pragma unroll
+        for (int q = 0; q < Q; ++q) nx[q] = list(q, r);
+#pragma unroll
+        for (int q = 0; q < Q; ++q)
+            acc[q] = warp_top32_of_two(acc[q], warp_remove_present(nx[q], acc[q], lane), lane);
     }
-    int out_idx[Q];
-    float out_sim[Q];
-    warp_top_k(sim, idx, live, k, lane, out_idx, out_sim);
     if (lane < k) {
 #pragma unroll
         for (int q = 0; q < Q; ++q) {
             const long tok = tok0 + q;
             if (tok >= n_tok) break;
-            nn_idx[(size_t)tok * k + lane] = out_idx[q];
-            nn_sim[(size_t)tok * k + lane] = out_sim[q];
+            nn_idx[(size_t)tok * k + lane] = acc[q] ? (int)~(unsigned)acc[q] : -1;
+            nn_sim[(size_t)tok * k + lane] = acc[q] ? key_sim(acc[q]) : -2.f;
         }
     }
 }
@@ -289,16 +355,8 @@ cudaError_t knn_launch(const Problem &p, int k, const void *qk, const int32_t *b
                       : launch_round<float, 128>(p, k, qk, buckets, perm, inv_norm, cand_idx, cand_sim, st);
     if (e != cudaSuccess) return e;
     const long n = p.n_tok();
-    const unsigned g4 = (unsigned)((n + 31) / 32), g2 = (unsigned)((n + 15) / 16);
-    const int ne = (p.n_rounds * k + 31) / 32;
-    if (ne <= 1)
-        knn_merge_kernel<1, 4><<<g4, 256, 0, st>>>(cand_idx, cand_sim, n, p.L, p.n_rounds, k, nn_idx, nn_sim);
-    else if (ne <= 2)
-        knn_merge_kernel<2, 4><<<g4, 256, 0, st>>>(cand_idx, cand_sim, n, p.L, p.n_rounds, k, nn_idx, nn_sim);
-    else if (ne <= 4)
-        knn_merge_kernel<4, 4><<<g4, 256, 0, st>>>(cand_idx, cand_sim, n, p.L, p.n_rounds, k, nn_idx, nn_sim);
-    else
-        knn_merge_kernel<8, 2><<<g2, 256, 0, st>>>(cand_idx, cand_sim, n, p.L, p.n_rounds, k, nn_idx, nn_sim);
+    const unsigned g4 = (unsigned)((n + 31) / 32);          // 8 warps x 4 tokens per CTA
+    knn_merge_kernel<4><<<g4, 256, 0, st>>>(cand_idx, cand_sim, n, p.L, p.n_rounds, k, nn_idx, nn_sim);
     return cudaGetLastError();
 }
 
