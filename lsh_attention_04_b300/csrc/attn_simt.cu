@@ -14,6 +14,8 @@
 // Scores use scale * (q . k) * |k|^-1; softmax and the value sum run in fp32.
 #include <math.h>
 
+#include <type_traits>
+
 #include "internal.cuh"
 
 namespace lsh {
@@ -23,6 +25,18 @@ constexpr int kWarps = 16;
 
 // T: input element type; TO: per-round row type (fp32 for fp32 inputs, bf16 for both
 // 16-bit input types)
+// Shared-memory element of the staged window rows: fp32, except 16-bit inputs at chunk
+// 128 and d = 128, whose rows stay 16-bit so the 256-row window fits.
+template <typename T, int D, int C>
+using Stage = typename std::conditional<(C == 128 && D == 128 && sizeof(T) == 2), T, float>::type;
+__device__ __forceinline__ float tof(float x) { return x; }
+__device__ __forceinline__ float tof(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float tof(__half x) { return __half2float(x); }
+template <typename E> __device__ __forceinline__ E fromf(float x);
+template <> __device__ __forceinline__ float fromf<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 fromf<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+template <> __device__ __forceinline__ __half fromf<__half>(float x) { return __float2half_rn(x); }
+
 template <typename T, typename TO, int D, int C>
 __global__ void __launch_bounds__(kWarps * 32)
 attn_simt_kernel(const T *__restrict__ qk, const T *__restrict__ v,
@@ -31,12 +45,14 @@ attn_simt_kernel(const T *__restrict__ qk, const T *__restrict__ v,
                  int n_rounds, int nb, int causal, float scale, int token_order,
                  TO *__restrict__ o_r, float *__restrict__ lse_r)
 {
-    constexpr int KS = D + 1;  // padded key row: lanes reading different rows hit different banks
+    using E = Stage<T, D, C>;
+    constexpr int KS = D + (sizeof(E) == 4 ? 1 : 2);  // padded key row: lanes reading
+                                                      // different rows hit different banks
     extern __shared__ float smem[];
-    float *Ks = smem;                      // [2C][D+1]
-    float *Vs = Ks + 2 * C * KS;           // [2C][D]
-    float *kin = Vs + 2 * C * D;           // [2C]  |k|^-1
+    float *kin = smem;                     // [2C]  |k|^-1
     int *kb = (int *)(kin + 2 * C);        // [2C]  bucket
+    E *Ks = reinterpret_cast<E *>(kb + 2 * C);   // [2C][KS]
+    E *Vs = Ks + 2 * C * KS;               // [2C][D]
 
     const int chunk_id = blockIdx.x;
     const long seg = blockIdx.y;
@@ -51,8 +67,8 @@ attn_simt_kernel(const T *__restrict__ qk, const T *__restrict__ v,
     for (int idx = threadIdx.x; idx < nwin * D; idx += blockDim.x) {
         const int t = idx / D, e = idx % D;
         const int j = P[lo + t];
-        Ks[t * KS + e] = ld_f32(qkh, (size_t)j * D + e);
-        Vs[t * D + e] = ld_f32(vh, (size_t)j * D + e);
+        Ks[t * KS + e] = fromf<E>(ld_f32(qkh, (size_t)j * D + e));
+        Vs[t * D + e] = fromf<E>(ld_f32(vh, (size_t)j * D + e));
     }
     for (int t = threadIdx.x; t < nwin; t += blockDim.x) {
         const int j = P[lo + t];
@@ -81,7 +97,7 @@ attn_simt_kernel(const T *__restrict__ qk, const T *__restrict__ v,
             if (t < nwin && sidx >= klo && sidx < khi && sidx != s) {
                 float dot = 0.f;
 #pragma unroll 8
-                for (int e = 0; e < D; ++e) dot = fmaf(Ks[ts * KS + e], Ks[t * KS + e], dot);
+                for (int e = 0; e < D; ++e) dot = fmaf(tof(Ks[ts * KS + e]), tof(Ks[t * KS + e]), dot);
                 val = scale * dot * kin[t];
             }
             sc[m] = val;
@@ -92,7 +108,7 @@ attn_simt_kernel(const T *__restrict__ qk, const T *__restrict__ v,
         float lse;
         if (mx == -INFINITY) {
 #pragma unroll
-            for (int i = 0; i < EPL; ++i) o[i] = Vs[ts * D + lane + 32 * i];
+            for (int i = 0; i < EPL; ++i) o[i] = tof(Vs[ts * D + lane + 32 * i]);
             lse = kSelfLogit;
         } else {
             float sum = 0.f;
@@ -111,7 +127,7 @@ attn_simt_kernel(const T *__restrict__ qk, const T *__restrict__ v,
                     const int t = 32 * m + src;
                     if (pw != 0.f) {
 #pragma unroll
-                        for (int i = 0; i < EPL; ++i) o[i] = fmaf(pw, Vs[t * D + lane + 32 * i], o[i]);
+                        for (int i = 0; i < EPL; ++i) o[i] = fmaf(pw, tof(Vs[t * D + lane + 32 * i]), o[i]);
                     }
                 }
             }
@@ -132,7 +148,9 @@ cudaError_t launch(const Problem &p, const void *qk, const void *v, const int32_
                    const int32_t *perm, const int32_t *bstart, const float *inv_norm, void *o_r,
                    float *lse_r, cudaStream_t st)
 {
-    const size_t smem = sizeof(float) * (2 * C * (D + 1) + 2 * C * D + 2 * C) + sizeof(int) * 2 * C;
+    using E = Stage<T, D, C>;
+    constexpr int KS = D + (sizeof(E) == 4 ? 1 : 2);
+    const size_t smem = sizeof(E) * (2 * C * KS + 2 * C * D) + (sizeof(float) + sizeof(int)) * 2 * C;
     auto k = attn_simt_kernel<T, TO, D, C>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -150,7 +168,13 @@ cudaError_t dispatch(const Problem &p, const void *qk, const void *v, const int3
 {
     if (p.d == 64)
         return p.chunk == 32 ? launch<T, TO, 64, 32>(p, qk, v, buckets, perm, bstart, inv_norm, o_r, lse_r, st)
-                             : launch<T, TO, 64, 64>(p, qk, v, buckets, perm, bstart, inv_norm, o_r, lse_r, st);
+             : p.chunk == 64 ? launch<T, TO, 64, 64>(p, qk, v, buckets, perm, bstart, inv_norm, o_r, lse_r, st)
+                             : launch<T, TO, 64, 128>(p, qk, v, buckets, perm, bstart, inv_norm, o_r, lse_r, st);
+    if (p.chunk == 128) {
+        if constexpr (sizeof(T) == 2)
+            return launch<T, TO, 128, 128>(p, qk, v, buckets, perm, bstart, inv_norm, o_r, lse_r, st);
+        return cudaErrorInvalidValue;      // fp32 at d = 128: the window does not fit
+    }
     return p.chunk == 32 ? launch<T, TO, 128, 32>(p, qk, v, buckets, perm, bstart, inv_norm, o_r, lse_r, st)
                          : launch<T, TO, 128, 64>(p, qk, v, buckets, perm, bstart, inv_norm, o_r, lse_r, st);
 }

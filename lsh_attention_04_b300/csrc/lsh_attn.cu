@@ -21,7 +21,9 @@ lsh_status_t validate(const Problem &p, bool check_chunk = true)
     if (check_chunk && p.L % p.chunk != 0) return LSH_ERR_INVALID_ARGUMENT;  // equal chunks
     if (p.causal != 0 && p.causal != 1) return LSH_ERR_INVALID_ARGUMENT;
     if (p.d != 64 && p.d != 128) return LSH_ERR_UNSUPPORTED;
-    if (check_chunk && p.chunk != 32 && p.chunk != 64) return LSH_ERR_UNSUPPORTED;
+    if (check_chunk && p.chunk != 32 && p.chunk != 64 && p.chunk != 128) return LSH_ERR_UNSUPPORTED;
+    // chunk 128: the forward pass only, on the CUDA cores; fp32 rows at d = 128 do not fit
+    if (check_chunk && p.chunk == 128 && p.d == 128 && p.dtype == LSH_F32) return LSH_ERR_UNSUPPORTED;
     if (p.nb > 2048) return LSH_ERR_UNSUPPORTED;
     if (is16(p.dtype) && p.nb % 16 != 0) return LSH_ERR_UNSUPPORTED;
     if ((long long)p.B * p.H * p.n_rounds * p.L >= (1LL << 31)) return LSH_ERR_UNSUPPORTED;
@@ -205,6 +207,7 @@ lsh_status_t backward(const void *qk, const void *v, const void *R, lsh_dtype_t 
     const Problem p = make_problem(B, H, L, d, n_buckets, n_rounds, chunk, causal, scale, dtype);
     lsh_status_t s = validate(p);
     if (s != LSH_OK) return s;
+    if (chunk == 128) return LSH_ERR_UNSUPPORTED;            // forward only
     if (!qk || !v || !R || !out || !lse || !g_out || !dqk || !dv || !workspace)
         return LSH_ERR_INVALID_ARGUMENT;
     if (((uintptr_t)workspace) % 256 != 0) return LSH_ERR_INVALID_ARGUMENT;
@@ -274,7 +277,7 @@ size_t lsh_attn_backward_workspace_bytes(int B, int H, int L, int d, int n_bucke
                                          int n_rounds, int chunk, lsh_dtype_t dtype)
 {
     const Problem p = make_problem(B, H, L, d, n_buckets, n_rounds, chunk, 0, 1.f, dtype);
-    if (validate(p) != LSH_OK) return 0;
+    if (validate(p) != LSH_OK || chunk == 128) return 0;
     return backward_bytes(p);
 }
 
@@ -433,7 +436,7 @@ size_t lsh_knn_workspace_bytes(int B, int H, int L, int d, int n_buckets, int n_
                                int k, lsh_dtype_t dtype)
 {
     const Problem p = make_problem(B, H, L, d, n_buckets, n_rounds, chunk, 0, 1.f, dtype);
-    if (validate(p) != LSH_OK || !knn_k_ok(n_rounds, k) || dtype == LSH_F16) return 0;
+    if (validate(p) != LSH_OK || !knn_k_ok(n_rounds, k) || dtype == LSH_F16 || chunk == 128) return 0;
     return knn_layout(p, k).total;
 }
 
@@ -444,7 +447,7 @@ lsh_status_t lsh_knn(const void *qk, const void *R, lsh_dtype_t dtype, int B, in
     const Problem p = make_problem(B, H, L, d, n_buckets, n_rounds, chunk, 0, 1.f, dtype);
     lsh_status_t s = validate(p);
     if (s != LSH_OK) return s;
-    if (dtype == LSH_F16) return LSH_ERR_UNSUPPORTED;        // bf16 or fp32 candidates only
+    if (dtype == LSH_F16 || chunk == 128) return LSH_ERR_UNSUPPORTED;   // bf16 / fp32, window <= 128
     if (!knn_k_ok(n_rounds, k)) return LSH_ERR_INVALID_ARGUMENT;
     if (!qk || !R || !nn_idx || !nn_sim || !workspace) return LSH_ERR_INVALID_ARGUMENT;
     if (((uintptr_t)workspace) % 256 != 0) return LSH_ERR_INVALID_ARGUMENT;

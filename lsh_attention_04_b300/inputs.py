@@ -82,6 +82,9 @@ WORKLOADS["long_f16_B1_H8_L65536_d128_R8"] = WORKLOADS["long_B1_H8_L65536_d128_R
 WORKLOADS["long_chunk32_B1_H8_L65536_d128_R8"] = WORKLOADS["long_B1_H8_L65536_d128_R8"].replace(
     name="long_chunk32_B1_H8_L65536_d128_R8", chunk=32)
 
+WORKLOADS["long_chunk128_B1_H8_L65536_d128_R8"] = WORKLOADS["long_B1_H8_L65536_d128_R8"].replace(
+    name="long_chunk128_B1_H8_L65536_d128_R8", chunk=128)
+
 #: The headline workload: L = 64K, 8 rounds.
 HEADLINE = "long_B1_H8_L65536_d128_R8"
 

@@ -124,7 +124,9 @@ def _fwd(lib, **kw):
     (dict(causal=2), lsh.LSH_ERR_INVALID_ARGUMENT),
     (dict(dtype=7), lsh.LSH_ERR_INVALID_ARGUMENT),
     (dict(d=96), lsh.LSH_ERR_UNSUPPORTED),
-    (dict(chunk=128, L=1024), lsh.LSH_ERR_UNSUPPORTED),
+    (dict(chunk=256, L=1024), lsh.LSH_ERR_UNSUPPORTED),
+    (dict(chunk=128, d=128, dtype=lsh.LSH_F32), lsh.LSH_ERR_UNSUPPORTED),
+    (dict(chunk=128, wsb=1024), lsh.LSH_ERR_WORKSPACE_TOO_SMALL),   # chunk 128 passes validation
     (dict(nb=4096), lsh.LSH_ERR_UNSUPPORTED),
     (dict(nb=40), lsh.LSH_ERR_UNSUPPORTED),              # bf16 needs n_buckets % 16 == 0
     (dict(B=1 << 12, H=1 << 12, L=1 << 10, R_=1 << 2), lsh.LSH_ERR_UNSUPPORTED),
@@ -206,6 +208,7 @@ def _bwd(lib, **kw):
     (dict(g_out=0x604), lsh.LSH_ERR_INVALID_ARGUMENT),   # bf16: 16-byte aligned gradients
     (dict(dv=0x804), lsh.LSH_ERR_INVALID_ARGUMENT),
     (dict(g_out=0x604, dtype=lsh.LSH_F32, wsb=1024), lsh.LSH_ERR_WORKSPACE_TOO_SMALL),
+    (dict(chunk=128), lsh.LSH_ERR_UNSUPPORTED),
 ])
 @no_device
 def test_backward_validation(lib, kw, expect):
@@ -244,6 +247,7 @@ def test_knn_workspace_sizing(lib):
     (dict(d=96), lsh.LSH_ERR_UNSUPPORTED),
     (dict(dtype=lsh.LSH_F16), lsh.LSH_ERR_UNSUPPORTED),
     (dict(dtype=3), lsh.LSH_ERR_INVALID_ARGUMENT),
+    (dict(chunk=128), lsh.LSH_ERR_UNSUPPORTED),
     (dict(wsb=256), lsh.LSH_ERR_WORKSPACE_TOO_SMALL),
 ])
 def test_knn_argument_checks(lib, kw, expect):
@@ -340,3 +344,14 @@ def test_f16_workspace_matches_bf16(lib):
         lib.lsh_attn_workspace_bytes(*args, lsh.LSH_BF16)
     assert lib.lsh_attn_workspace_bytes(1, 1, 1024, 64, 40, 1, 64, lsh.LSH_F16) == 0   # nb % 16
     assert lib.lsh_attn_workspace_bytes(1, 1, 1024, 64, 32, 1, 64, 3) == 0
+
+
+def test_chunk128_scope(lib):
+    """Chunk 128: the forward pass only, and not fp32 rows at d = 128."""
+    f = lib.lsh_attn_workspace_bytes
+    assert f(1, 1, 1024, 64, 16, 2, 128, lsh.LSH_F32) > 0
+    assert f(1, 1, 1024, 128, 16, 2, 128, lsh.LSH_BF16) > 0
+    assert f(1, 1, 1024, 128, 16, 2, 128, lsh.LSH_F32) == 0
+    assert f(1, 1, 1024, 64, 16, 2, 256, lsh.LSH_BF16) == 0
+    assert lib.lsh_attn_backward_workspace_bytes(1, 1, 1024, 64, 16, 2, 128, lsh.LSH_BF16) == 0
+    assert lib.lsh_knn_workspace_bytes(1, 1, 1024, 64, 16, 2, 128, 8, lsh.LSH_BF16) == 0

@@ -37,6 +37,11 @@ SMALL = [
     # (L = 1056 is not a multiple of 64)
     W("bf16_chunk32_L2048_d128_noncausal", 1, 2, 2048, 128, "bf16", 64, 3, 32, False, 32, 23),
     W("bf16_chunk32_L1056_d64_simt", 1, 1, 1056, 64, "bf16", 32, 2, 32, True, 16, 24),
+    # chunk 128 (CUDA cores; 16-bit staged rows at d = 128)
+    W("bf16_chunk128_L1024_d64", 1, 2, 1024, 64, "bf16", 16, 2, 128, True, 8, 25),
+    W("bf16_chunk128_L1024_d128_noncausal", 1, 1, 1024, 128, "bf16", 16, 2, 128, False, 8, 26),
+    W("f32_chunk128_L512_d64", 1, 1, 512, 64, "f32", 8, 2, 128, True, 0, 27),
+    W("f16_chunk128_L768_d128", 1, 1, 768, 128, "f16", 16, 3, 128, True, 8, 28),
     # fp16 inputs: the tensor-core hash and attention with fp16 operands (chunk 64), the
     # SIMT attention (chunk 32) and the SIMT hash (an R group too large at nb = 2048)
     W("f16_B2_H2_L1344_d64_R4", 2, 2, 1344, 64, "f16", 64, 4, 64, True, 16, 19),
