@@ -166,7 +166,9 @@ size_t lsh_attn_backward_workspace_bytes(int B, int H, int L, int d, int n_bucke
  * in {32, 64}) runs its five contractions on the tensor cores with bf16 operands and
  * fp32 accumulation: g_out, the weights exp(s_ij - lse_i) and the score gradients are
  * rounded to bf16 for the products (scores, their softmax and g_out . out stay fp32);
- * out, g_out, dqk and dv must then be 16-byte aligned (else LSH_ERR_INVALID_ARGUMENT).
+ * qk, v, out, g_out, dqk and dv must then be 16-byte aligned (else
+ * LSH_ERR_INVALID_ARGUMENT).  At d = 128 and chunk 64 the contractions run on tcgen05
+ * (shared-memory operands, TMEM accumulators); the other shapes on warp-level MMA.
  */
 lsh_status_t lsh_attn_backward(const void *qk, const void *v, const void *R, lsh_dtype_t dtype,
                                int B, int H, int L, int d, int n_buckets, int n_rounds,

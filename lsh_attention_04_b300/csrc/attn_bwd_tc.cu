@@ -33,9 +33,7 @@ namespace lsh {
 namespace {
 
 using namespace nvcuda;
-using sm100::cp_async16;
-using sm100::cp_async_wait_all;
-using sm100::smem_u32;
+using namespace sm100;
 
 // g16 = bf16(g_out); dsum = g_out . out, one warp per token, 4 columns per lane.
 __global__ void __launch_bounds__(256)
@@ -89,6 +87,12 @@ struct TcBwd {
     // meta: tok[NW] bkt[NW] kin[NW] used[NW] lse[C] has[C] qmeta[C][2] qf[C][2]
     static constexpr size_t kBytes = kMeta + (size_t)4 * (4 * NW + 6 * C);
 };
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
 
 __device__ __forceinline__ void atomic_add4(float *dst, float4 v)
 {
@@ -363,6 +367,389 @@ cudaError_t launch_tc(const Problem &p, const void *qk, const void *v, const int
     return cudaGetLastError();
 }
 
+
+// ---------------------------------------------------------------------------------------
+// d = 128, chunk 64: the five contractions on the tcgen05 tensor cores.
+//
+// One CTA per (head, round, 128-row tile): query rows = chunks 2t and 2t+1 of the sorted
+// segment, window = chunks 2t-1 .. 2t+1 (192 rows; the first 64 absent for t = 0).  The
+// operands live in shared memory as planes of 64 columns, each plane rows x 128 bytes
+// with the 128-byte swizzle; one such tile serves as a K-major operand (rows = M or N,
+// columns = K) and as an MN-major one (rows = K, columns = M or N) through its
+// descriptor.  TMEM (512 columns):
+//     phase 1   S = Q K^T   [0, 192)    dP = G V^T  [192, 384)        (M 128, N 192)
+//     pass A    E1 = ds scale / |k|,  E2 = ds scale  (bf16 tiles; E2 over the V rows)
+//               dQ = E1 K   [384, 512)                                 (M 128, N 128)
+//     pass B    P = pi (bf16, over E1)
+//     phase 2   dV^T = G^T P   [0, 192)     dK^T = Q^T E2   [192, 384) (M = d, N 192)
+// Warps w and w + 4 share TMEM lane quarter w (a query row, or in phase 2 a column d)
+// and split the columns; warp 4 also issues the MMAs and owns TMEM; all eight gather.
+// A row's keys are one interval of the window (its bucket run, clipped to its window, and
+// before it when causal), from run bounds computed once per tile.  One mbarrier takes the first two commits
+// (phase 1, then dQ: waited with parities 0 and 1 by warps that saw the one before), a
+// second the last (phase 2: every MMA of the CTA), so no wait can alias a phase.
+constexpr int kT5Rows = 128, kT5Win = 192, kT5D = 128;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kT5Threads = 256;
+constexpr int kPlK = kT5Win * 128;                   // window-tile plane (192 rows)
+constexpr int kPlQ = kT5Rows * 128;                  // query-tile plane (128 rows)
+constexpr size_t kT5OffK = 0;                        // qk window rows, 2 planes
+constexpr size_t kT5OffV = kT5OffK + 2 * kPlK;       // v window rows, 2 planes; then E2
+constexpr size_t kT5OffG = kT5OffV + 2 * kPlK;       // g_out query rows, 2 planes
+constexpr size_t kT5OffP = kT5OffG + 2 * kPlQ;       // E1, then P: 3 planes of 64 keys
+constexpr size_t kT5OffMeta = kT5OffP + 3 * kPlQ;
+static_assert(2 * kPlK == 3 * kPlQ, "E2 (3 key planes) fits the v rows (2 d planes)");
+struct T5Meta {
+    int tok[kT5Win], bkt[kT5Win];
+    float kin[kT5Win], kcs[kT5Win];                  // 1/|k|, scale log2(e) / |k|
+    int rs[kT5Win], re[kT5Win];                      // bucket run of each window row: [rs, re)
+    float lq[kT5Rows], base[kT5Rows];                // lse log2(e), D - g_lse of each query row
+    int has[kT5Rows];
+    unsigned used[kT5Win / 32];
+    float red[2][4][32], proj[2][32];
+};
+constexpr size_t kT5Smem = 1024 + kT5OffMeta + sizeof(T5Meta);
+
+// byte offset of element (row, col) of a tile of `plane` bytes per 64-column plane
+__device__ __forceinline__ uint32_t sw_off(int row, int col, int plane)
+{
+    return (uint32_t)((col >> 6) * plane + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4) + (col & 7) * 2);
+}
+
+// 32 consecutive columns [c0, c0 + 32) of row `row` of a 16-bit tile, from fp32 values
+__device__ __forceinline__ void put_row32(uint8_t *tile, int plane, int row, int c0, const float (&x)[32])
+{
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        uint4 u;
+        u.x = pack_bf16x2(x[8 * g], x[8 * g + 1]);
+        u.y = pack_bf16x2(x[8 * g + 2], x[8 * g + 3]);
+        u.z = pack_bf16x2(x[8 * g + 4], x[8 * g + 5]);
+        u.w = pack_bf16x2(x[8 * g + 6], x[8 * g + 7]);
+        *reinterpret_cast<uint4 *>(tile + sw_off(row, c0 + 8 * g, plane)) = u;
+    }
+}
+
+__global__ void __launch_bounds__(kT5Threads, 1)
+attn_bwd_tc5_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *__restrict__ v,
+                    const int32_t *__restrict__ buckets, const int32_t *__restrict__ perm,
+                    const float *__restrict__ inv_norm, const float *__restrict__ lse,
+                    const float *__restrict__ g_out, const __nv_bfloat16 *__restrict__ g16,
+                    const float *__restrict__ dsum, const float *__restrict__ g_lse, int L,
+                    int n_rounds, int causal, float scale, float *__restrict__ dqk,
+                    float *__restrict__ dv, StatusBlock *status)
+{
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint64_t bar_mma, bar_done;            // phases 1 and pass A's MMA; phase 2
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag_s;
+    uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t *Kt = sm + kT5OffK, *Vt = sm + kT5OffV, *Gt = sm + kT5OffG, *Pt = sm + kT5OffP;
+    T5Meta &mt = *reinterpret_cast<T5Meta *>(sm + kT5OffMeta);
+    volatile int *abort_flag = &abort_flag_s;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tps = (L + kT5Rows - 1) / kT5Rows;
+    const long seg = (long)blockIdx.x / tps;
+    const int t = (int)((long)blockIdx.x - seg * tps);
+    const long bh = seg / n_rounds;
+    const size_t head = (size_t)bh * L;
+    const int32_t *Pm = perm + seg * L;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bar_mma, 1);
+        mbar_init(&bar_done, 1);
+        abort_flag_s = 0;
+        mbar_fence_init();
+    }
+    if (warp == 4) tmem_alloc(&tmem_slot, 512);
+
+    // ---- 1. gather: window rows w (sorted 128 t - 64 + w) and query rows q (128 t + q)
+    for (int x = threadIdx.x; x < kT5Win * 16; x += kT5Threads) {
+        const int w = x >> 4, pc = x & 15;
+        const int s = kT5Rows * t - 64 + w;
+        const uint32_t o = sw_off(w, 8 * pc, kPlK);
+        if (s >= 0 && s < L) {
+            int j = Pm[s];
+            j = (unsigned)j < (unsigned)L ? j : 0;
+            cp_async16(smem_u32(Kt + o), qk + (head + j) * kT5D + 8 * pc);
+            cp_async16(smem_u32(Vt + o), v + (head + j) * kT5D + 8 * pc);
+        } else {
+            *reinterpret_cast<uint4 *>(Kt + o) = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4 *>(Vt + o) = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    for (int x = threadIdx.x; x < kT5Rows * 16; x += kT5Threads) {
+        const int q = x >> 4, pc = x & 15;
+        const int s = kT5Rows * t + q;
+        const uint32_t o = sw_off(q, 8 * pc, kPlQ);
+        if (s < L) {
+            int i = Pm[s];
+            i = (unsigned)i < (unsigned)L ? i : 0;
+            cp_async16(smem_u32(Gt + o), g16 + (head + i) * kT5D + 8 * pc);
+        } else {
+            *reinterpret_cast<uint4 *>(Gt + o) = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    for (int w = threadIdx.x; w < kT5Win; w += kT5Threads) {
+        const int s = kT5Rows * t - 64 + w;
+        const bool present = s >= 0 && s < L;
+        int j = present ? Pm[s] : 0;
+        j = (unsigned)j < (unsigned)L ? j : 0;
+        mt.tok[w] = present ? j : INT_MAX;
+        mt.bkt[w] = present ? buckets[seg * L + j] : -1;
+        mt.kin[w] = present ? inv_norm[head + j] : 0.f;
+        mt.kcs[w] = present ? scale * kLog2e * inv_norm[head + j] : 0.f;
+        if (w >= 64) {
+            const int q = w - 64;
+            mt.lq[q] = present ? lse[head + j] * kLog2e : 0.f;
+            mt.base[q] = present ? dsum[head + j] - (g_lse ? g_lse[head + j] : 0.f) : 0.f;
+            mt.has[q] = 0;
+        }
+        if (w < kT5Win / 32) mt.used[w] = 0u;
+    }
+    __syncthreads();
+    // bucket runs of the window (sorted order keeps a bucket's rows together): warp 0 scans
+    // the start flags forward and the end flags backward, 32 rows at a time
+    if (warp == 0) {
+        int carry = 0;
+        for (int b0 = 0; b0 < kT5Win; b0 += 32) {
+            const int w = b0 + lane;
+            int x = (w == 0 || mt.bkt[w] != mt.bkt[w - 1]) ? w : 0;   // a run starts here
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) x = max(x, __shfl_up_sync(0xffffffffu, x, o));
+            x = max(x, carry);
+            mt.rs[w] = x;
+            carry = __shfl_sync(0xffffffffu, x, 31);
+        }
+        carry = kT5Win;
+        for (int b0 = kT5Win - 32; b0 >= 0; b0 -= 32) {
+            const int w = b0 + lane;
+            int x = (w == kT5Win - 1 || mt.bkt[w] != mt.bkt[w + 1]) ? w + 1 : kT5Win;   // ends here
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) x = min(x, __shfl_down_sync(0xffffffffu, x, o));
+            x = min(x, carry);
+            mt.re[w] = x;
+            carry = __shfl_sync(0xffffffffu, x, 0);
+        }
+    }
+    cp_async_wait_all();
+    fence_proxy_async();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = tmem_slot;
+    const uint32_t kb = smem_u32(Kt), vb = smem_u32(Vt), gb = smem_u32(Gt), pb = smem_u32(Pt);
+
+    // ---- 2. phase 1: S = Q K^T, dP = G V^T
+    if (warp == 4) {
+        const uint32_t idesc = idesc_bf16(kT5Rows, kT5Win, 0, 0);
+        for (int ks = 0; ks < kT5D / 16; ++ks) {
+            const int pl = ks >> 2, ko = (ks & 3) * 32;
+            mma_ss(tmem, smem_desc(kb + pl * kPlK + 64 * 128 + ko, 16, 1024),
+                   smem_desc(kb + pl * kPlK + ko, 16, 1024), idesc, ks > 0);
+            mma_ss(tmem + kT5Win, smem_desc(gb + pl * kPlQ + ko, 16, 1024),
+                   smem_desc(vb + pl * kPlK + ko, 16, 1024), idesc, ks > 0);
+        }
+        mma_commit(smem_u32(&bar_mma));
+    }
+
+    // rows: warps w and w + 4 share TMEM lane quarter w (query q = its lane) and split the
+    // column batches (keys [0, 96) and [96, 192); d [0, 64) and [64, 128) for dQ)
+    const int quarter = warp & 3, half = warp >> 2;
+    const int q = 32 * quarter + lane, qi = 64 + q;
+    const bool qlive = kT5Rows * t + q < L;
+    const uint32_t tl = tmem + ((uint32_t)(32 * quarter) << 16);
+    // the row's keys: its bucket run inside its window ([0, 128) for chunk 2t, [64, 192) for
+    // 2t+1), before it when causal (sorted order is position order inside a bucket), itself
+    // excluded
+    const int wlo = q < 64 ? 0 : 64;
+    const int klo = qlive ? max(wlo, mt.rs[qi]) : 0;
+    const int khi = qlive ? (causal ? qi : min(wlo + 128, mt.re[qi])) : 0;
+    const float lq2 = qlive ? mt.lq[q] : 0.f, bs = qlive ? mt.base[q] : 0.f;
+    bool ok = true;
+
+    // the row's weights pi (and score gradients ds) of keys [32 c, 32 c + 32)
+    auto row_batch = [&](int c, bool with_ds, float (&pi)[32], float (&ds)[32]) -> unsigned {
+        uint32_t sv[32], pv[32];
+        tmem_ld32(tl + 32 * c, sv);
+        if (with_ds) {
+            tmem_ld32(tl + kT5Win + 32 * c, pv);
+            tmem_wait_ld(sv, pv);
+        } else {
+            tmem_wait_ld(sv);
+        }
+        unsigned vm = 0u;
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+            const int w = 32 * c + jj;
+            const bool valid = w >= klo && w < khi && w != qi;
+            pi[jj] = valid ? exp2f(__uint_as_float(sv[jj]) * mt.kcs[w] - lq2) : 0.f;
+            if (with_ds) ds[jj] = pi[jj] * (__uint_as_float(pv[jj]) - bs);
+            vm |= valid ? 1u << jj : 0u;
+        }
+        return vm;
+    };
+
+    // ---- 3. pass A: E1 = ds scale / |k| (over P), E2 = ds scale (over the v rows)
+    {
+        ok = wait(&bar_mma, 0, abort_flag, status, 0x901);
+        fence_after_sync();
+        bool any = false;
+        for (int c = 3 * half; c < 3 * half + 3; ++c) {
+            float pi[32], ds[32], e1[32], e2[32];
+            const unsigned vm = row_batch(c, true, pi, ds);
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+                e2[jj] = ds[jj] * scale;
+                e1[jj] = e2[jj] * mt.kin[32 * c + jj];
+            }
+            put_row32(Pt, kPlQ, q, 32 * c, e1);
+            put_row32(Vt, kPlQ, q, 32 * c, e2);
+            any |= vm != 0u;
+            const unsigned col = __reduce_or_sync(0xffffffffu, vm);
+            if (lane == 0 && col) atomicOr(&mt.used[c], col);
+        }
+        if (any) atomicOr(&mt.has[q], 1);
+        fence_proxy_async();
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+
+    // ---- 4. dQ = E1 K (K-major E1 rows, the qk window rows as an MN-major operand)
+    if (warp == 4) {
+        const uint32_t idesc = idesc_bf16(kT5Rows, kT5D, 0, 1);
+        for (int ks = 0; ks < kT5Win / 16; ++ks) {
+            const int pl = ks >> 2, ko = (ks & 3) * 32;
+            mma_ss(tmem + 2 * kT5Win, smem_desc(pb + pl * kPlQ + ko, 16, 1024),
+                   smem_desc(kb + 16 * ks * 128, kPlK, 1024), idesc, ks > 0);
+        }
+        mma_commit(smem_u32(&bar_mma));
+    }
+
+    // ---- 5. pass B: P = pi over E1 once dQ has read it
+    {
+        ok = wait(&bar_mma, 1, abort_flag, status, 0x902) && ok;
+        fence_after_sync();
+        for (int c = 3 * half; c < 3 * half + 3; ++c) {
+            float pi[32], ds[32];
+            row_batch(c, false, pi, ds);
+            put_row32(Pt, kPlQ, q, 32 * c, pi);
+        }
+        fence_proxy_async();
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+
+    // ---- 6. phase 2: dV^T = G^T P, dK^T = Q^T E2 (both operands MN-major)
+    if (warp == 4) {
+        const uint32_t idesc = idesc_bf16(kT5D, kT5Win, 1, 1);
+        for (int ks = 0; ks < kT5Rows / 16; ++ks) {
+            mma_ss(tmem, smem_desc(gb + 16 * ks * 128, kPlQ, 1024),
+                   smem_desc(pb + 16 * ks * 128, kPlQ, 1024), idesc, ks > 0);
+            mma_ss(tmem + kT5Win, smem_desc(kb + (64 + 16 * ks) * 128, kPlK, 1024),
+                   smem_desc(vb + 16 * ks * 128, kPlQ, 1024), idesc, ks > 0);
+        }
+        mma_commit(smem_u32(&bar_done));
+    }
+
+    // ---- 7. epilogue (all eight warps; the two halves of a lane quarter split the columns)
+    {
+        ok = wait(&bar_done, 0, abort_flag, status, 0x903) && ok;
+        fence_after_sync();
+        // dQ: lane = query row, columns = d
+        const bool hq = qlive && mt.has[q];
+        const int tq = qlive ? mt.tok[qi] : 0;
+        for (int c = 2 * half; c < 2 * half + 2; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tl + 2 * kT5Win + 32 * c, r);
+            tmem_wait_ld(r);
+            if (hq && ok) {
+                float *dst = dqk + (head + tq) * kT5D + 32 * c;
+#pragma unroll
+                for (int g4 = 0; g4 < 8; ++g4)
+                    atomicAdd(reinterpret_cast<float4 *>(dst + 4 * g4),
+                              make_float4(__uint_as_float(r[4 * g4]), __uint_as_float(r[4 * g4 + 1]),
+                                          __uint_as_float(r[4 * g4 + 2]), __uint_as_float(r[4 * g4 + 3])));
+            }
+        }
+        // dV^T and dK^T: lane = column d of v and qk, columns = window keys
+        const int d = 32 * quarter + lane;
+        for (int c = 3 * half; c < 3 * half + 3; ++c) {
+            uint32_t r[32], gk[32];
+            tmem_ld32(tl + 32 * c, r);
+            tmem_ld32(tl + kT5Win + 32 * c, gk);
+            tmem_wait_ld(r, gk);
+            const unsigned used = mt.used[c];
+            if (ok) {
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj)
+                    if ((used >> jj) & 1u)
+                        atomicAdd(dv + (head + mt.tok[32 * c + jj]) * kT5D + d, __uint_as_float(r[jj]));
+            }
+            // key role: dqk_j += (g - khat (khat . g)) / |k_j|, the dot over d across the
+            // 128 lanes of the half: a transposing butterfly in the warp, then its 4 warps
+            float pr[32], kh[32];
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+                const int w = 32 * c + jj;
+                const float kf = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(Kt + sw_off(w, d, kPlK)));
+                kh[jj] = kf * mt.kin[w];
+                pr[jj] = kh[jj] * __uint_as_float(gk[jj]);
+            }
+#pragma unroll
+            for (int s2 = 16; s2 >= 1; s2 >>= 1) {
+                const bool up = (lane & s2) != 0;
+#pragma unroll
+                for (int i2 = 0; i2 < s2; ++i2) {
+                    const float lo = pr[i2], hi = pr[i2 + s2];
+                    const float send = up ? lo : hi;
+                    const float keep = up ? hi : lo;
+                    pr[i2] = keep + __shfl_xor_sync(0xffffffffu, send, s2);
+                }
+            }
+            mt.red[half][quarter][lane] = pr[0];      // the warp's sum for key 32 c + lane
+            named_bar_sync(1 + half, 128);
+            if (quarter == 0)
+                mt.proj[half][lane] = mt.red[half][0][lane] + mt.red[half][1][lane] +
+                                      mt.red[half][2][lane] + mt.red[half][3][lane];
+            named_bar_sync(1 + half, 128);
+            if (ok) {
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) {
+                    if (!((used >> jj) & 1u)) continue;
+                    const int w = 32 * c + jj;
+                    const float val = mt.kin[w] * (__uint_as_float(gk[jj]) - kh[jj] * mt.proj[half][jj]);
+                    atomicAdd(dqk + (head + mt.tok[w]) * kT5D + d, val);
+                }
+            }
+            named_bar_sync(1 + half, 128);            // red and proj are reused
+        }
+        // a token with no key in any round copies v_i: 1 / n_rounds of g_out from each round
+        if (half == 0 && ok && qlive && !mt.has[q] && mt.lq[q] < 0.5f * kSelfLogit * kLog2e) {
+            const float wself = 1.0f / (float)n_rounds;
+            for (int c = 0; c < kT5D; c += 4) {
+                const float4 g = *reinterpret_cast<const float4 *>(g_out + (head + tq) * kT5D + c);
+                atomicAdd(reinterpret_cast<float4 *>(dv + (head + tq) * kT5D + c),
+                          make_float4(wself * g.x, wself * g.y, wself * g.z, wself * g.w));
+            }
+        }
+    }
+
+    // ---- teardown: every MMA has completed (the last commit covers all of them)
+    if (warp == 4) {
+        int dummy = 0;
+        wait_w(&bar_done, 0, &dummy, status, 0x904);
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 4) {
+        fence_after_sync();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
 }  // namespace
 
 bool attn_bwd_tc_supported(const Problem &p)
@@ -378,7 +765,7 @@ size_t attn_bwd_tc_scratch_bytes(const Problem &p)
 cudaError_t attn_bwd_tc(const Problem &p, const void *qk, const void *v, const int32_t *buckets,
                         const int32_t *perm, const float *inv_norm, const float *out,
                         const float *lse, const float *g_out, const float *g_lse, float *dqk,
-                        float *dv, void *scratch, cudaStream_t st)
+                        float *dv, void *scratch, StatusBlock *status, cudaStream_t st)
 {
     __nv_bfloat16 *g16 = (__nv_bfloat16 *)scratch;
     float *dsum = (float *)((char *)scratch + (size_t)p.n_tok() * p.d * 2);
@@ -394,8 +781,16 @@ cudaError_t attn_bwd_tc(const Problem &p, const void *qk, const void *v, const i
         return launch_tc<64, 64>(p, qk, v, buckets, perm, inv_norm, lse, g_out, g16, dsum, g_lse, dqk, dv, st);
     if (p.d == 128 && p.chunk == 32)
         return launch_tc<128, 32>(p, qk, v, buckets, perm, inv_norm, lse, g_out, g16, dsum, g_lse, dqk, dv, st);
-    if (p.d == 128 && p.chunk == 64)
-        return launch_tc<128, 64>(p, qk, v, buckets, perm, inv_norm, lse, g_out, g16, dsum, g_lse, dqk, dv, st);
+    if (p.d == 128 && p.chunk == 64) {
+        e = cudaFuncSetAttribute(attn_bwd_tc5_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kT5Smem);
+        if (e != cudaSuccess) return e;
+        const long blocks = p.n_seg() * ((p.L + kT5Rows - 1) / kT5Rows);
+        attn_bwd_tc5_kernel<<<(unsigned)blocks, kT5Threads, kT5Smem, st>>>(
+            (const __nv_bfloat16 *)qk, (const __nv_bfloat16 *)v, buckets, perm, inv_norm, lse, g_out,
+            g16, dsum, g_lse, p.L, p.n_rounds, p.causal, p.scale, dqk, dv, status);
+        return cudaGetLastError();
+    }
     return cudaErrorInvalidValue;
 }
 

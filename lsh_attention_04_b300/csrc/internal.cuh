@@ -107,7 +107,7 @@ size_t attn_bwd_tc_scratch_bytes(const Problem &p);
 cudaError_t attn_bwd_tc(const Problem &p, const void *qk, const void *v, const int32_t *buckets,
                         const int32_t *perm, const float *inv_norm, const float *out,
                         const float *lse, const float *g_out, const float *g_lse, float *dqk,
-                        float *dv, void *scratch, cudaStream_t st);
+                        float *dv, void *scratch, StatusBlock *status, cudaStream_t st);
 
 cudaError_t selftest_wait_launch(StatusBlock *status, cudaStream_t st);
 

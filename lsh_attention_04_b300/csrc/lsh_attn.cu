@@ -215,7 +215,8 @@ lsh_status_t backward(const void *qk, const void *v, const void *R, lsh_dtype_t 
     const bool tc = attn_bwd_tc_supported(p);
     if (tc) {
         const auto a16 = [](const void *x) { return ((uintptr_t)x) % 16 == 0; };
-        if (!a16(out) || !a16(g_out) || !a16(dqk) || !a16(dv)) return LSH_ERR_INVALID_ARGUMENT;
+        if (!a16(qk) || !a16(v) || !a16(out) || !a16(g_out) || !a16(dqk) || !a16(dv))
+            return LSH_ERR_INVALID_ARGUMENT;
     }
     if (workspace_bytes < backward_bytes(p)) return LSH_ERR_WORKSPACE_TOO_SMALL;
     cudaStream_t st = (cudaStream_t)stream;
@@ -238,7 +239,7 @@ lsh_status_t backward(const void *qk, const void *v, const void *R, lsh_dtype_t 
     if ((s = record(events, 2, st)) != LSH_OK) return s;
     if (tc)
         s = cuda_status(attn_bwd_tc(p, qk, v, buckets, perm, inv_norm, out, lse, g_out, g_lse, dqk,
-                                    dv, at<void>(workspace, w.total), st));
+                                    dv, at<void>(workspace, w.total), (StatusBlock *)workspace, st));
     else
         s = cuda_status(attn_bwd(p, qk, v, buckets, perm, inv_norm, out, lse, g_out, g_lse, dqk,
                                  dv, st));
