@@ -44,6 +44,8 @@ CASES = [
     W("bwd_bf16_chunk32_L768_d128_R2", 1, 1, 768, 128, "bf16", 32, 2, 32, True, 8, 55),
     W("bwd_bf16_one_chunk_L64", 1, 1, 64, 64, "bf16", 16, 2, 64, True, 2, 56),
     W("bwd_f16_B1_H2_L1024_d128_R2", 1, 2, 1024, 128, "f16", 32, 2, 64, True, 16, 57),
+    # the tcgen05 kernel non-causal, with a last 128-row tile of one chunk (L = 1088)
+    W("bwd_bf16_B2_H1_L1088_d128_R2_noncausal", 2, 1, 1088, 128, "bf16", 32, 2, 64, False, 16, 59),
 ]
 ids = [w.name for w in CASES]
 
