@@ -682,9 +682,6 @@ def run_backward(args, w):
     peak_c = peaks["bf16_tflops"] if unit_c == "tensor" else FP32_ALU_TFLOPS
     kernels = {n: kernel_roof(w, n, stage_ms[n], wk[n], unit_c, peak_c, peaks, peak_src)
                for n in stage_names}
-    # the attention backward runs on the CUDA cores' fp32 lanes: its share of those too
-    kb = kernels["attn_bwd"]
-    kb["alu_frac"] = kb["algorithmic_flops"] / (kb["ms"] / 1e3) / 1e12 / FP32_ALU_TFLOPS
     dom = max(stage_ms, key=stage_ms.get)
     F = sum(k["flops"] for k in wk.values())
     Bts = sum(k["bytes"] for k in wk.values())
