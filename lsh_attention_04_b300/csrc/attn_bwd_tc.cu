@@ -371,8 +371,9 @@ cudaError_t launch_tc(const Problem &p, const void *qk, const void *v, const int
 // ---------------------------------------------------------------------------------------
 // d = 128, chunk 64: the five contractions on the tcgen05 tensor cores.
 //
-// One CTA per (head, round, 128-row tile): query rows = chunks 2t and 2t+1 of the sorted
-// segment, window = chunks 2t-1 .. 2t+1 (192 rows; the first 64 absent for t = 0).  The
+// One unit per (head, round, 128-row tile): query rows = chunks 2t and 2t+1 of the sorted
+// segment, window = chunks 2t-1 .. 2t+1 (192 rows; the first 64 absent for t = 0).
+// Persistent CTAs, one per SM, take the units in turn (TMEM and the barriers set up once).  The
 // operands live in shared memory as planes of 64 columns, each plane rows x 128 bytes
 // with the 128-byte swizzle; one such tile serves as a K-major operand (rows = M or N,
 // columns = K) and as an MN-major one (rows = K, columns = M or N) through its
@@ -380,8 +381,10 @@ cudaError_t launch_tc(const Problem &p, const void *qk, const void *v, const int
 //     phase 1   S = Q K^T   [0, 192)    dP = G V^T  [192, 384)        (M 128, N 192)
 //     pass A    E1 = ds scale / |k|,  E2 = ds scale  (bf16 tiles; E2 over the V rows)
 //               dQ = E1 K   [384, 512)                                 (M 128, N 128)
-//     pass B    P = pi (bf16, over E1)
+//     pass B    P = pi (bf16, over E1; kept in registers since pass A)
 //     phase 2   dV^T = G^T P   [0, 192)     dK^T = Q^T E2   [192, 384) (M = d, N 192)
+//     epilogue  dV^T, dK^T + dQ through the freed v / g_out / P tiles as fp32 rows, each
+//               added to dv or dqk by one warp
 // Warps w and w + 4 share TMEM lane quarter w (a query row, or in phase 2 a column d)
 // and split the columns; warp 4 also issues the MMAs and owns TMEM; all eight gather.
 // A row's keys are one interval of the window (its bucket run, clipped to its window, and
@@ -406,7 +409,6 @@ struct T5Meta {
     float lq[kT5Rows], base[kT5Rows];                // lse log2(e), D - g_lse of each query row
     int has[kT5Rows];
     unsigned used[kT5Win / 32];
-    float red[2][4][32], proj[2][32];
 };
 constexpr size_t kT5Smem = 1024 + kT5OffMeta + sizeof(T5Meta);
 
@@ -430,6 +432,15 @@ __device__ __forceinline__ void put_row32(uint8_t *tile, int plane, int row, int
     }
 }
 
+// the same 32 columns from bf16 pairs already packed (word k = columns c0 + 2k, c0 + 2k + 1)
+__device__ __forceinline__ void put_row32p(uint8_t *tile, int plane, int row, int c0, const uint32_t (&u)[16])
+{
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+        *reinterpret_cast<uint4 *>(tile + sw_off(row, c0 + 8 * g, plane)) =
+            make_uint4(u[4 * g], u[4 * g + 1], u[4 * g + 2], u[4 * g + 3]);
+}
+
 __global__ void __launch_bounds__(kT5Threads, 1)
 attn_bwd_tc5_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *__restrict__ v,
                     const int32_t *__restrict__ buckets, const int32_t *__restrict__ perm,
@@ -437,7 +448,7 @@ attn_bwd_tc5_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *_
                     const float *__restrict__ g_out, const __nv_bfloat16 *__restrict__ g16,
                     const float *__restrict__ dsum, const float *__restrict__ g_lse, int L,
                     int n_rounds, int causal, float scale, float *__restrict__ dqk,
-                    float *__restrict__ dv, StatusBlock *status)
+                    float *__restrict__ dv, long n_units, StatusBlock *status)
 {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t bar_mma, bar_done;            // phases 1 and pass A's MMA; phase 2
@@ -449,11 +460,6 @@ attn_bwd_tc5_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *_
     volatile int *abort_flag = &abort_flag_s;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tps = (L + kT5Rows - 1) / kT5Rows;
-    const long seg = (long)blockIdx.x / tps;
-    const int t = (int)((long)blockIdx.x - seg * tps);
-    const long bh = seg / n_rounds;
-    const size_t head = (size_t)bh * L;
-    const int32_t *Pm = perm + seg * L;
 
     if (threadIdx.x == 0) {
         mbar_init(&bar_mma, 1);
@@ -462,15 +468,40 @@ attn_bwd_tc5_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *_
         mbar_fence_init();
     }
     if (warp == 4) tmem_alloc(&tmem_slot, 512);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = tmem_slot;
+    const uint32_t kb = smem_u32(Kt), vb = smem_u32(Vt), gb = smem_u32(Gt), pb = smem_u32(Pt);
 
-    // ---- 1. gather: window rows w (sorted 128 t - 64 + w) and query rows q (128 t + q)
+    // persistent: units u = seg * tps + t, strided over the grid
+    int it = 0;
+    bool failed = false;
+    for (long u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
+    const long seg = u / tps;
+    const int t = (int)(u - seg * tps);
+    const long bh = seg / n_rounds;
+    const size_t head = (size_t)bh * L;
+    const int32_t *Pm = perm + seg * L;
+    LSH_SPAN_BEGIN(t_all);
+    LSH_SPAN_BEGIN(t_gather);
+
+    // ---- 1. gather: window rows w (sorted 128 t - 64 + w) and query rows q (128 t + q,
+    // the window's rows 64 + q).  The permutation entries come first (one load per row, all
+    // in flight at once); the row copies are then issued from shared memory with no load
+    // on their path, and the row metadata loads go out while the copies stream.
+    for (int w = threadIdx.x; w < kT5Win; w += kT5Threads) {
+        const int s = kT5Rows * t - 64 + w;
+        int j = (s >= 0 && s < L) ? Pm[s] : INT_MAX;
+        mt.tok[w] = (s >= 0 && s < L) ? ((unsigned)j < (unsigned)L ? j : 0) : INT_MAX;
+        if (w < kT5Win / 32) mt.used[w] = 0u;
+    }
+    __syncthreads();
     for (int x = threadIdx.x; x < kT5Win * 16; x += kT5Threads) {
         const int w = x >> 4, pc = x & 15;
-        const int s = kT5Rows * t - 64 + w;
         const uint32_t o = sw_off(w, 8 * pc, kPlK);
-        if (s >= 0 && s < L) {
-            int j = Pm[s];
-            j = (unsigned)j < (unsigned)L ? j : 0;
+        const int j = mt.tok[w];
+        if (j != INT_MAX) {
             cp_async16(smem_u32(Kt + o), qk + (head + j) * kT5D + 8 * pc);
             cp_async16(smem_u32(Vt + o), v + (head + j) * kT5D + 8 * pc);
         } else {
@@ -480,34 +511,31 @@ attn_bwd_tc5_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *_
     }
     for (int x = threadIdx.x; x < kT5Rows * 16; x += kT5Threads) {
         const int q = x >> 4, pc = x & 15;
-        const int s = kT5Rows * t + q;
         const uint32_t o = sw_off(q, 8 * pc, kPlQ);
-        if (s < L) {
-            int i = Pm[s];
-            i = (unsigned)i < (unsigned)L ? i : 0;
+        const int i = mt.tok[64 + q];
+        if (i != INT_MAX)
             cp_async16(smem_u32(Gt + o), g16 + (head + i) * kT5D + 8 * pc);
-        } else {
+        else
             *reinterpret_cast<uint4 *>(Gt + o) = make_uint4(0u, 0u, 0u, 0u);
-        }
     }
     for (int w = threadIdx.x; w < kT5Win; w += kT5Threads) {
-        const int s = kT5Rows * t - 64 + w;
-        const bool present = s >= 0 && s < L;
-        int j = present ? Pm[s] : 0;
-        j = (unsigned)j < (unsigned)L ? j : 0;
-        mt.tok[w] = present ? j : INT_MAX;
-        mt.bkt[w] = present ? buckets[seg * L + j] : -1;
-        mt.kin[w] = present ? inv_norm[head + j] : 0.f;
-        mt.kcs[w] = present ? scale * kLog2e * inv_norm[head + j] : 0.f;
+        const int j = mt.tok[w];
+        const bool present = j != INT_MAX;
+        const int jj = present ? j : 0;
+        const float kn = present ? inv_norm[head + jj] : 0.f;
+        mt.bkt[w] = present ? buckets[seg * L + jj] : -1;
+        mt.kin[w] = kn;
+        mt.kcs[w] = scale * kLog2e * kn;
         if (w >= 64) {
             const int q = w - 64;
-            mt.lq[q] = present ? lse[head + j] * kLog2e : 0.f;
-            mt.base[q] = present ? dsum[head + j] - (g_lse ? g_lse[head + j] : 0.f) : 0.f;
+            mt.lq[q] = present ? lse[head + jj] * kLog2e : 0.f;
+            mt.base[q] = present ? dsum[head + jj] - (g_lse ? g_lse[head + jj] : 0.f) : 0.f;
             mt.has[q] = 0;
         }
-        if (w < kT5Win / 32) mt.used[w] = 0u;
     }
     __syncthreads();
+    LSH_SPAN_END(t_gather, 0xa01);
+    LSH_SPAN_BEGIN(t_runs);
     // bucket runs of the window (sorted order keeps a bucket's rows together): warp 0 scans
     // the start flags forward and the end flags backward, 32 rows at a time
     if (warp == 0) {
@@ -537,8 +565,7 @@ attn_bwd_tc5_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *_
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    const uint32_t tmem = tmem_slot;
-    const uint32_t kb = smem_u32(Kt), vb = smem_u32(Vt), gb = smem_u32(Gt), pb = smem_u32(Pt);
+    LSH_SPAN_END(t_runs, 0xa02);
 
     // ---- 2. phase 1: S = Q K^T, dP = G V^T
     if (warp == 4) {
@@ -590,14 +617,21 @@ attn_bwd_tc5_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *_
         return vm;
     };
 
-    // ---- 3. pass A: E1 = ds scale / |k| (over P), E2 = ds scale (over the v rows)
+    // ---- 3. pass A: E1 = ds scale / |k| (over P), E2 = ds scale (over the v rows); the
+    // row's P stays in registers (bf16 pairs) until dQ has read E1
+    uint32_t pp[3][16];
     {
         ok = wait(&bar_mma, 0, abort_flag, status, 0x901);
         fence_after_sync();
+        LSH_SPAN_BEGIN(t_pa);
         bool any = false;
-        for (int c = 3 * half; c < 3 * half + 3; ++c) {
+#pragma unroll
+        for (int cc = 0; cc < 3; ++cc) {
+            const int c = 3 * half + cc;
             float pi[32], ds[32], e1[32], e2[32];
             const unsigned vm = row_batch(c, true, pi, ds);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) pp[cc][k] = pack_bf16x2(pi[2 * k], pi[2 * k + 1]);
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) {
                 e2[jj] = ds[jj] * scale;
@@ -611,6 +645,7 @@ attn_bwd_tc5_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *_
         }
         if (any) atomicOr(&mt.has[q], 1);
         fence_proxy_async();
+        LSH_SPAN_END(t_pa, 0xa03);
     }
     fence_before_sync();
     __syncthreads();
@@ -627,16 +662,15 @@ attn_bwd_tc5_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *_
         mma_commit(smem_u32(&bar_mma));
     }
 
-    // ---- 5. pass B: P = pi over E1 once dQ has read it
+    // ---- 5. pass B: P over E1 once dQ has read it
     {
         ok = wait(&bar_mma, 1, abort_flag, status, 0x902) && ok;
         fence_after_sync();
-        for (int c = 3 * half; c < 3 * half + 3; ++c) {
-            float pi[32], ds[32];
-            row_batch(c, false, pi, ds);
-            put_row32(Pt, kPlQ, q, 32 * c, pi);
-        }
+        LSH_SPAN_BEGIN(t_pb);
+#pragma unroll
+        for (int cc = 0; cc < 3; ++cc) put_row32p(Pt, kPlQ, q, 32 * (3 * half + cc), pp[cc]);
         fence_proxy_async();
+        LSH_SPAN_END(t_pb, 0xa04);
     }
     fence_before_sync();
     __syncthreads();
@@ -654,78 +688,92 @@ attn_bwd_tc5_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *_
         mma_commit(smem_u32(&bar_done));
     }
 
-    // ---- 7. epilogue (all eight warps; the two halves of a lane quarter split the columns)
+    // ---- 7. epilogue (all eight warps).  After the last commit every MMA has read its
+    // operands, so the v, g_out and P tiles (128 KB from kT5OffV) are free.  The gradients
+    // pass through them as fp32 rows [window row][d] (528-byte pitch: the rows a warp
+    // touches at once fall on distinct banks), and a warp adds a whole 512-byte row to dv
+    // or dqk with one float4 atomic per lane (lane l: d = 4 l .. 4 l + 3), where one token
+    // per lane would scatter 32 rows per instruction.  A token that is both a key (window
+    // row 64 + q) and a query (row q) of the tile gets its two dqk terms summed here
+    // first, so it costs one row update instead of two.
     {
-        ok = wait(&bar_done, 0, abort_flag, status, 0x903) && ok;
+        ok = wait(&bar_done, it & 1, abort_flag, status, 0x903) && ok;
         fence_after_sync();
-        // dQ: lane = query row, columns = d
-        const bool hq = qlive && mt.has[q];
+        LSH_SPAN_BEGIN(t_eq);
+        constexpr int kXs = kT5D + 4;
+        float *X = reinterpret_cast<float *>(sm + kT5OffV);
         const int tq = qlive ? mt.tok[qi] : 0;
-        for (int c = 2 * half; c < 2 * half + 2; ++c) {
-            uint32_t r[32];
-            tmem_ld32(tl + 2 * kT5Win + 32 * c, r);
-            tmem_wait_ld(r);
-            if (hq && ok) {
-                float *dst = dqk + (head + tq) * kT5D + 32 * c;
-#pragma unroll
-                for (int g4 = 0; g4 < 8; ++g4)
-                    atomicAdd(reinterpret_cast<float4 *>(dst + 4 * g4),
-                              make_float4(__uint_as_float(r[4 * g4]), __uint_as_float(r[4 * g4 + 1]),
-                                          __uint_as_float(r[4 * g4 + 2]), __uint_as_float(r[4 * g4 + 3])));
-            }
-        }
-        // dV^T and dK^T: lane = column d of v and qk, columns = window keys
         const int d = 32 * quarter + lane;
-        for (int c = 3 * half; c < 3 * half + 3; ++c) {
-            uint32_t r[32], gk[32];
-            tmem_ld32(tl + 32 * c, r);
-            tmem_ld32(tl + kT5Win + 32 * c, gk);
-            tmem_wait_ld(r, gk);
-            const unsigned used = mt.used[c];
-            if (ok) {
+        auto key_used = [&](int w) { return (mt.used[w >> 5] >> (w & 31)) & 1u; };
+        // dV^T or dK^T (TMEM lane = d, columns = window keys) into the rows
+        auto stage_keys = [&](uint32_t col0) {
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj)
-                    if ((used >> jj) & 1u)
-                        atomicAdd(dv + (head + mt.tok[32 * c + jj]) * kT5D + d, __uint_as_float(r[jj]));
+            for (int cc = 0; cc < 3; ++cc) {
+                const int c = 3 * half + cc;
+                uint32_t r[32];
+                tmem_ld32(tl + col0 + 32 * c, r);
+                tmem_wait_ld(r);
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) X[(32 * c + jj) * kXs + d] = __uint_as_float(r[jj]);
             }
-            // key role: dqk_j += (g - khat (khat . g)) / |k_j|, the dot over d across the
-            // 128 lanes of the half: a transposing butterfly in the warp, then its 4 warps
-            float pr[32], kh[32];
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-                const int w = 32 * c + jj;
-                const float kf = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(Kt + sw_off(w, d, kPlK)));
-                kh[jj] = kf * mt.kin[w];
-                pr[jj] = kh[jj] * __uint_as_float(gk[jj]);
+        };
+        stage_keys(0);
+        __syncthreads();
+        for (int w = warp; w < kT5Win; w += kT5Threads / 32)
+            if (key_used(w) && ok)
+                atomicAdd(reinterpret_cast<float4 *>(dv + (head + mt.tok[w]) * kT5D) + lane,
+                          reinterpret_cast<const float4 *>(X + w * kXs)[lane]);
+        __syncthreads();
+        LSH_SPAN_END(t_eq, 0xa05);
+        LSH_SPAN_BEGIN(t_ek);
+        stage_keys(kT5Win);
+        __syncthreads();
+        // key role: dqk_j += (g - khat (khat . g)) / |k_j|, khat = k_j / |k_j|, the dot over
+        // the row's d by the warp (lane l: d = 4 l .. 4 l + 3); rows of unused keys become 0
+        for (int w = warp; w < kT5Win; w += kT5Threads / 32) {
+            float4 *xr = reinterpret_cast<float4 *>(X + w * kXs);
+            float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (key_used(w)) {                                           // warp-uniform
+                const float4 g = xr[lane];
+                const uint2 kr = *reinterpret_cast<const uint2 *>(Kt + sw_off(w, 4 * lane, kPlK));
+                const float2 k01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kr.x));
+                const float2 k23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kr.y));
+                const float kn = mt.kin[w];
+                const float h0 = k01.x * kn, h1 = k01.y * kn, h2 = k23.x * kn, h3 = k23.y * kn;
+                const float dot = warp_sum(h0 * g.x + h1 * g.y + h2 * g.z + h3 * g.w);
+                val = make_float4(kn * (g.x - h0 * dot), kn * (g.y - h1 * dot),
+                                  kn * (g.z - h2 * dot), kn * (g.w - h3 * dot));
             }
-#pragma unroll
-            for (int s2 = 16; s2 >= 1; s2 >>= 1) {
-                const bool up = (lane & s2) != 0;
-#pragma unroll
-                for (int i2 = 0; i2 < s2; ++i2) {
-                    const float lo = pr[i2], hi = pr[i2 + s2];
-                    const float send = up ? lo : hi;
-                    const float keep = up ? hi : lo;
-                    pr[i2] = keep + __shfl_xor_sync(0xffffffffu, send, s2);
-                }
-            }
-            mt.red[half][quarter][lane] = pr[0];      // the warp's sum for key 32 c + lane
-            named_bar_sync(1 + half, 128);
-            if (quarter == 0)
-                mt.proj[half][lane] = mt.red[half][0][lane] + mt.red[half][1][lane] +
-                                      mt.red[half][2][lane] + mt.red[half][3][lane];
-            named_bar_sync(1 + half, 128);
-            if (ok) {
-#pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    if (!((used >> jj) & 1u)) continue;
-                    const int w = 32 * c + jj;
-                    const float val = mt.kin[w] * (__uint_as_float(gk[jj]) - kh[jj] * mt.proj[half][jj]);
-                    atomicAdd(dqk + (head + mt.tok[w]) * kT5D + d, val);
-                }
-            }
-            named_bar_sync(1 + half, 128);            // red and proj are reused
+            xr[lane] = val;
         }
+        __syncthreads();
+        {
+            // query role: dQ (TMEM lane = query row q, this warp's half of d) onto row 64 + q
+            uint32_t r0[32], r1[32];
+            tmem_ld32(tl + 2 * kT5Win + 64 * half, r0);
+            tmem_ld32(tl + 2 * kT5Win + 64 * half + 32, r1);
+            tmem_wait_ld(r0, r1);
+            float4 *xr = reinterpret_cast<float4 *>(X + qi * kXs) + 16 * half;
+#pragma unroll
+            for (int g4 = 0; g4 < 8; ++g4) {
+                float4 a = xr[g4], b = xr[8 + g4];
+                a.x += __uint_as_float(r0[4 * g4]);     a.y += __uint_as_float(r0[4 * g4 + 1]);
+                a.z += __uint_as_float(r0[4 * g4 + 2]); a.w += __uint_as_float(r0[4 * g4 + 3]);
+                b.x += __uint_as_float(r1[4 * g4]);     b.y += __uint_as_float(r1[4 * g4 + 1]);
+                b.z += __uint_as_float(r1[4 * g4 + 2]); b.w += __uint_as_float(r1[4 * g4 + 3]);
+                xr[g4] = a;
+                xr[8 + g4] = b;
+            }
+        }
+        __syncthreads();
+        for (int w = warp; w < kT5Win; w += kT5Threads / 32) {
+            const int qq = w - 64;
+            const bool qrow = qq >= 0 && kT5Rows * t + qq < L && mt.has[qq];
+            if ((key_used(w) || qrow) && ok)                             // warp-uniform
+                atomicAdd(reinterpret_cast<float4 *>(dqk + (head + mt.tok[w]) * kT5D) + lane,
+                          reinterpret_cast<const float4 *>(X + w * kXs)[lane]);
+        }
+        LSH_SPAN_END(t_ek, 0xa06);
         // a token with no key in any round copies v_i: 1 / n_rounds of g_out from each round
         if (half == 0 && ok && qlive && !mt.has[q] && mt.lq[q] < 0.5f * kSelfLogit * kLog2e) {
             const float wself = 1.0f / (float)n_rounds;
@@ -736,11 +784,20 @@ attn_bwd_tc5_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *_
             }
         }
     }
+    LSH_SPAN_END(t_all, 0xa0f);
+    // the next unit overwrites the tiles, the staged rows and TMEM: every thread is done
+    // with them (and a failed wait anywhere ends the loop for the whole CTA)
+    fence_before_sync();
+    failed = __syncthreads_or(!ok) != 0;
+    fence_after_sync();
+    if (failed) break;
+    }
 
-    // ---- teardown: every MMA has completed (the last commit covers all of them)
-    if (warp == 4) {
+    // ---- teardown.  Normally every MMA has completed (each unit waited for its last
+    // commit); after a failed wait, give the unit's MMAs a bounded wait first.
+    if (warp == 4 && failed) {
         int dummy = 0;
-        wait_w(&bar_done, 0, &dummy, status, 0x904);
+        wait_w(&bar_done, it & 1, &dummy, status, 0x904);
     }
     fence_before_sync();
     __syncthreads();
@@ -785,10 +842,13 @@ cudaError_t attn_bwd_tc(const Problem &p, const void *qk, const void *v, const i
         e = cudaFuncSetAttribute(attn_bwd_tc5_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kT5Smem);
         if (e != cudaSuccess) return e;
-        const long blocks = p.n_seg() * ((p.L + kT5Rows - 1) / kT5Rows);
-        attn_bwd_tc5_kernel<<<(unsigned)blocks, kT5Threads, kT5Smem, st>>>(
+        const long units = p.n_seg() * ((p.L + kT5Rows - 1) / kT5Rows);
+        int dev = 0, sms = 148;
+        if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        const long grid = units < sms ? units : sms;
+        attn_bwd_tc5_kernel<<<(unsigned)grid, kT5Threads, kT5Smem, st>>>(
             (const __nv_bfloat16 *)qk, (const __nv_bfloat16 *)v, buckets, perm, inv_norm, lse, g_out,
-            g16, dsum, g_lse, p.L, p.n_rounds, p.causal, p.scale, dqk, dv, status);
+            g16, dsum, g_lse, p.L, p.n_rounds, p.causal, p.scale, dqk, dv, units, status);
         return cudaGetLastError();
     }
     return cudaErrorInvalidValue;
