@@ -385,15 +385,16 @@ cudaError_t launch_tc(const Problem &p, const void *qk, const void *v, const int
 //     phase 2   dV^T = G^T P   [0, 192)     dK^T = Q^T E2   [192, 384) (M = d, N 192)
 //     epilogue  dV^T, dK^T + dQ through the freed v / g_out / P tiles as fp32 rows, each
 //               added to dv or dqk by one warp
-// Warps w and w + 4 share TMEM lane quarter w (a query row, or in phase 2 a column d)
-// and split the columns; warp 4 also issues the MMAs and owns TMEM; all eight gather.
+// Warps w, w + 4, w + 8 and w + 12 share TMEM lane quarter w (a query row, or in phase 2
+// a column d) and split the columns four ways; warp 4 also issues the MMAs and owns TMEM;
+// all sixteen gather.
 // A row's keys are one interval of the window (its bucket run, clipped to its window, and
 // before it when causal), from run bounds computed once per tile.  One mbarrier takes the first two commits
 // (phase 1, then dQ: waited with parities 0 and 1 by warps that saw the one before), a
 // second the last (phase 2: every MMA of the CTA), so no wait can alias a phase.
 constexpr int kT5Rows = 128, kT5Win = 192, kT5D = 128;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kT5Threads = 256;
+constexpr int kT5Threads = 512;
 constexpr int kPlK = kT5Win * 128;                   // window-tile plane (192 rows)
 constexpr int kPlQ = kT5Rows * 128;                  // query-tile plane (128 rows)
 constexpr size_t kT5OffK = 0;                        // qk window rows, 2 planes
@@ -418,11 +419,11 @@ __device__ __forceinline__ uint32_t sw_off(int row, int col, int plane)
     return (uint32_t)((col >> 6) * plane + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4) + (col & 7) * 2);
 }
 
-// 32 consecutive columns [c0, c0 + 32) of row `row` of a 16-bit tile, from fp32 values
-__device__ __forceinline__ void put_row32(uint8_t *tile, int plane, int row, int c0, const float (&x)[32])
+// 16 consecutive columns [c0, c0 + 16) of row `row` of a 16-bit tile, from fp32 values
+__device__ __forceinline__ void put_row16(uint8_t *tile, int plane, int row, int c0, const float (&x)[16])
 {
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
+    for (int g = 0; g < 2; ++g) {
         uint4 u;
         u.x = pack_bf16x2(x[8 * g], x[8 * g + 1]);
         u.y = pack_bf16x2(x[8 * g + 2], x[8 * g + 3]);
@@ -431,16 +432,14 @@ __device__ __forceinline__ void put_row32(uint8_t *tile, int plane, int row, int
         *reinterpret_cast<uint4 *>(tile + sw_off(row, c0 + 8 * g, plane)) = u;
     }
 }
-
-// the same 32 columns from bf16 pairs already packed (word k = columns c0 + 2k, c0 + 2k + 1)
-__device__ __forceinline__ void put_row32p(uint8_t *tile, int plane, int row, int c0, const uint32_t (&u)[16])
+// the same 16 columns from bf16 pairs already packed (word k = columns c0 + 2k, c0 + 2k + 1)
+__device__ __forceinline__ void put_row16p(uint8_t *tile, int plane, int row, int c0, const uint32_t (&u)[8])
 {
 #pragma unroll
-    for (int g = 0; g < 4; ++g)
+    for (int g = 0; g < 2; ++g)
         *reinterpret_cast<uint4 *>(tile + sw_off(row, c0 + 8 * g, plane)) =
             make_uint4(u[4 * g], u[4 * g + 1], u[4 * g + 2], u[4 * g + 3]);
 }
-
 __global__ void __launch_bounds__(kT5Threads, 1)
 attn_bwd_tc5_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *__restrict__ v,
                     const int32_t *__restrict__ buckets, const int32_t *__restrict__ perm,
@@ -454,6 +453,9 @@ attn_bwd_tc5_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *_
     __shared__ uint64_t bar_mma, bar_done;            // phases 1 and pass A's MMA; phase 2
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag_s;
+    // the next unit's permutation entries and row metadata, fetched while this one computes
+    __shared__ int nx_tok[kT5Win], nx_bkt[kT5Win];
+    __shared__ float nx_kin[kT5Win], nx_lse[kT5Win], nx_dsum[kT5Win], nx_glse[kT5Win];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *Kt = sm + kT5OffK, *Vt = sm + kT5OffV, *Gt = sm + kT5OffG, *Pt = sm + kT5OffP;
     T5Meta &mt = *reinterpret_cast<T5Meta *>(sm + kT5OffMeta);
@@ -483,17 +485,22 @@ attn_bwd_tc5_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *_
     const long bh = seg / n_rounds;
     const size_t head = (size_t)bh * L;
     const int32_t *Pm = perm + seg * L;
+    const long un = u + gridDim.x;                 // this CTA's next unit
+    const long seg2 = un / tps;
+    const int t2 = (int)(un - seg2 * tps);
     LSH_SPAN_BEGIN(t_all);
     LSH_SPAN_BEGIN(t_gather);
 
     // ---- 1. gather: window rows w (sorted 128 t - 64 + w) and query rows q (128 t + q,
-    // the window's rows 64 + q).  The permutation entries come first (one load per row, all
-    // in flight at once); the row copies are then issued from shared memory with no load
-    // on their path, and the row metadata loads go out while the copies stream.
+    // the window's rows 64 + q).  The permutation entries and row metadata of every unit
+    // but a CTA's first were fetched during its previous unit (nx_*); the row copies are
+    // issued from shared memory with no load on their path.
+    const bool pre = it > 0;
     for (int w = threadIdx.x; w < kT5Win; w += kT5Threads) {
         const int s = kT5Rows * t - 64 + w;
-        int j = (s >= 0 && s < L) ? Pm[s] : INT_MAX;
-        mt.tok[w] = (s >= 0 && s < L) ? ((unsigned)j < (unsigned)L ? j : 0) : INT_MAX;
+        const bool in = s >= 0 && s < L;
+        const int j = in ? (pre ? nx_tok[w] : Pm[s]) : INT_MAX;
+        mt.tok[w] = in ? ((unsigned)j < (unsigned)L ? j : 0) : INT_MAX;
         if (w < kT5Win / 32) mt.used[w] = 0u;
     }
     __syncthreads();
@@ -522,14 +529,17 @@ attn_bwd_tc5_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *_
         const int j = mt.tok[w];
         const bool present = j != INT_MAX;
         const int jj = present ? j : 0;
-        const float kn = present ? inv_norm[head + jj] : 0.f;
-        mt.bkt[w] = present ? buckets[seg * L + jj] : -1;
+        const float kn = present ? (pre ? nx_kin[w] : inv_norm[head + jj]) : 0.f;
+        mt.bkt[w] = present ? (pre ? nx_bkt[w] : buckets[seg * L + jj]) : -1;
         mt.kin[w] = kn;
         mt.kcs[w] = scale * kLog2e * kn;
         if (w >= 64) {
             const int q = w - 64;
-            mt.lq[q] = present ? lse[head + jj] * kLog2e : 0.f;
-            mt.base[q] = present ? dsum[head + jj] - (g_lse ? g_lse[head + jj] : 0.f) : 0.f;
+            const float l = pre ? nx_lse[w] : lse[head + jj];
+            const float ds = pre ? nx_dsum[w] : dsum[head + jj];
+            const float gl = g_lse ? (pre ? nx_glse[w] : g_lse[head + jj]) : 0.f;
+            mt.lq[q] = present ? l * kLog2e : 0.f;
+            mt.base[q] = present ? ds - gl : 0.f;
             mt.has[q] = 0;
         }
     }
@@ -580,9 +590,9 @@ attn_bwd_tc5_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *_
         mma_commit(smem_u32(&bar_mma));
     }
 
-    // rows: warps w and w + 4 share TMEM lane quarter w (query q = its lane) and split the
-    // column batches (keys [0, 96) and [96, 192); d [0, 64) and [64, 128) for dQ)
-    const int quarter = warp & 3, half = warp >> 2;
+    // rows: warps w, w + 4, w + 8, w + 12 share TMEM lane quarter w (query q = its lane)
+    // and split the columns four ways (keys [48 p, 48 p + 48), d [32 p, 32 p + 32))
+    const int quarter = warp & 3, part = warp >> 2;
     const int q = 32 * quarter + lane, qi = 64 + q;
     const bool qlive = kT5Rows * t + q < L;
     const uint32_t tl = tmem + ((uint32_t)(32 * quarter) << 16);
@@ -595,23 +605,20 @@ attn_bwd_tc5_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *_
     const float lq2 = qlive ? mt.lq[q] : 0.f, bs = qlive ? mt.base[q] : 0.f;
     bool ok = true;
 
-    // the row's weights pi (and score gradients ds) of keys [32 c, 32 c + 32)
-    auto row_batch = [&](int c, bool with_ds, float (&pi)[32], float (&ds)[32]) -> unsigned {
-        uint32_t sv[32], pv[32];
-        tmem_ld32(tl + 32 * c, sv);
-        if (with_ds) {
-            tmem_ld32(tl + kT5Win + 32 * c, pv);
-            tmem_wait_ld(sv, pv);
-        } else {
-            tmem_wait_ld(sv);
-        }
+    // the row's weights pi (and score gradients ds) of keys [16 c, 16 c + 16)
+    auto row_batch = [&](int c, float (&pi)[16], float (&ds)[16]) -> unsigned {
+        uint32_t sv[16], pv[16];
+        tmem_ld16(tl + 16 * c, sv);
+        tmem_ld16(tl + kT5Win + 16 * c, pv);
+        tmem_wait_ld16(sv);
+        tmem_tie16(pv);
         unsigned vm = 0u;
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-            const int w = 32 * c + jj;
+        for (int jj = 0; jj < 16; ++jj) {
+            const int w = 16 * c + jj;
             const bool valid = w >= klo && w < khi && w != qi;
             pi[jj] = valid ? exp2f(__uint_as_float(sv[jj]) * mt.kcs[w] - lq2) : 0.f;
-            if (with_ds) ds[jj] = pi[jj] * (__uint_as_float(pv[jj]) - bs);
+            ds[jj] = pi[jj] * (__uint_as_float(pv[jj]) - bs);
             vm |= valid ? 1u << jj : 0u;
         }
         return vm;
@@ -619,29 +626,35 @@ attn_bwd_tc5_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *_
 
     // ---- 3. pass A: E1 = ds scale / |k| (over P), E2 = ds scale (over the v rows); the
     // row's P stays in registers (bf16 pairs) until dQ has read E1
-    uint32_t pp[3][16];
+    uint32_t pp[3][8];
     {
         ok = wait(&bar_mma, 0, abort_flag, status, 0x901);
         fence_after_sync();
         LSH_SPAN_BEGIN(t_pa);
+        // the next unit's permutation entries (this thread's window row), in flight until
+        // the epilogue
+        if (un < n_units && threadIdx.x < kT5Win) {
+            const int s2 = kT5Rows * t2 - 64 + (int)threadIdx.x;
+            if (s2 >= 0 && s2 < L) cp_async4(smem_u32(&nx_tok[threadIdx.x]), perm + seg2 * L + s2);
+        }
         bool any = false;
 #pragma unroll
         for (int cc = 0; cc < 3; ++cc) {
-            const int c = 3 * half + cc;
-            float pi[32], ds[32], e1[32], e2[32];
-            const unsigned vm = row_batch(c, true, pi, ds);
+            const int c = 3 * part + cc;
+            float pi[16], ds[16], e1[16], e2[16];
+            const unsigned vm = row_batch(c, pi, ds);
 #pragma unroll
-            for (int k = 0; k < 16; ++k) pp[cc][k] = pack_bf16x2(pi[2 * k], pi[2 * k + 1]);
+            for (int k = 0; k < 8; ++k) pp[cc][k] = pack_bf16x2(pi[2 * k], pi[2 * k + 1]);
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
+            for (int jj = 0; jj < 16; ++jj) {
                 e2[jj] = ds[jj] * scale;
-                e1[jj] = e2[jj] * mt.kin[32 * c + jj];
+                e1[jj] = e2[jj] * mt.kin[16 * c + jj];
             }
-            put_row32(Pt, kPlQ, q, 32 * c, e1);
-            put_row32(Vt, kPlQ, q, 32 * c, e2);
+            put_row16(Pt, kPlQ, q, 16 * c, e1);
+            put_row16(Vt, kPlQ, q, 16 * c, e2);
             any |= vm != 0u;
             const unsigned col = __reduce_or_sync(0xffffffffu, vm);
-            if (lane == 0 && col) atomicOr(&mt.used[c], col);
+            if (lane == 0 && col) atomicOr(&mt.used[c >> 1], col << (16 * (c & 1)));
         }
         if (any) atomicOr(&mt.has[q], 1);
         fence_proxy_async();
@@ -668,7 +681,7 @@ attn_bwd_tc5_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *_
         fence_after_sync();
         LSH_SPAN_BEGIN(t_pb);
 #pragma unroll
-        for (int cc = 0; cc < 3; ++cc) put_row32p(Pt, kPlQ, q, 32 * (3 * half + cc), pp[cc]);
+        for (int cc = 0; cc < 3; ++cc) put_row16p(Pt, kPlQ, q, 16 * (3 * part + cc), pp[cc]);
         fence_proxy_async();
         LSH_SPAN_END(t_pb, 0xa04);
     }
@@ -700,6 +713,23 @@ attn_bwd_tc5_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *_
         ok = wait(&bar_done, it & 1, abort_flag, status, 0x903) && ok;
         fence_after_sync();
         LSH_SPAN_BEGIN(t_eq);
+        // the next unit's row metadata, from its permutation entries (landed by now)
+        if (un < n_units && threadIdx.x < kT5Win) {
+            const int w = threadIdx.x, s2 = kT5Rows * t2 - 64 + w;
+            cp_async_wait_all();
+            if (s2 >= 0 && s2 < L) {
+                int j = nx_tok[w];
+                j = (unsigned)j < (unsigned)L ? j : 0;
+                const size_t head2 = (size_t)(seg2 / n_rounds) * L;
+                cp_async4(smem_u32(&nx_bkt[w]), buckets + seg2 * L + j);
+                cp_async4(smem_u32(&nx_kin[w]), inv_norm + head2 + j);
+                if (w >= 64) {
+                    cp_async4(smem_u32(&nx_lse[w]), lse + head2 + j);
+                    cp_async4(smem_u32(&nx_dsum[w]), dsum + head2 + j);
+                    if (g_lse) cp_async4(smem_u32(&nx_glse[w]), g_lse + head2 + j);
+                }
+            }
+        }
         constexpr int kXs = kT5D + 4;
         float *X = reinterpret_cast<float *>(sm + kT5OffV);
         const int tq = qlive ? mt.tok[qi] : 0;
@@ -709,12 +739,12 @@ attn_bwd_tc5_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *_
         auto stage_keys = [&](uint32_t col0) {
 #pragma unroll
             for (int cc = 0; cc < 3; ++cc) {
-                const int c = 3 * half + cc;
-                uint32_t r[32];
-                tmem_ld32(tl + col0 + 32 * c, r);
-                tmem_wait_ld(r);
+                const int c = 3 * part + cc;
+                uint32_t r[16];
+                tmem_ld16(tl + col0 + 16 * c, r);
+                tmem_wait_ld16(r);
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) X[(32 * c + jj) * kXs + d] = __uint_as_float(r[jj]);
+                for (int jj = 0; jj < 16; ++jj) X[(16 * c + jj) * kXs + d] = __uint_as_float(r[jj]);
             }
         };
         stage_keys(0);
@@ -748,21 +778,18 @@ attn_bwd_tc5_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *_
         }
         __syncthreads();
         {
-            // query role: dQ (TMEM lane = query row q, this warp's half of d) onto row 64 + q
-            uint32_t r0[32], r1[32];
-            tmem_ld32(tl + 2 * kT5Win + 64 * half, r0);
-            tmem_ld32(tl + 2 * kT5Win + 64 * half + 32, r1);
-            tmem_wait_ld(r0, r1);
-            float4 *xr = reinterpret_cast<float4 *>(X + qi * kXs) + 16 * half;
+            // query role: dQ (TMEM lane = query row q, this warp's quarter of d) onto row
+            // 64 + q
+            uint32_t r0[32];
+            tmem_ld32(tl + 2 * kT5Win + 32 * part, r0);
+            tmem_wait_ld(r0);
+            float4 *xr = reinterpret_cast<float4 *>(X + qi * kXs) + 8 * part;
 #pragma unroll
             for (int g4 = 0; g4 < 8; ++g4) {
-                float4 a = xr[g4], b = xr[8 + g4];
+                float4 a = xr[g4];
                 a.x += __uint_as_float(r0[4 * g4]);     a.y += __uint_as_float(r0[4 * g4 + 1]);
                 a.z += __uint_as_float(r0[4 * g4 + 2]); a.w += __uint_as_float(r0[4 * g4 + 3]);
-                b.x += __uint_as_float(r1[4 * g4]);     b.y += __uint_as_float(r1[4 * g4 + 1]);
-                b.z += __uint_as_float(r1[4 * g4 + 2]); b.w += __uint_as_float(r1[4 * g4 + 3]);
                 xr[g4] = a;
-                xr[8 + g4] = b;
             }
         }
         __syncthreads();
@@ -775,7 +802,7 @@ attn_bwd_tc5_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *_
         }
         LSH_SPAN_END(t_ek, 0xa06);
         // a token with no key in any round copies v_i: 1 / n_rounds of g_out from each round
-        if (half == 0 && ok && qlive && !mt.has[q] && mt.lq[q] < 0.5f * kSelfLogit * kLog2e) {
+        if (part == 0 && ok && qlive && !mt.has[q] && mt.lq[q] < 0.5f * kSelfLogit * kLog2e) {
             const float wself = 1.0f / (float)n_rounds;
             for (int c = 0; c < kT5D; c += 4) {
                 const float4 g = *reinterpret_cast<const float4 *>(g_out + (head + tq) * kT5D + c);
@@ -786,7 +813,9 @@ attn_bwd_tc5_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *_
     }
     LSH_SPAN_END(t_all, 0xa0f);
     // the next unit overwrites the tiles, the staged rows and TMEM: every thread is done
-    // with them (and a failed wait anywhere ends the loop for the whole CTA)
+    // with them, and its prefetched metadata has landed (a failed wait anywhere ends the
+    // loop for the whole CTA)
+    cp_async_wait_all();
     fence_before_sync();
     failed = __syncthreads_or(!ok) != 0;
     fence_after_sync();
