@@ -2,15 +2,17 @@
 // copies.
 //
 // Inside the fused forward the attention step writes round r's row of token i at position
-// i of plane r (o_r [B][H][R][L][d] bf16, lse_r [B][H][R][L]).  Then for a tile of 32
-// consecutive tokens of one head, each round's rows are one contiguous 32*d*2-byte block
-// and its log-normalisers one 128-byte block.  One producer lane moves these blocks into
+// i of plane r (o_r [B][H][R][L][d] bf16, lse_r [B][H][R][L]).  Then for a tile of 16
+// consecutive tokens of one head, each round's rows are one contiguous 16*d*2-byte block
+// and its log-normalisers one 64-byte block.  One producer lane moves these blocks into
 // a 3-stage shared-memory ring with cp.async.bulk (large contiguous transfers, which the
 // copy engine streams at full rate; a warp gathering the same rows token by token touches
-// R DRAM pages per token instead).  Eight consumer warps then combine four tokens each:
+// R DRAM pages per token instead).  Eight consumer warps then combine two tokens each:
 //   lse_i = logsumexp_r lse_r(i),   out_i = sum_r exp(lse_r(i) - lse_i) * o_r(i)
 // (rounds weighted by their share of the softmax mass, as in combine.cu), and stream the
-// fp32 outputs.  Persistent CTAs, one per SM; every wait is bounded (sm100::wait).
+// fp32 outputs.  Persistent CTAs, two per SM (two independent copy pipelines keep more
+// DRAM reads in flight than one CTA with a deeper ring); every wait is bounded
+// (sm100::wait).
 #include <math.h>
 
 #include "sm100.cuh"
@@ -20,11 +22,12 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kT = 32;            // tokens per tile
+constexpr int kT = 16;            // tokens per tile
 constexpr int kStages = 3;
 constexpr int kMaxR = 8;          // rounds this kernel takes
 constexpr int kCWarps = 8;        // consumer warps, kT / kCWarps tokens each
 constexpr int kThreads = (kCWarps + 1) * 32;
+constexpr int kCtasPerSm = 2;
 
 struct __align__(8) CombineBars {
     uint64_t full[kStages], empty[kStages];
@@ -36,7 +39,7 @@ __host__ __device__ constexpr size_t stage_bytes(int d) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
 combine_tma_kernel(const __nv_bfloat16 *__restrict__ o_r, const float *__restrict__ lse_r,
                    long n_tiles, int L, int R, float *__restrict__ out, float *__restrict__ lse,
                    StatusBlock *status)
@@ -156,7 +159,7 @@ cudaError_t launch(const Problem &p, const void *o_r, const float *lse_r, float 
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const long grid = n_tiles < sms ? n_tiles : sms;
+    const long grid = n_tiles < (long)kCtasPerSm * sms ? n_tiles : (long)kCtasPerSm * sms;
     combine_tma_kernel<D><<<(unsigned)grid, kThreads, smem, st>>>(
         (const __nv_bfloat16 *)o_r, lse_r, n_tiles, p.L, p.n_rounds, out, lse, status);
     return cudaGetLastError();
