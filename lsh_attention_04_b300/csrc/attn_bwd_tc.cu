@@ -392,6 +392,14 @@ cudaError_t launch_tc(const Problem &p, const void *qk, const void *v, const int
 // before it when causal), from run bounds computed once per tile.  One mbarrier takes the first two commits
 // (phase 1, then dQ: waited with parities 0 and 1 by warps that saw the one before), a
 // second the last (phase 2: every MMA of the CTA), so no wait can alias a phase.
+// 2^x by the special-function unit (relative error near 2^-22).  Results below 2^-126
+// flush to 0: a row's weights sum to 1 over at most 128 keys, so its largest is at least
+// 2^-7 and a flushed one is below 2^-119 of it.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 constexpr int kT5Rows = 128, kT5Win = 192, kT5D = 128;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kT5Threads = 512;
@@ -617,7 +625,7 @@ attn_bwd_tc5_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *_
         for (int jj = 0; jj < 16; ++jj) {
             const int w = 16 * c + jj;
             const bool valid = w >= klo && w < khi && w != qi;
-            pi[jj] = valid ? exp2f(__uint_as_float(sv[jj]) * mt.kcs[w] - lq2) : 0.f;
+            pi[jj] = valid ? ex2(fmaf(__uint_as_float(sv[jj]), mt.kcs[w], -lq2)) : 0.f;
             ds[jj] = pi[jj] * (__uint_as_float(pv[jj]) - bs);
             vm |= valid ? 1u << jj : 0u;
         }
