@@ -393,8 +393,8 @@ cudaError_t launch_tc(const Problem &p, const void *qk, const void *v, const int
 // (phase 1, then dQ: waited with parities 0 and 1 by warps that saw the one before), a
 // second the last (phase 2: every MMA of the CTA), so no wait can alias a phase.
 // 2^x by the special-function unit (relative error near 2^-22).  Results below 2^-126
-// flush to 0: a row's weights sum to 1 over at most 128 keys, so its largest is at least
-// 2^-7 and a flushed one is below 2^-119 of it.
+// flush to 0: the weights here are a token's softmax weights over the keys of all its
+// rounds (their total is 1), so a flushed one is below 2^-126 of that total.
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
