@@ -49,9 +49,9 @@
 // one warp's cp.async stream manages about 5-10.)  So every chunk is filled by several
 // loader warps at once.  The MMA warps fence the async proxy after each wait, since the
 // rows were written through the generic one.
-// Warp roles (16 warps, 128 registers each): 0-7 softmax + output epilogue (warps w and
-// w+4 share TMEM lane quarter w and split the row's columns and O's columns), 8 the
-// metadata warp, 9-13 row copiers, 14 S issuer and TMEM owner, 15 P V issuer.
+// Warp roles (24 warps, 80 registers each): 0-15 softmax + output epilogue (warps w, w+4,
+// w+8 and w+12 share TMEM lane quarter w and split the row's columns and O's columns four
+// ways), 16 the metadata warp, 17-21 row copiers, 22 S issuer and TMEM owner, 23 P V issuer.
 // Persistent CTAs take contiguous ranges of tiles of a group of heads small enough for
 // L2, so all rounds of those heads share cached rows.  Every wait is bounded
 // (sm100::wait); on a timeout the kernel records where in the workspace status block and
@@ -69,7 +69,7 @@ constexpr int kC = 64;            // chunk length
 constexpr int kRows = 128;        // rows per tile
 constexpr int kWin = 192;         // S columns per tile (window rows)
 constexpr int kSlots = 6;         // chunk ring (even: chunk parity = slot parity)
-constexpr int kSmWarps = 8;       // softmax / epilogue warps
+constexpr int kSmWarps = 16;      // softmax / epilogue warps (4 per TMEM lane quarter)
 constexpr int kLoaders = 6;       // loader warps: 1 metadata warp + kCopyWarps row copiers
 constexpr int kCopyWarps = kLoaders - 1;
 constexpr int kSWarp = kSmWarps + kLoaders;
@@ -234,7 +234,7 @@ lsh_attn_tc_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *__
 #ifdef LSH_WAIT_PROF
     __shared__ volatile long long slot_clk[kSlots];   // when a slot's fill was released
 #endif
-    __shared__ float l_part[kLBufs][2][kRows];   // partial row sums of the two column halves
+    __shared__ float l_part[kLBufs][4][kRows];   // partial row sums of the four column parts
     // 1024-byte aligned base, derived from the shared array by pointer arithmetic so the
     // compiler keeps the shared state space (shared loads, not generic ones)
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -518,15 +518,16 @@ lsh_attn_tc_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *__
     } else if (warp < kSmWarps) {
         // ------------------------------------------------------------- softmax + epilogue
         const int q4 = warp & 3;                   // TMEM lane quarter
-        const int half = warp >> 2;                // which half of the row's columns
+        const int part = warp >> 2;                // which quarter of the row's columns
         const int i = q4 * 32 + lane;              // tile row = TMEM lane
         const int hi_half = i >= kC;               // row of chunk 2t+1
         const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
-        const int colA = (hi_half ? kC : 0) + 64 * half;   // this warp's 64 S columns
-        // the third of the window outside the row's reach, zeroed by one of the halves
-        const int colZ = (hi_half ? 0 : 2 * kC) + 32 * half;
+        const int colA = (hi_half ? kC : 0) + 32 * part;   // this warp's 32 S columns
+        // the third of the window outside the row's reach (64 keys = packed P columns
+        // [z, z + 16) and [z + 32, z + 48)), zeroed 8 packed columns per part
+        const int colZ = (hi_half ? 0 : 2 * kC) + 32 * (part >> 1) + 8 * (part & 1);
         const int self_c0 = kC + 32 * q4;          // batch holding the rows' own columns
-        const int dh = P.d / 2;                    // O columns of this warp
+        const int dh = P.d / 4;                    // O columns of this warp
         uint32_t full_bits = 0;
         int ctr = 0;
         // epilogue state of the previous tile
@@ -542,12 +543,13 @@ lsh_attn_tc_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *__
             if (!__all_sync(FULL, w)) return false;
             fence_after_sync();
             LSH_SPAN_BEGIN(t_ep);
-            const float l = l_part[q % kLBufs][0][i] + l_part[q % kLBufs][1][i];
+            const float l = (l_part[q % kLBufs][0][i] + l_part[q % kLBufs][1][i]) +
+                            (l_part[q % kLBufs][2][i] + l_part[q % kLBufs][3][i]);
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
-            __nv_bfloat16 *dst = o_r + LSH_IDX(e_row, (long long)n_rows, 0x712) * P.d + half * dh;
-            for (int c = 0; c < dh; c += 32) {
+            __nv_bfloat16 *dst = o_r + LSH_IDX(e_row, (long long)n_rows, 0x712) * P.d + part * dh;
+            if (dh == 32) {
                 uint32_t o[32];
-                tmem_ld32(tl + kTmemO + half * dh + c, o);
+                tmem_ld32(tl + kTmemO + part * dh, o);
                 tmem_wait_ld(o);
                 if (e_live) {
                     uint32_t pk[16];
@@ -555,11 +557,23 @@ lsh_attn_tc_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *__
                     for (int k = 0; k < 16; ++k)
                         pk[k] = pack_bf16(__uint_as_float(o[2 * k]) * inv_l,
                                           __uint_as_float(o[2 * k + 1]) * inv_l);
-                    st_global_v8(dst + c, pk);
-                    st_global_v8(dst + c + 16, pk + 8);
+                    st_global_v8(dst, pk);
+                    st_global_v8(dst + 16, pk + 8);
+                }
+            } else {
+                uint32_t o[16];
+                tmem_ld16(tl + kTmemO + part * dh, o);
+                tmem_wait_ld16(o);
+                if (e_live) {
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        pk[k] = pack_bf16(__uint_as_float(o[2 * k]) * inv_l,
+                                          __uint_as_float(o[2 * k + 1]) * inv_l);
+                    st_global_v8(dst, pk);
                 }
             }
-            if (e_live && half == 0)
+            if (e_live && part == 0)
                 __stcs(&lse_r[LSH_IDX(e_row, (long long)n_rows, 0x713)],
                        e_self ? kSelfLogit : (e_m2 + __log2f(l)) * kLn2);
             LSH_SPAN_END(t_ep, 0x783);
@@ -650,36 +664,26 @@ lsh_attn_tc_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *__
                     // The pass read the partner warp's S columns: both warps of the lane
                     // quarter (which take this branch together: same rows, same bound)
                     // finish reading before either overwrites S with P.
-                    named_bar_sync(1 + q4, 64);
+                    named_bar_sync(1 + q4, 128);
                 }
 
                 LSH_SPAN_END(t_setup, 0x791);
                 LSH_SPAN_BEGIN(t_sm);
                 float l = 0.f;
-                // This warp's 64 columns are two 32-key batches (a mask and key scales
-                // each), processed as four 16-column quarters through two register
-                // buffers: quarter q+1 loads while q becomes P, so a tcgen05.ld is always
-                // in flight and the warp needs 32 registers of S, not 64.  P of quarter q
-                // (8 words at cc + 8 (q & 1)) only covers S columns already read.
-                const bool nb0 = batch_needed(colA), nb1 = batch_needed(colA + 32);
-                uint32_t vmb[2];
-                const float *csb[2];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int cc = colA + 32 * h;
-                    const int t0 = tk0 + cc;               // sorted index of batch column 0
-                    uint32_t vm = live ? range_mask(klo - t0, khi - t0) : 0u;
-                    if (cc == self_c0 && !P.causal) vm &= ~(1u << lane);
-                    vmb[h] = vm;
-                    csb[h] = meta[(2 * t - 1 + cc / kC + kSlots) % kSlots].cs + (cc & (kC - 1));
-                }
-                const bool self_here = colA == self_c0 || colA + 32 == self_c0;
-                auto quarter = [&](const uint32_t (&sq)[16], int q) {
-                    const int h = q >> 1, hq = q & 1;
-                    const int cc = colA + 32 * h;
+                // This warp's 32 columns are one 32-key batch (a mask and key scales),
+                // processed as two 16-column quarters; both loads are in flight before
+                // the one wait.  P of quarter q (8 words at colA + 8 q) only covers S
+                // columns already read.
+                const bool nb0 = batch_needed(colA);
+                const int t0 = tk0 + colA;                 // sorted index of batch column 0
+                uint32_t vm0 = live ? range_mask(klo - t0, khi - t0) : 0u;
+                if (colA == self_c0 && !P.causal) vm0 &= ~(1u << lane);
+                const float *cs0 = meta[(2 * t - 1 + colA / kC + kSlots) % kSlots].cs + (colA & (kC - 1));
+                const bool self_here = colA == self_c0;
+                auto quarter = [&](const uint32_t (&sq)[16], int hq) {
                     uint32_t pk[8];
-                    l += softmax_quarter<F16>(sq, csb[h] + 16 * hq, vmb[h] >> (16 * hq), m2, pk);
-                    if (cc == self_c0) {
+                    l += softmax_quarter<F16>(sq, cs0 + 16 * hq, vm0 >> (16 * hq), m2, pk);
+                    if (self_here) {
                         // a row with no key but itself: weight 1 on its own column (all
                         // its other columns are masked).  Selects, not a conditional store
                         // into pk, which would move pk to local memory.
@@ -690,34 +694,27 @@ lsh_attn_tc_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *__
 #pragma unroll
                         for (int k = 0; k < 8; ++k) pk[k] = k == kself ? one : pk[k];
                     }
-                    tmem_st8(sbase + cc + 8 * hq, pk);
+                    tmem_st8(sbase + colA + 8 * hq, pk);
                 };
-                uint32_t qa[16], qb[16];
                 if (nb0) {
+                    uint32_t qa[16], qb[16];
                     tmem_ld16(sbase + colA, qa);
-                    tmem_wait_ld16(qa);
                     tmem_ld16(sbase + colA + 16, qb);
+                    tmem_wait_ld16(qa);
+                    tmem_tie16(qb);
                     quarter(qa, 0);
-                    tmem_wait_ld16(qb);
+                    quarter(qb, 1);
                 } else {
                     tmem_st16_zero(sbase + colA);
-                }
-                if (nb1) tmem_ld16(sbase + colA + 32, qa);
-                if (nb0) quarter(qb, 1);
-                if (nb1) {
-                    tmem_wait_ld16(qa);
-                    tmem_ld16(sbase + colA + 48, qb);
-                    quarter(qa, 2);
-                    tmem_wait_ld16(qb);
-                    quarter(qb, 3);
-                } else {
-                    tmem_st16_zero(sbase + colA + 32);
                 }
                 if (self_here && self_only) l = 1.f;
                 LSH_SPAN_END(t_sm, 0x781);
                 LSH_SPAN_BEGIN(t_tail);
-                tmem_st16_zero(sbase + colZ);
-                l_part[ctr % kLBufs][half][i] = l;
+                {
+                    const uint32_t z8[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                    tmem_st8(sbase + colZ, z8);
+                }
+                l_part[ctr % kLBufs][part][i] = l;
                 tmem_wait_st();
                 fence_before_sync();
                 mbar_arrive(&sb.p_full[b]);

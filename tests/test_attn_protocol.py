@@ -29,7 +29,7 @@ import pytest
 
 SLOTS = 6           # chunk ring
 COPY_WARPS = 5      # row copiers (plus one metadata warp)
-SOFTMAX = 2         # softmax warps modelled (the kernel has 8; all run the same program)
+SOFTMAX = 2         # softmax warps modelled (the kernel has 16; all run the same program)
 
 
 class Barrier:
