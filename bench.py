@@ -848,7 +848,9 @@ def run_knn(args, w):
     wk = work_knn(w, k)
     F = sum(x["flops"] for x in wk.values())
     Bts = sum(x["bytes"] for x in wk.values())
-    t_roof = max(F / (peaks["bf16_tflops"] * 1e12), Bts / (peaks["hbm_gbs"] * 1e9))
+    # the similarity tiles run on the tensor cores for 16-bit inputs, the fp32 lanes else
+    peak_c = peaks["bf16_tflops"] if COMPUTE_UNIT[w.dtype] == "tensor" else FP32_ALU_TFLOPS
+    t_roof = max(F / (peak_c * 1e12), Bts / (peaks["hbm_gbs"] * 1e9))
     line = {
         "metric": METRIC_KNN, "value": job_value(w.tokens, world, ms_max), "unit": "tokens/s",
         "n_gpus": world, "steps": K, "warmup": Wm, "ms_per_step": ms_max,
