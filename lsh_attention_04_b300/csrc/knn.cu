@@ -32,8 +32,8 @@ namespace {
 
 using namespace nvcuda;
 
-constexpr int kKnnWarps = 8;
-constexpr int kRowsInFlight = 4;       // rows a warp selects for at once (independent chains)
+constexpr int kKnnWarps = 16;
+constexpr int kRowsInFlight = 2;       // rows a warp selects for at once (independent chains)
 constexpr int kWinMax = 128;           // window rows: two chunks of at most 64
 constexpr int kSPitch = kWinMax + 4;   // fp32 similarity tile row pitch
 
