@@ -355,8 +355,8 @@ cudaError_t knn_launch(const Problem &p, int k, const void *qk, const int32_t *b
                       : launch_round<float, 128>(p, k, qk, buckets, perm, inv_norm, cand_idx, cand_sim, st);
     if (e != cudaSuccess) return e;
     const long n = p.n_tok();
-    const unsigned g4 = (unsigned)((n + 31) / 32);          // 8 warps x 4 tokens per CTA
-    knn_merge_kernel<4><<<g4, 256, 0, st>>>(cand_idx, cand_sim, n, p.L, p.n_rounds, k, nn_idx, nn_sim);
+    const unsigned g2 = (unsigned)((n + 15) / 16);          // 8 warps x 2 tokens per CTA
+    knn_merge_kernel<2><<<g2, 256, 0, st>>>(cand_idx, cand_sim, n, p.L, p.n_rounds, k, nn_idx, nn_sim);
     return cudaGetLastError();
 }
 
