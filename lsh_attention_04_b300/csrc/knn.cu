@@ -17,7 +17,7 @@
 //      same-bucket candidates: 64-bit keys (similarity, then smaller index) sorted in
 //      32-entry blocks by a bitonic network across the lanes and the blocks' top 32
 //      merged.  Lists go to a per-round buffer at the token's position.
-//   2. knn_merge_kernel, four tokens per warp: the rounds' sorted lists folded in one at a
+//   2. knn_merge_kernel, two tokens per warp: the rounds' sorted lists folded in one at a
 //      time by the bitonic top-32 merge; a token found in several rounds has the same key
 //      in each (the same similarity by the same arithmetic), so before each fold the list
 //      drops the keys the running result already holds.
