@@ -49,9 +49,9 @@
 // one warp's cp.async stream manages about 5-10.)  So every chunk is filled by several
 // loader warps at once.  The MMA warps fence the async proxy after each wait, since the
 // rows were written through the generic one.
-// Warp roles (24 warps, 80 registers each): 0-15 softmax + output epilogue (warps w, w+4,
+// Warp roles (28 warps, 72 registers each): 0-15 softmax + output epilogue (warps w, w+4,
 // w+8 and w+12 share TMEM lane quarter w and split the row's columns and O's columns four
-// ways), 16 the metadata warp, 17-21 row copiers, 22 S issuer and TMEM owner, 23 P V issuer.
+// ways), 16 the metadata warp, 17-25 row copiers, 26 S issuer and TMEM owner, 27 P V issuer.
 // Persistent CTAs take contiguous ranges of tiles of a group of heads small enough for
 // L2, so all rounds of those heads share cached rows.  Every wait is bounded
 // (sm100::wait); on a timeout the kernel records where in the workspace status block and
@@ -70,7 +70,7 @@ constexpr int kRows = 128;        // rows per tile
 constexpr int kWin = 192;         // S columns per tile (window rows)
 constexpr int kSlots = 6;         // chunk ring (even: chunk parity = slot parity)
 constexpr int kSmWarps = 16;      // softmax / epilogue warps (4 per TMEM lane quarter)
-constexpr int kLoaders = 6;       // loader warps: 1 metadata warp + kCopyWarps row copiers
+constexpr int kLoaders = 10;      // loader warps: 1 metadata warp + kCopyWarps row copiers
 constexpr int kCopyWarps = kLoaders - 1;
 constexpr int kSWarp = kSmWarps + kLoaders;
 constexpr int kPvWarp = kSWarp + 1;
@@ -279,7 +279,7 @@ lsh_attn_tc_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *__
     if (warp >= kSmWarps && warp < kSmWarps + kLoaders) {
         // ------------------------------------------------------------- loaders
         // Every chunk is filled by all loader warps together, so a chunk lands in about a
-        // fifth of the time one warp's cp.async stream needs (the ring cannot hold more
+        // ninth of the time one warp's cp.async stream needs (the ring cannot hold more
         // chunks in flight).  Warp kSmWarps is the metadata warp (row metadata); the copy
         // warps copy the Q/K and V rows.  Every loader waits for the slot itself and
         // takes part in every fill of every slot, in order, so no warp can fall a phase

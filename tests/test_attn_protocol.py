@@ -28,7 +28,7 @@ import random
 import pytest
 
 SLOTS = 6           # chunk ring
-COPY_WARPS = 5      # row copiers (plus one metadata warp)
+COPY_WARPS = 9      # row copiers (plus one metadata warp)
 SOFTMAX = 2         # softmax warps modelled (the kernel has 16; all run the same program)
 
 
