@@ -389,9 +389,12 @@ cudaError_t launch_tc(const Problem &p, const void *qk, const void *v, const int
 // a column d) and split the columns four ways; warp 4 also issues the MMAs and owns TMEM;
 // all sixteen gather.
 // A row's keys are one interval of the window (its bucket run, clipped to its window, and
-// before it when causal), from run bounds computed once per tile.  One mbarrier takes the first two commits
-// (phase 1, then dQ: waited with parities 0 and 1 by warps that saw the one before), a
-// second the last (phase 2: every MMA of the CTA), so no wait can alias a phase.
+// before it when causal), from run bounds computed once per unit.  One mbarrier takes a
+// unit's first two commits (phase 1, then dQ: waited with parities 0 and 1 by warps that
+// saw the one before), a second its last (phase 2: every MMA of the unit, waited with the
+// unit's count mod 2), so no wait can alias a phase.  The next unit's permutation entries
+// and row metadata are fetched (4-byte cp.async) while the current one computes.
+
 // 2^x by the special-function unit (relative error near 2^-22).  Results below 2^-126
 // flush to 0: the weights here are a token's softmax weights over the keys of all its
 // rounds (their total is 1), so a flushed one is below 2^-126 of that total.
