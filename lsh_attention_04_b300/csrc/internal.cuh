@@ -90,6 +90,11 @@ cudaError_t sort_launch(const Problem &p, const int32_t *buckets, int32_t *perm,
 cudaError_t attn_simt(const Problem &p, const void *qk, const void *v, const int32_t *buckets,
                       const int32_t *perm, const int32_t *bstart, const float *inv_norm,
                       void *o_r, float *lse_r, cudaStream_t st);
+// chunk 128 on the tensor cores (bf16 / fp16, d = 128, L a multiple of 128)
+bool attn_c128_supported(const Problem &p);
+cudaError_t attn_c128(const Problem &p, const void *qk, const void *v, const int32_t *buckets,
+                      const int32_t *perm, const float *inv_norm, void *o_r, float *lse_r,
+                      StatusBlock *status, cudaStream_t st);
 bool attn_tc_supported(const Problem &p);
 cudaError_t attn_tc(const Problem &p, const void *qk, const void *v, const int32_t *buckets,
                     const int32_t *perm, const int32_t *bstart, const float *inv_norm, void *o_r,

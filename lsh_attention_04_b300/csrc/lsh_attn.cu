@@ -89,6 +89,9 @@ lsh_status_t run_attn(const Problem &p, const void *qk, const void *v, const int
                       const int32_t *perm, const int32_t *bstart, const float *inv_norm,
                       void *o_r, float *lse_r, void *ws, cudaStream_t st)
 {
+    if (attn_c128_supported(p))
+        return cuda_status(attn_c128(p, qk, v, buckets, perm, inv_norm, o_r, lse_r,
+                                     (StatusBlock *)ws, st));
     if (attn_tc_supported(p))
         return cuda_status(attn_tc(p, qk, v, buckets, perm, bstart, inv_norm, o_r, lse_r,
                                    (StatusBlock *)ws, st));

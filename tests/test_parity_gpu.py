@@ -37,8 +37,10 @@ SMALL = [
     # (L = 1056 is not a multiple of 64)
     W("bf16_chunk32_L2048_d128_noncausal", 1, 2, 2048, 128, "bf16", 64, 3, 32, False, 32, 23),
     W("bf16_chunk32_L1056_d64_simt", 1, 1, 1056, 64, "bf16", 32, 2, 32, True, 16, 24),
-    # chunk 128 (CUDA cores; 16-bit staged rows at d = 128)
+    # chunk 128: tensor cores at d = 128 with L a multiple of 128, CUDA cores otherwise
+    # (16-bit staged rows at d = 128)
     W("bf16_chunk128_L1024_d64", 1, 2, 1024, 64, "bf16", 16, 2, 128, True, 8, 25),
+    W("bf16_chunk128_L2048_d128_R3", 1, 2, 2048, 128, "bf16", 32, 3, 128, True, 16, 29),
     W("bf16_chunk128_L1024_d128_noncausal", 1, 1, 1024, 128, "bf16", 16, 2, 128, False, 8, 26),
     W("f32_chunk128_L512_d64", 1, 1, 512, 64, "f32", 8, 2, 128, True, 0, 27),
     W("f16_chunk128_L768_d128", 1, 1, 768, 128, "f16", 16, 3, 128, True, 8, 28),
@@ -400,6 +402,10 @@ BOUND_CASES = [
     # exact maximum past it
     (W("bound_f16_m2_4_10", 1, 2, 1024, 64, "f16", 16, 2, 64, True, 0, 46), 4.0, 10.0),
     (W("bound_f16_m2_10_20_d128", 1, 2, 1024, 128, "f16", 16, 1, 64, True, 0, 47), 10.0, 20.0),
+    # the chunk-128 tensor-core kernel: both paths, bf16 and fp16 weights
+    (W("bound_bf16_m2_55_70_d128_chunk128_noncausal", 1, 1, 1024, 128, "bf16", 16, 1, 128, False, 0, 48),
+     55.0, 70.0),
+    (W("bound_f16_m2_4_10_d128_chunk128", 1, 2, 1024, 128, "f16", 16, 1, 128, True, 0, 49), 4.0, 10.0),
 ]
 
 
@@ -426,7 +432,8 @@ def test_softmax_bound_extremes(w, lo, hi):
 # Every workload: the three small-to-image ones and all 24 points of the length sweep.
 FULL_ALL = ["gauss_f32_B1_H1_L1024_d64", "clustered_B8_H8_L4096_d64_R4",
             "image_B8_H8_L12288_d128_R8", "long_B1_H8_L65536_d128_R8",
-            "long_f16_B1_H8_L65536_d128_R8", "long_chunk32_B1_H8_L65536_d128_R8"] + \
+            "long_f16_B1_H8_L65536_d128_R8", "long_chunk32_B1_H8_L65536_d128_R8",
+            "long_chunk128_B1_H8_L65536_d128_R8"] + \
     sorted(n for n in gen.WORKLOADS if n.startswith("sweep_"))
 FULL = ["gauss_f32_B1_H1_L1024_d64", "clustered_B8_H8_L4096_d64_R4", "image_B8_H8_L12288_d128_R8",
         "long_B1_H8_L65536_d128_R8", "sweep_B128_H8_L1024_d64_R8", "sweep_B4_H8_L32768_d64_R8",
