@@ -84,7 +84,8 @@ typedef enum {
  * Supported range (anything else returns LSH_ERR_UNSUPPORTED):
  *   d in {64, 128};  chunk in {32, 64, 128};  2 <= n_buckets <= 2048;
  *   chunk 128: the forward pass and the staged steps only (lsh_attn_backward and lsh_knn
- *   return LSH_ERR_UNSUPPORTED), on the CUDA cores, and not for LSH_F32 at d = 128;
+ *   return LSH_ERR_UNSUPPORTED); on the tensor cores for 16-bit inputs at d = 128 with
+ *   L % 128 == 0, on the CUDA cores otherwise, and not for LSH_F32 at d = 128;
  *   n_buckets % 16 == 0 for LSH_BF16 and LSH_F16;  B*H*n_rounds*L < 2^31.
  */
 
