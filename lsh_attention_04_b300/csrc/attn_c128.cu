@@ -29,8 +29,9 @@
 // Persistent CTAs of 16 warps, one per SM, take the units in turn and run each one's
 // gather, S, softmax, P V and epilogue in sequence: warps w, w+4, w+8 and w+12 share TMEM
 // lane quarter w (32 query rows) and split the 256 key columns and the 128 output columns
-// four ways; warp 0 also issues the MMAs and owns TMEM.  Every wait is bounded
-// (sm100::wait).
+// four ways; warp 0 also issues the MMAs and owns TMEM.  The next unit's permutation
+// entries and row metadata are fetched (4-byte cp.async) while the current one computes.
+// Every wait is bounded (sm100::wait).
 #include <limits.h>
 #include <math.h>
 
@@ -129,6 +130,9 @@ lsh_attn_c128_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *
     __shared__ uint64_t bar_s, bar_o;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag_s;
+    // the next unit's permutation entries and row metadata, fetched while this one computes
+    __shared__ int nx_tok[kWin], nx_bkt[kWin];
+    __shared__ float nx_kin[kWin];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     C128Meta &mt = *reinterpret_cast<C128Meta *>(sm + kOffMeta);
     volatile int *abort_flag = &abort_flag_s;
@@ -164,11 +168,15 @@ lsh_attn_c128_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *
         const size_t head = (size_t)bh * L;
         const int32_t *Pm = perm + seg * L;
         const int w0 = kC * (t - 1);               // sorted index of window row 0
+        const long un = u + gridDim.x;             // this CTA's next unit
+        const long seg2 = un / tpc;
+        const int t2 = (int)(un - seg2 * tpc);
+        const bool pre = it > 0;                   // this unit's metadata was prefetched
 
         // ---- 1. the window's permutation entries, then its rows and row metadata
         for (int w = threadIdx.x; w < kWin; w += kThreads) {
             const int s = w0 + w;
-            const int j = s >= 0 ? Pm[s] : INT_MAX;
+            const int j = s >= 0 ? (pre ? nx_tok[w] : Pm[s]) : INT_MAX;
             mt.tok[w] = s >= 0 ? ((unsigned)j < (unsigned)L ? j : 0) : INT_MAX;
         }
         __syncthreads();
@@ -188,8 +196,8 @@ lsh_attn_c128_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *
             const int j = mt.tok[w];
             const bool present = j != INT_MAX;
             const int jj = present ? j : 0;
-            const float kn = present ? inv_norm[head + jj] : 0.f;
-            mt.bkt[w] = present ? buckets[seg * L + jj] : -1;
+            const float kn = present ? (pre ? nx_kin[w] : inv_norm[head + jj]) : 0.f;
+            mt.bkt[w] = present ? (pre ? nx_bkt[w] : buckets[seg * L + jj]) : -1;
             mt.kcs[w] = cscale * kn;
             if (w >= kC) mt.m2[w - kC] = kn > 0.f ? ascale / kn : 0.f;
         }
@@ -246,6 +254,12 @@ lsh_attn_c128_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *
         };
         bool ok = __all_sync(FULL, wait(&bar_s, it & 1, abort_flag, status, 0xc01));
         fence_after_sync();
+        // the next unit's permutation entries (this thread's window row), in flight until
+        // the epilogue
+        if (un < n_units && threadIdx.x < kWin) {
+            const int s2 = kC * (t2 - 1) + (int)threadIdx.x;
+            if (s2 >= 0) cp_async4(smem_u32(&nx_tok[threadIdx.x]), perm + seg2 * L + s2);
+        }
 
         // ---- 3. softmax over this warp's 64 columns; P over S
         if (ok) {
@@ -315,6 +329,18 @@ lsh_attn_c128_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *
             mma_commit(smem_u32(&bar_o));
         }
 
+        // the next unit's row metadata, from its permutation entries (landed by now)
+        if (un < n_units && threadIdx.x < kWin) {
+            const int w = threadIdx.x, s2 = kC * (t2 - 1) + w;
+            cp_async_wait_all();
+            if (s2 >= 0) {
+                int j = nx_tok[w];
+                j = (unsigned)j < (unsigned)L ? j : 0;
+                cp_async4(smem_u32(&nx_bkt[w]), buckets + seg2 * L + j);
+                cp_async4(smem_u32(&nx_kin[w]), inv_norm + (size_t)(seg2 / n_rounds) * L + j);
+            }
+        }
+
         // ---- 5. epilogue: O / l in 16 bits, lse
         if (ok) {
             ok = __all_sync(FULL, wait(&bar_o, it & 1, abort_flag, status, 0xc02));
@@ -339,7 +365,9 @@ lsh_attn_c128_kernel(const __nv_bfloat16 *__restrict__ qk, const __nv_bfloat16 *
             if (part == 0) lse_r[orow] = self_only ? kSelfLogit : (m2 + __log2f(lt)) * kLn2;
         }
         // the next unit overwrites the tiles, the metadata and TMEM: every thread is done
-        // with them (and a failed wait anywhere ends the loop for the whole CTA)
+        // with them, and its prefetched metadata has landed (a failed wait anywhere ends
+        // the loop for the whole CTA)
+        cp_async_wait_all();
         fence_before_sync();
         failed = __syncthreads_or(!ok) != 0;
         fence_after_sync();
